@@ -1,0 +1,104 @@
+// Host-side internals of libar_gb300.so: the handle, the launch plan and the
+// per-file launchers.  Not part of the C-ABI (that is include/ar.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <type_traits>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ar.h"
+
+namespace argb {
+
+constexpr int kMaxRanks = 16;
+constexpr int kThreads = 256;  // threads per CTA of the streaming kernels
+
+struct DevStatus;
+
+// Optional per-launch timing (AR_OPT_TIMING): a ring of event pairs created
+// when the option is set; recording costs two cudaEventRecord calls per
+// launch and allocates nothing.
+struct Timing {
+    int capacity = 0;
+    std::vector<cudaEvent_t> start, stop;
+    std::vector<ar_launch_time_t> rec;
+    size_t head = 0, count = 0;
+    int op = 0;  // the call being recorded
+};
+
+struct Handle {
+    int n = 0;
+    size_t max_bytes = 0;
+    int device = 0;
+    int sm_count = 0;
+    int ctas_per_sm = 8;
+    int64_t spin_ns = 1000000;
+    int one_shot_impl = 0;
+    float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
+    size_t ring_chunk_max = 0;      // elements
+    DevStatus* status = nullptr;    // device
+    cudaStream_t last_stream = nullptr;
+    ar_traffic_t last{};
+    Timing timing;
+};
+
+// Bracket one launch with the timing events (no-ops when timing is off).
+inline void rec_begin(Handle& h, cudaStream_t s)
+{
+    Timing& t = h.timing;
+    if (t.capacity) cudaEventRecord(t.start[t.head], s);
+}
+
+inline void rec_end(Handle& h, cudaStream_t s, int kernel, uint64_t hbm_bytes)
+{
+    Timing& t = h.timing;
+    if (!t.capacity) return;
+    cudaEventRecord(t.stop[t.head], s);
+    t.rec[t.head] = ar_launch_time_t{kernel, t.op, 0.0f, hbm_bytes};
+    t.head = (t.head + 1) % (size_t)t.capacity;
+    if (t.count < (size_t)t.capacity) ++t.count;
+}
+
+inline size_t elem_bytes(int dt) { return dt == AR_F32 ? 4u : 2u; }
+
+// Two-shot / ring chunk: ceil(N/n) rounded up to a whole 16-byte vector.
+inline size_t chunk_elems(int n, size_t N, int dt)
+{
+    size_t per = (N + (size_t)n - 1) / (size_t)n;
+    size_t q = 16u / elem_bytes(dt);
+    return (per + q - 1) / q * q;
+}
+
+// CTAs for a streaming kernel that needs `work` thread-iterations.
+inline unsigned grid_for(const Handle& h, size_t work)
+{
+    size_t want = (work + kThreads - 1) / kThreads;
+    size_t cap = (size_t)h.sm_count * (size_t)h.ctas_per_sm;
+    if (want > cap) want = cap;
+    return want ? (unsigned)want : 1u;
+}
+
+// Launchers: argument checks are done by the caller; these only launch.
+int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                    cudaStream_t s, int* launches);
+int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                    cudaStream_t s, int* launches);
+int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                cudaStream_t s, int* launches);
+int launch_ll_pack(Handle& h, const float* src, void* lines, size_t count, uint32_t step,
+                   cudaStream_t s);
+int launch_ll_unpack(Handle& h, const void* lines, float* dst, size_t count, uint32_t step,
+                     cudaStream_t s);
+int launch_ll_reduce(Handle& h, const void* const* in, void* const* out, size_t count,
+                     uint32_t step, cudaStream_t s);
+int launch_ll128_pack(Handle& h, const float* src, void* lines, size_t count, uint64_t step,
+                      cudaStream_t s);
+int launch_ll128_unpack(Handle& h, const void* lines, float* dst, size_t count, uint64_t step,
+                        cudaStream_t s);
+int launch_ll128_reduce(Handle& h, const void* const* in, void* const* out, size_t count,
+                        uint64_t step, cudaStream_t s);
+
+}  // namespace argb

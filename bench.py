@@ -1,0 +1,558 @@
+#!/usr/bin/env python3
+"""Benchmark of the emulated sum all-reduce on one GB300 (per GPU).
+
+Metric: all-reduce HBM GB/s (algorithmic bytes / device time), and its
+fraction of the measured HBM peak, n = 8 ranks, bf16.
+
+One step = one pass of every row of the hot path over one batch:
+  batch   n = 8 rank buffers of S = 64 MiB bf16, N(0,1) (the prefill
+          workload's largest size: 4096 tokens x hidden 8192), plus n = 8
+          fp32 payloads of 1 MiB, U[-1,1] (the LL workload's largest size)
+  rows    one-shot, two-shot (reduce-scatter + all-gather) and the
+          2(n-1)-step ring over the bf16 batch; LL and LL128 pack ->
+          flag-checked reduce -> unpack over the fp32 payloads (fresh step id
+          per pass).  Argument checks and planning run inside every call.
+`value` = all algorithmic HBM bytes of K steps on all ranks / max-over-ranks
+device time.  The 1.3 GiB per-step working set is 10x the 129 MB L2, so no
+flush is needed between steps.  Per-kernel times come from the library's
+own launch record (CUDA events on the launching stream, AR_OPT_TIMING).
+
+--impl reference times the CPU oracle instead (the reference arm), on a
+bounded sample of the same workload.  Multi-GPU runs (torchrun) are
+independent replicas: the path has no exchange between GPUs.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+MiB = 1 << 20
+METRIC = "all-reduce HBM GB/s & % of GB300 HBM peak vs msg size, n=8 bf16"
+NOMINAL_PEAK_GBS = 8000.0        # the ~8 TB/s HBM3e figure the target is stated against
+FALLBACK_PEAK_GBS = 6800.0       # profiling recipe fallback when no measured peak is present
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas: a barrier and max/sum of scalars only)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def reduce_scalar(x: float, op: str = "max") -> float:
+    """max / sum of a host scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# workload bookkeeping
+# --------------------------------------------------------------------------
+
+def step_bytes(n: int, N: int, e: int, ll_count: int) -> dict:
+    """Algorithmic HBM bytes of every row of one step, from the library's plan."""
+    import all_reduce_reduction_rank_gb300 as ar
+    rows = {}
+    for name, op in (("one_shot", ar.AR_OP_ONE_SHOT), ("two_shot", ar.AR_OP_TWO_SHOT), ("ring", ar.AR_OP_RING)):
+        t = ar.ar_plan(op, n, N, {4: "f32", 2: "bf16"}[e])
+        rows[name] = t.hbm_read_bytes + t.hbm_write_bytes
+    for kind, (pk, rd, up) in (("ll", (ar.AR_OP_LL_PACK, ar.AR_OP_LL_REDUCE, ar.AR_OP_LL_UNPACK)),
+                               ("ll128", (ar.AR_OP_LL128_PACK, ar.AR_OP_LL128_REDUCE, ar.AR_OP_LL128_UNPACK))):
+        b = 0
+        for op, k in ((pk, n), (rd, 1), (up, n)):
+            t = ar.ar_plan(op, n, ll_count, "f32")
+            b += k * (t.hbm_read_bytes + t.hbm_write_bytes)
+        rows[kind] = b
+    return rows
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, read+write bytes)"
+    except Exception:
+        return FALLBACK_PEAK_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+KERNEL_SOURCES = {
+    "one_shot": ["one_shot.cu"], "reduce_scatter": ["two_shot.cu"], "all_gather": ["two_shot.cu"],
+    "ring_rs_step": ["ring.cu"], "ring_ag_step": ["ring.cu"],
+    "ll_pack": ["ll.cu"], "ll_unpack": ["ll.cu"], "ll_reduce": ["ll.cu"],
+    "ll128_pack": ["ll.cu"], "ll128_unpack": ["ll.cu"], "ll128_reduce": ["ll.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    csrc = os.path.join(ROOT, "all_reduce_reduction_rank_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel] + ["common.cuh", "internal.h"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str, bytes_per_launch: float):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    launch by algorithmic bytes; None when there is none or the kernel's
+    source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    scale = bytes_per_launch / float(rec["algorithmic_bytes_per_launch"])
+    return float(rec["dram_bytes_per_launch"]) * scale
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, bus_id: int | None):
+        self.bus_id = bus_id
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5:   # wait for the first sample
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict | None:
+        if not self.rows:
+            return None
+        rows = [r for t, r in self.rows if len(r) >= 10]
+        if self.bus_id is not None:
+            mine = [r for r in rows if _bus_number(r[1]) == self.bus_id]
+            rows = mine or rows
+        timed = [r for (t, r) in self.rows if t0 <= t <= t1 and r in rows]
+        use = timed if len(timed) >= 1 else rows
+        sm = [float(r[2]) for r in use if _isnum(r[2])]
+        mx = [float(r[3]) for r in use if _isnum(r[3])]
+        reasons = sorted({name for r in use for name, v in zip(self.REASONS, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "in_timed_region": len(timed),
+                "power_w_max": max((float(r[4]) for r in use if _isnum(r[4])), default=None)}
+
+
+def _isnum(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+def _bus_number(bus_id: str):
+    try:
+        return int(bus_id.split(":")[-2], 16)
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+class Workload:
+    """Device buffers of one batch and the pre-marshalled C-ABI calls of a step."""
+
+    def __init__(self, n: int, S: int, ll_count: int, dev, seed: int):
+        import ctypes
+
+        import torch
+
+        import all_reduce_reduction_rank_gb300 as ar
+        import workloads
+
+        self.n, self.S, self.N, self.ll_count, self.dev = n, S, S // 2, ll_count, dev
+        self.ins = workloads.rank_inputs_device(n, self.N, "bf16", "normal", seed, device=dev)
+        self.outs = [torch.empty_like(t) for t in self.ins]
+        self.pay = workloads.rank_inputs_device(n, ll_count, "f32", "uniform", seed + 1, device=dev)
+        lb, l128 = ar.ar_ll_bytes(4 * ll_count), ar.ar_ll128_bytes(4 * ll_count)
+        mk = lambda nb: [torch.zeros(nb, dtype=torch.uint8, device=dev) for _ in range(n)]
+        self.ll_lines, self.ll_red, self.l128_lines, self.l128_red = mk(lb), mk(lb), mk(l128), mk(l128)
+        self.ll_dst = [torch.zeros(ll_count, dtype=torch.float32, device=dev) for _ in range(n)]
+        self.l128_dst = [torch.zeros(ll_count, dtype=torch.float32, device=dev) for _ in range(n)]
+        self.h = ar.ar_create(n, S)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.s = ctypes.c_void_p(self.stream.cuda_stream)
+        P = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+        self.p_in, self.p_out = P(self.ins), P(self.outs)
+        self.p_ll, self.p_llr = P(self.ll_lines), P(self.ll_red)
+        self.p_l128, self.p_l128r = P(self.l128_lines), P(self.l128_red)
+        self.L = ar.lib()
+        self.step_id = 0
+        self.launches_per_step = 1 + 2 + 2 * (n - 1) + 2 * (2 * n + 1)
+
+    def run(self):
+        L, h, s, n, N, c = self.L, self.h, self.s, self.n, self.N, self.ll_count
+        self.step_id += 1
+        k = self.step_id
+        rc = L.ar_one_shot(h, self.p_in, self.p_out, N, 1, s)
+        rc |= L.ar_two_shot(h, self.p_in, self.p_out, N, 1, s)
+        rc |= L.ar_ring(h, self.p_in, self.p_out, N, 1, s)
+        for r in range(n):
+            rc |= L.ar_ll_pack(h, self.pay[r].data_ptr(), self.ll_lines[r].data_ptr(), c, k, s)
+        rc |= L.ar_ll_reduce(h, self.p_ll, self.p_llr, c, k, s)
+        for r in range(n):
+            rc |= L.ar_ll_unpack(h, self.ll_red[r].data_ptr(), self.ll_dst[r].data_ptr(), c, k, s)
+        for r in range(n):
+            rc |= L.ar_ll128_pack(h, self.pay[r].data_ptr(), self.l128_lines[r].data_ptr(), c, k, s)
+        rc |= L.ar_ll128_reduce(h, self.p_l128, self.p_l128r, c, k, s)
+        for r in range(n):
+            rc |= L.ar_ll128_unpack(h, self.l128_red[r].data_ptr(), self.l128_dst[r].data_ptr(), c, k, s)
+        if rc:
+            raise RuntimeError(f"a C-ABI call failed in step {k}")
+
+    def close(self):
+        import all_reduce_reduction_rank_gb300 as ar
+        ar.check(ar.ar_destroy(self.h), "ar_destroy")
+
+
+def time_steps(wl, K: int) -> float:
+    """Device ms of exactly K steps, bracketed by a barrier + synchronize."""
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(wl.stream)
+    for _ in range(K):
+        wl.run()
+    ev1.record(wl.stream)
+    torch.cuda.synchronize()
+    barrier()
+    return ev0.elapsed_time(ev1)
+
+
+def per_kernel(records, K: int, peak: float) -> dict:
+    agg = {}
+    for name, _op, ms, b in records:
+        a = agg.setdefault(name, {"launches": 0, "ms": 0.0, "bytes": 0})
+        a["launches"] += 1
+        a["ms"] += ms
+        a["bytes"] += b
+    total = sum(a["ms"] for a in agg.values()) or 1.0
+    out = {}
+    for name, a in agg.items():
+        gbs = a["bytes"] / (a["ms"] * 1e-3) / 1e9 if a["ms"] > 0 else None
+        out[name] = {"launches_per_step": a["launches"] / K, "us_per_launch": 1e3 * a["ms"] / a["launches"],
+                     "bytes_per_launch": a["bytes"] / a["launches"], "GB/s": gbs,
+                     "frac_of_peak": gbs / peak if gbs else None, "share": a["ms"] / total}
+    return out
+
+
+def sweep(wl, peak: float, iters_small: int = 200, iters_large: int = 50) -> dict:
+    """one-shot and two-shot over the decode and prefill message sizes (n = 8,
+    bf16): per size the median of CUDA-event-timed calls, L2 flushed (a
+    256 MiB write) before every call, outside the timed interval."""
+    import torch
+
+    import all_reduce_reduction_rank_gb300 as ar
+    import workloads
+
+    flush = torch.empty(256 * MiB, dtype=torch.uint8, device=wl.dev)
+    sizes = sorted({2 * c for c in workloads.CONFIGS[2]["counts"]} | {2 * c for c in workloads.CONFIGS[3]["counts"]})
+    res = {"one_shot": [], "two_shot": []}
+    n = wl.n
+    for S in sizes:
+        if S > wl.S:
+            continue
+        N = S // 2
+        iters = iters_small if S <= MiB else iters_large
+        for algo, call, op in (("one_shot", wl.L.ar_one_shot, ar.AR_OP_ONE_SHOT),
+                               ("two_shot", wl.L.ar_two_shot, ar.AR_OP_TWO_SHOT)):
+            t = ar.ar_plan(op, n, N, "bf16")
+            b = t.hbm_read_bytes + t.hbm_write_bytes
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            with torch.cuda.stream(wl.stream):
+                for e0, e1 in evs:
+                    flush.fill_(0x5A)
+                    e0.record(wl.stream)
+                    ar.check(call(wl.h, wl.p_in, wl.p_out, N, 1, wl.s), algo)
+                    e1.record(wl.stream)
+            torch.cuda.synchronize()
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+            gbs = b / (ms * 1e-3) / 1e9
+            algbw = S / (ms * 1e-3) / 1e9
+            res[algo].append({"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
+                              "busbw_GB/s": round(algbw * 2 * (n - 1) / n, 1), "iters": iters})
+    del flush
+    return res
+
+
+def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
+    """The same step through the public API with HOST buffers: every step
+    copies its inputs from pinned host memory, runs, and reads its results
+    (the n all-reduced buffers and the n LL and LL128 unpacked payloads) back."""
+    import torch
+    n = wl.n
+    h_in = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.ins]
+    h_pay = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.pay]
+    for h, d in zip(h_in + h_pay, wl.ins + wl.pay):
+        h.copy_(d)
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.outs]
+    h_ll = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.ll_dst + wl.l128_dst]
+    h2d = sum(t.numel() * t.element_size() for t in h_in + h_pay)
+    d2h = sum(t.numel() * t.element_size() for t in h_out + h_ll)
+
+    def one():
+        with torch.cuda.stream(wl.stream):
+            for h, d in zip(h_in + h_pay, wl.ins + wl.pay):
+                d.copy_(h, non_blocking=True)
+            wl.run()
+            for h, d in zip(h_out + h_ll, wl.outs + wl.ll_dst + wl.l128_dst):
+                h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(wl.stream)
+    for _ in range(K):
+        one()
+    ev1.record(wl.stream)
+    torch.cuda.synchronize()
+    ms = reduce_scalar(ev0.elapsed_time(ev1), "max") / K
+    world = dist_env()[1]
+    return {"value": round(world * bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_ours(args):
+    import torch
+
+    import all_reduce_reduction_rank_gb300 as ar
+
+    rank, world = dist_init("nccl")
+    local = dist_env()[2]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ar.lib()                                   # fails loudly if the library is not built
+    n, S, ll_count = 8, args.size_mib * MiB, (1 * MiB) // 4
+    wl = Workload(n, S, ll_count, dev, seed=1003)
+    peak, peak_src = measured_peak()
+    rows = step_bytes(n, wl.N, 2, ll_count)
+    bytes_step = sum(rows.values())
+    for _ in range(args.warmup):
+        wl.run()
+    torch.cuda.synchronize()
+    ar.check(ar.ar_status(wl.h), "warm-up status")
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_TIMING, min(1 << 20, wl.launches_per_step * args.steps)))
+
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    clocks = ClockSampler(bus)
+    clocks.start()
+    t_wall0 = time.time()
+    ms = time_steps(wl, args.steps)
+    t_wall1 = time.time()
+    clocks.stop()
+    records = ar.ar_timing(wl.h)
+    ar.check(ar.ar_status(wl.h), "timed-region status")
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_TIMING, 0))
+    ms_max = reduce_scalar(ms, "max")
+    total_bytes = reduce_scalar(bytes_step * args.steps, "sum")
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    kernels = per_kernel(records, args.steps, peak)
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    dk = kernels[dom]
+    traffic = ncu_traffic(dom, dk["bytes_per_launch"])
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dk["GB/s"], 1), "peak": peak, "unit": "GB/s",
+                "frac": round(dk["GB/s"] / peak, 4), "traffic": traffic,
+                "bytes_per_launch": dk["bytes_per_launch"], "peak_source": peak_src}
+
+    sw = sweep(wl, peak) if args.sweep else None
+    e2e = e2e_leg(wl, max(3, min(args.steps, args.e2e_steps)), bytes_step) if args.e2e else None
+    cpu = None
+    if world == 1 and rank == 0 and args.cpu_baseline:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+    wl.close()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"n8_bf16_S{args.size_mib}MiB_prefill+n8_f32_P1MiB_ll", "n_ranks": n,
+                   "bytes_per_rank": S, "payload": "bf16 N(0,1), fp32 accumulation",
+                   "ll_payload_bytes_per_rank": 4 * ll_count,
+                   "rows": ["one_shot", "two_shot", "ring", "ll(pack,reduce,unpack)", "ll128(pack,reduce,unpack)"],
+                   "bytes_per_step": bytes_step, "bytes_per_step_by_row": rows,
+                   "l2": "inputs larger than L2: 1.3 GiB touched per step vs 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_peak": round(value / world / peak, 4), "frac_of_8tbs": round(value / world / NOMINAL_PEAK_GBS, 4),
+        "roofline": roofline, "kernels": kernels, "gpu_launches": len(records),
+        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "sweep": sw,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host (CPU baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(scale_div: int, seed: int = 1003):
+    """The step's rows at 1/scale_div of the workload, run by the oracle."""
+    import oracle
+    import workloads
+    n = 8
+    N = (64 * MiB // 2) // scale_div
+    c = ((1 * MiB) // 4) // scale_div
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed)
+    ps = workloads.payload_f32(n, c, seed + 1)
+    rows = step_bytes(n, N, 2, c)
+
+    def run(step_id: int):
+        oracle.all_reduce(xs, "bf16")
+        oracle.all_gather(oracle.reduce_scatter(xs, "bf16"), "bf16")
+        oracle.ring(xs, "bf16")
+        red, _ = oracle.ll_reduce([oracle.ll_pack(p, step_id) for p in ps], c, step_id)
+        for r in red:
+            oracle.ll_unpack(r, c, step_id)
+        red, _ = oracle.ll128_reduce([oracle.ll128_pack(p, step_id) for p in ps], c, step_id)
+        for r in red:
+            oracle.ll128_unpack(r, c, step_id)
+
+    desc = f"oracle on n=8 bf16 {2 * N // 1024} KiB per rank + LL/LL128 {4 * c // 1024} KiB fp32 payloads (1/{scale_div} of the step)"
+    return run, sum(rows.values()), desc
+
+
+def cpu_baseline(seconds: float = 10.0, scale_div: int = 32) -> dict:
+    run, b, desc = oracle_sample(scale_div)
+    run(1)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run(2 + reps)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(reps * b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{desc}, {reps} passes in {dt:.1f} s, single-threaded C"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return                                   # rank 0 alone runs the reference arm
+    budget = args.reference_budget / max(1, args.steps + args.warmup)   # seconds per step
+    div = 1024
+    run, b, desc = oracle_sample(div)
+    t0 = time.perf_counter()
+    run(1)
+    t_small = time.perf_counter() - t0
+    while div > 8 and t_small * 2 <= budget:
+        div //= 2
+        t_small *= 2
+    run, b, desc = oracle_sample(div)
+    for i in range(args.warmup):
+        run(1 + i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run(1000 + i)
+    dt = time.perf_counter() - t0
+    value = args.steps * b / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"n8_bf16_S{args.size_mib}MiB_prefill+n8_f32_P1MiB_ll", "n_ranks": 8,
+                       "sample_scale": f"1/{div}"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--size-mib", type=int, default=64, help="bytes per rank of the bf16 batch, MiB")
+    p.add_argument("--no-sweep", dest="sweep", action="store_false")
+    p.add_argument("--no-e2e", dest="e2e", action="store_false")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--reference-budget", type=float, default=150.0,
+                   help="seconds the reference arm's warm-up + timed steps should take in all")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

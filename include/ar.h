@@ -1,0 +1,272 @@
+/*
+ * ar.h -- C-ABI of libar_gb300.so: the sum all-reduce of n ranks' buffers,
+ * emulated on one GB300 (sm_103a), the n ranks being n buffers in its HBM.
+ *
+ * What is computed (all entry points):
+ *   Every rank ends with the elementwise sum of all n ranks' buffers
+ *   (handbook chapter "多 GPU 与 NCCL", §集合通信, the all-reduce row).
+ *   Sums accumulate in fp32 and are rounded once, round-to-nearest-even, to
+ *   the payload type ("SGLang JIT custom all-reduce" notes, §4 "求和
+ *   (reduce_impl)").  One-shot, two-shot and the LL/LL128 reduce add the
+ *   ranks in rank order 0..n-1 starting from +0, so their outputs are
+ *   bit-identical to each other and on every rank (same notes, §4, last
+ *   paragraph).  The ring adds chunk c in the order c, c+1, ..., c+n-1.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named in/out/src/dst/lines are DEVICE pointers owned by the
+ *     caller and must be 16-byte aligned (the notes' §2 and §1: 16-byte
+ *     vectors; a misaligned pointer returns AR_ERR_ALIGN).  The arrays
+ *     `in`, `out`, `lines_in`, `lines_out` are HOST arrays of n_ranks device
+ *     pointers; they are copied into the launch, so they may be freed when
+ *     the call returns.
+ *   - `count` is in elements of the payload type (0 is a no-op).
+ *   - In place is allowed: out[r] == in[r].  Otherwise the buffers of
+ *     different ranks, and each rank's input and output, must not overlap
+ *     (AR_ERR_INVALID).  Inputs may alias each other (they are only read).
+ *   - count x element size must not exceed the handle's max_bytes
+ *     (AR_ERR_TOO_LARGE): the library is sized once, up front, the way the
+ *     pages' custom all-reduce pre-registers a fixed buffer (handbook chapter
+ *     "集合通信：NCCL 的算法、协议与推理框架的定制 all-reduce", §练习
+ *     exercise 3).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream), never allocate and never synchronize, so they can be
+ *     issued inside CUDA graph capture.  Host-side argument errors are
+ *     returned at once and nothing is launched.  Errors found by a kernel
+ *     are sticky in the handle and are returned by ar_status().
+ *   - A handle may be used from one host thread at a time.
+ *
+ * Return codes: AR_OK (0) or a negative AR_ERR_* value; ar_strerror() names it.
+ */
+#ifndef AR_GB300_H
+#define AR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ar_stream_t; /* the same type as cudaStream_t */
+typedef struct ar_ctx* ar_handle;        /* opaque */
+
+typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_F16 = 2 } ar_dtype;
+
+enum {
+    AR_OK = 0,
+    AR_ERR_INVALID = -1,      /* bad handle, n, dtype, step 0, NULL or overlapping pointers */
+    AR_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned */
+    AR_ERR_TOO_LARGE = -3,    /* count x element size > max_bytes */
+    AR_ERR_CUDA = -4,         /* a CUDA runtime call or a launch failed */
+    AR_ERR_FLAG_TIMEOUT = -5  /* an LL/LL128 line never showed the expected flag */
+};
+
+/* Which call an ar_traffic_t describes. */
+typedef enum {
+    AR_OP_NONE = 0,
+    AR_OP_ONE_SHOT = 1,
+    AR_OP_TWO_SHOT = 2,
+    AR_OP_RING = 3,
+    AR_OP_LL_PACK = 4,
+    AR_OP_LL_UNPACK = 5,
+    AR_OP_LL_REDUCE = 6,
+    AR_OP_LL128_PACK = 7,
+    AR_OP_LL128_UNPACK = 8,
+    AR_OP_LL128_REDUCE = 9
+} ar_op;
+
+/* Traffic of one call.
+ *   link_bytes_per_rank, steps: the pages' model of a real n-GPU run, for
+ *     all-reduce calls: one-shot (n-1) S in 1 step, two-shot 2(n-1)/n S in 2
+ *     steps, ring 2(n-1) S / n in 2(n-1) steps (handbook "集合通信：NCCL 的
+ *     算法、协议…", §算法; "多 GPU 与 NCCL", §ring all-reduce).  They are
+ *     per-rank averages over the call's own chunks; every chunk moves once
+ *     per step, so they equal the closed forms for any count.  0 for the
+ *     LL/LL128 calls (whose reduce counts as 1 step).
+ *   hbm_read_bytes / hbm_write_bytes: the bytes the call must move in this
+ *     GPU's HBM (algorithmic, not measured).
+ *   launches: kernels the call launched. */
+typedef struct {
+    int op;                  /* ar_op */
+    int n_ranks;             /* 1 for the per-buffer LL/LL128 pack/unpack */
+    size_t count;            /* elements */
+    size_t elem_bytes;       /* 4 or 2 */
+    double link_bytes_per_rank;
+    int steps;
+    int launches;
+    uint64_t hbm_read_bytes;
+    uint64_t hbm_write_bytes;
+} ar_traffic_t;
+
+/* The sticky device-side error of a handle. */
+typedef struct {
+    int code;                /* AR_OK or AR_ERR_FLAG_TIMEOUT */
+    int rank;                /* rank whose line lacked the flag (-1: none) */
+    uint64_t line;           /* index of the first line found without its flag */
+    uint64_t lines_skipped;  /* lines left unconsumed (their outputs untouched) */
+} ar_status_info_t;
+
+/* Options for ar_set_option. */
+enum {
+    AR_OPT_CTAS_PER_SM = 1,  /* CTAs per SM for the streaming kernels, 1..32 (default 8) */
+    AR_OPT_SPIN_NS = 2,      /* LL/LL128 bounded wait per line, ns, 1..10^10 (default 10^6) */
+    AR_OPT_ONE_SHOT_IMPL = 3,/* 0 auto, 1 vector loads/stores, 2 bulk-copy staging */
+    AR_OPT_TIMING = 4        /* 0 off (default); k in 1..2^20: record a CUDA event pair
+                                around each launch, keeping the last k launches.  Setting
+                                it creates the events (not a hot-path call); do not time
+                                calls that are being captured into a CUDA graph. */
+};
+
+/* Kernels, as ar_timing reports them. */
+typedef enum {
+    AR_K_ONE_SHOT = 1,
+    AR_K_REDUCE_SCATTER = 2,  /* two-shot phase 1 */
+    AR_K_ALL_GATHER = 3,      /* two-shot phase 2 */
+    AR_K_RING_RS_STEP = 4,
+    AR_K_RING_AG_STEP = 5,
+    AR_K_LL_PACK = 6,
+    AR_K_LL_UNPACK = 7,
+    AR_K_LL_REDUCE = 8,
+    AR_K_LL128_PACK = 9,
+    AR_K_LL128_UNPACK = 10,
+    AR_K_LL128_REDUCE = 11
+} ar_kernel;
+
+/* One recorded launch: which kernel, for which call, its device time
+ * (cudaEventElapsedTime between events recorded on the call's stream right
+ * before and after the launch) and the HBM bytes it must move
+ * (algorithmic). */
+typedef struct {
+    int kernel;              /* ar_kernel */
+    int op;                  /* ar_op of the call that launched it */
+    float ms;
+    uint64_t hbm_bytes;
+} ar_launch_time_t;
+
+/* ---- handle --------------------------------------------------------------- */
+
+/* Create a handle for n_ranks in [2, 16] ranks of at most max_bytes each
+ * (max_bytes >= 16), on the calling thread's current CUDA device.  It
+ * allocates, once, the ring's fp32 partial-sum scratch (2 x n_ranks x chunk
+ * x 4 B, about 4 x max_bytes) and a status word.  *out is set only on AR_OK.
+ * The n-rank bound is the pages' kMaxNumGPU = 16 (custom all-reduce notes,
+ * §调用). */
+int ar_create(int n_ranks, size_t max_bytes, ar_handle* out);
+
+/* Synchronize the device, then free the handle and its device memory.  An
+ * invalid or NULL handle is AR_ERR_INVALID. */
+int ar_destroy(ar_handle h);
+
+/* Set one AR_OPT_* option; out-of-range values are AR_ERR_INVALID. */
+int ar_set_option(ar_handle h, int option, int64_t value);
+
+/* ---- all-reduce ------------------------------------------------------------- */
+
+/* One-shot: every rank reads all n buffers and reduces locally, in one step
+ * (handbook "集合通信：NCCL 的算法、协议…", §算法, one-shot; custom
+ * all-reduce notes §1-§5: 16-byte vectors, n loads in flight, fp32 sum in
+ * rank order, one rounding, then the store).  Here one kernel reads each
+ * 16-byte vector of the n inputs once and writes the rounded sum to all n
+ * outputs.  HBM: reads n S, writes n S. */
+int ar_one_shot(ar_handle h, const void* const* in, void* const* out, size_t count,
+                ar_dtype dt, ar_stream_t stream);
+
+/* Two-shot: reduce-scatter then all-gather (handbook "集合通信：NCCL 的
+ * 算法、协议…", §算法, two-shot; "多 GPU 与 NCCL", §集合通信: all-reduce =
+ * reduce-scatter + all-gather).  Chunk r = elements [rC, min((r+1)C, count))
+ * with C = ceil(count/n) rounded up to a whole 16-byte vector.  Phase 1
+ * writes chunk r's rank-order sum to out[r]; phase 2 copies chunk j of
+ * out[j] to every other rank.  Bit-identical to ar_one_shot.  HBM: reads
+ * (n+1) S, writes n S. */
+int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t count,
+                ar_dtype dt, ar_stream_t stream);
+
+/* Ring: the chunked ring, step by step ("多 GPU 与 NCCL", §ring all-reduce:
+ * n-1 reduce-scatter steps, then n-1 all-gather steps).  Chunks as in
+ * ar_two_shot.  Reduce-scatter step s = 0..n-2: for every rank r, rank
+ * d = r+1 (mod n) adds its chunk c = r-s (mod n) to the partial that r
+ * sends; partials stay fp32 in the handle's scratch and the rank completing
+ * a chunk rounds it into its output.  All-gather step s: rank r+1 copies
+ * chunk r+1-s (mod n) from rank r.  One launch per step, 2(n-1) launches.
+ * Chunk c is summed in the order c, c+1, ..., c+n-1. */
+int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
+            ar_dtype dt, ar_stream_t stream);
+
+/* ---- LL / LL128 protocol lines -------------------------------------------- */
+/* Handbook "集合通信：NCCL 的算法、协议…", §协议 table: LL puts 4 B of data
+ * and a 4 B flag in every 8 B line, LL128 120 B of data and an 8 B flag in
+ * every 128 B line; the receiver checks the flag to know the data arrived.
+ * Layout (a reading; the pages give no byte positions):
+ *   LL line i    : bytes 0..3 = payload word i (fp32 bits), bytes 4..7 = u32 flag
+ *   LL128 line k : bytes 0..119 = payload words 30k..30k+29 (zero padding
+ *                  past count), bytes 120..127 = u64 flag
+ * Payloads are fp32, count = payload elements.  The flag is the step id;
+ * step 0 is rejected (zeroed memory would look valid).  A consumer checks
+ * each line's flag, re-reading it for at most AR_OPT_SPIN_NS; a line still
+ * without its flag is left unconsumed (its output untouched) and the handle
+ * records AR_ERR_FLAG_TIMEOUT for ar_status(). */
+
+/* Bytes of LL lines for a payload of payload_bytes: 2 x payload, payload
+ * rounded up to whole 4-byte words. */
+size_t ar_ll_bytes(size_t payload_bytes);
+/* Bytes of LL128 lines for a payload of payload_bytes: 128 x ceil(P / 120). */
+size_t ar_ll128_bytes(size_t payload_bytes);
+
+/* Pack count fp32 words of src into count LL lines with flag `step`. */
+int ar_ll_pack(ar_handle h, const float* src, void* lines, size_t count, uint32_t step,
+               ar_stream_t stream);
+/* Check and unpack count LL lines into dst. */
+int ar_ll_unpack(ar_handle h, const void* lines, float* dst, size_t count, uint32_t step,
+                 ar_stream_t stream);
+/* Pack count fp32 words into ceil(count/30) LL128 lines with flag `step`. */
+int ar_ll128_pack(ar_handle h, const float* src, void* lines, size_t count, uint64_t step,
+                  ar_stream_t stream);
+/* Check and unpack ceil(count/30) LL128 lines into count words of dst. */
+int ar_ll128_unpack(ar_handle h, const void* lines, float* dst, size_t count, uint64_t step,
+                    ar_stream_t stream);
+
+/* Flag-checked reduce: a line is consumed when every rank's copy carries
+ * `step`; its words are summed in rank order (fp32, from +0) and written to
+ * every rank's output line with flag `step`.  lines_in / lines_out: host
+ * arrays of n_ranks device pointers (in place allowed).  count = payload
+ * elements per rank.  LL128 sums all 30 words of a line, padding included. */
+int ar_ll_reduce(ar_handle h, const void* const* lines_in, void* const* lines_out, size_t count,
+                 uint32_t step, ar_stream_t stream);
+int ar_ll128_reduce(ar_handle h, const void* const* lines_in, void* const* lines_out, size_t count,
+                    uint64_t step, ar_stream_t stream);
+
+/* ---- status, accounting, host-only helpers -------------------------------- */
+
+/* Synchronize the device (every stream, so also the calls this handle
+ * issued), return the sticky device error (AR_OK if none) and clear it.  Not
+ * for the hot path; a call that fails in CUDA returns AR_ERR_CUDA. */
+int ar_status(ar_handle h);
+/* As ar_status, with the details of the first failure. */
+int ar_status_info(ar_handle h, ar_status_info_t* info);
+
+/* Traffic of the last successful call on this handle. */
+int ar_traffic(ar_handle h, ar_traffic_t* t);
+
+/* With AR_OPT_TIMING on: wait for the recorded launches to finish, copy up
+ * to `max` of them, oldest first, into out[], set *n_out to the number
+ * copied, and clear the record.  AR_ERR_INVALID if timing is off. */
+int ar_timing(ar_handle h, ar_launch_time_t* out, int max, int* n_out);
+
+/* Host only, no GPU needed: the traffic a call of `op` would have (as
+ * ar_traffic reports it after the call). */
+int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
+
+/* Host only, no GPU needed: the code an all-reduce call (AR_OP_ONE_SHOT,
+ * AR_OP_TWO_SHOT, AR_OP_RING, AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE) would
+ * return for these arguments before launching anything.  Pointers are
+ * compared, never dereferenced.  For the LL ops dt must be AR_F32. */
+int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in,
+                  void* const* out, size_t count, ar_dtype dt);
+
+/* Static text for a return code. */
+const char* ar_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AR_GB300_H */

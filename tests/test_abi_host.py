@@ -1,0 +1,180 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/ar.h declares, and its host-only logic (sizes, traffic plan,
+argument checks, error codes) matches the pages' closed forms."""
+
+import os
+import re
+
+import pytest
+import torch
+
+import all_reduce_reduction_rank_gb300 as ar
+from all_reduce_reduction_rank_gb300 import build as arbuild
+from oracle import model
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    arbuild.build()
+    return ar.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "ar.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ar_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 20
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(ar.EXPORTS) == names
+
+
+def test_strerror_names_every_code(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert ar.ar_strerror(code) != "unknown error code"
+    assert ar.ar_strerror(-99) == "unknown error code"
+
+
+@pytest.mark.parametrize("P", [1, 4, 8, 119, 120, 121, 1 << 20, 3 * 120 + 7])
+def test_packed_sizes_match_the_protocol_table(lib, P):
+    # LL: 4 B data + 4 B flag per 8 B  ->  2P;  LL128: 120 + 8 per 128  ->  128 ceil(P/120)
+    assert ar.ar_ll_bytes(P) == 2 * (-(-P // 4) * 4)
+    assert ar.ar_ll128_bytes(P) == 128 * -(-P // 120)
+    if P % 4 == 0:
+        assert ar.ar_ll_bytes(P) == oracle.ll_bytes(P // 4)
+        assert ar.ar_ll128_bytes(P) == oracle.ll128_bytes(P // 4)
+
+
+E = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("count", [0, 1, 1000, 1 << 20, 4099])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_plan_matches_closed_forms(lib, n, count, dtype):
+    e = E[dtype]
+    S = count * e
+    t = ar.ar_plan(ar.AR_OP_ONE_SHOT, n, count, dtype)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_one_shot(n, S))
+    assert t.steps == model.steps_one_shot(n)
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == model.hbm_one_shot(n, count, e)
+    assert t.launches == (1 if count else 0)
+    t = ar.ar_plan(ar.AR_OP_TWO_SHOT, n, count, dtype)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_two_shot(n, S))
+    assert t.steps == model.steps_two_shot(n)
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == model.hbm_two_shot(n, count, e)
+    t = ar.ar_plan(ar.AR_OP_RING, n, count, dtype)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, S))
+    assert t.steps == model.steps_ring(n) and t.launches == (2 * (n - 1) if count else 0)
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == model.hbm_ring(n, count, e)
+
+
+@pytest.mark.parametrize("count", [0, 1, 29, 30, 31, 262144])
+def test_plan_ll_matches_closed_forms(lib, count):
+    assert _rw(ar.ar_plan(ar.AR_OP_LL_PACK, 1, count, "f32")) == model.hbm_ll_pack(count)
+    assert _rw(ar.ar_plan(ar.AR_OP_LL_UNPACK, 1, count, "f32")) == model.hbm_ll_unpack(count)
+    assert _rw(ar.ar_plan(ar.AR_OP_LL_REDUCE, 8, count, "f32")) == model.hbm_ll_reduce(8, count)
+    assert _rw(ar.ar_plan(ar.AR_OP_LL128_PACK, 1, count, "f32")) == model.hbm_ll128_pack(count)
+    assert _rw(ar.ar_plan(ar.AR_OP_LL128_UNPACK, 1, count, "f32")) == model.hbm_ll128_unpack(count)
+    assert _rw(ar.ar_plan(ar.AR_OP_LL128_REDUCE, 8, count, "f32")) == model.hbm_ll128_reduce(8, count)
+
+
+def _rw(t):
+    return t.hbm_read_bytes, t.hbm_write_bytes
+
+
+def test_plan_rejects_bad_arguments(lib):
+    for op, n in [(0, 8), (10, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17)]:
+        with pytest.raises(ar.ArError):
+            ar.ar_plan(op, n, 10, "f32")
+    with pytest.raises(ar.ArError):
+        ar.ar_plan(ar.AR_OP_ONE_SHOT, 8, 10, 7)
+
+
+# --- argument checks, pointers compared but never dereferenced -------------
+
+BASE = 1 << 40  # fake device addresses, 16-byte aligned, 1 MiB apart
+
+
+def _bufs(n, stride=1 << 20, off=0):
+    return [BASE + off + r * stride for r in range(n)]
+
+
+def _check(op, n, ins, outs, count, dtype="bf16", max_bytes=1 << 20):
+    return ar.ar_check_args(op, n, max_bytes, ins, outs, count, dtype)
+
+
+OPS = [ar.AR_OP_ONE_SHOT, ar.AR_OP_TWO_SHOT, ar.AR_OP_RING]
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_check_args(lib, op):
+    n = 8
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    assert _check(op, n, ins, outs, 1000) == ar.AR_OK
+    assert _check(op, n, ins, ins, 1000) == ar.AR_OK                     # in place
+    assert _check(op, n, [ins[0]] * n, outs, 1000) == ar.AR_OK           # inputs may alias
+    assert _check(op, n, ins, outs, 0) == ar.AR_OK                       # empty
+    assert _check(op, 1, ins, outs, 10) == ar.AR_ERR_INVALID
+    assert _check(op, 17, ins + ins, outs + outs, 10) == ar.AR_ERR_INVALID
+    assert _check(op, n, ins, outs, 10, dtype=3) == ar.AR_ERR_INVALID
+    assert _check(op, n, None, outs, 10) == ar.AR_ERR_INVALID
+    assert _check(op, n, ins[:-1] + [0], outs, 10) == ar.AR_ERR_INVALID
+    assert _check(op, n, ins, outs, (1 << 19) + 1) == ar.AR_ERR_TOO_LARGE  # bf16: 2 B each
+    assert _check(op, n, ins, outs, 1 << 19) == ar.AR_OK                   # exactly max_bytes
+    assert _check(op, n, ins, outs, 1 << 62) == ar.AR_ERR_TOO_LARGE
+    assert _check(op, n, [ins[0] + 8] + ins[1:], outs, 10) == ar.AR_ERR_ALIGN
+    assert _check(op, n, ins, outs[:3] + [outs[3] + 4] + outs[4:], 10) == ar.AR_ERR_ALIGN
+    # overlaps: two outputs, an output with another rank's input, a shifted in-place
+    over = outs[:]
+    over[2] = outs[1] + 16
+    assert _check(op, n, ins, over, 1000) == ar.AR_ERR_INVALID
+    cross = outs[:]
+    cross[5] = ins[6]
+    assert _check(op, n, ins, cross, 1000) == ar.AR_ERR_INVALID
+    shifted = [i + 16 for i in ins]
+    assert _check(op, n, ins, shifted, 1000) == ar.AR_ERR_INVALID
+    assert _check(op, n, ins, shifted, 8) == ar.AR_OK                     # 16 B apart, 16 B long
+
+
+def test_check_args_ll(lib):
+    n = 8
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    for op in (ar.AR_OP_LL_REDUCE, ar.AR_OP_LL128_REDUCE):
+        assert _check(op, n, ins, outs, 1000, dtype="f32") == ar.AR_OK
+        assert _check(op, n, ins, outs, 1000, dtype="bf16") == ar.AR_ERR_INVALID
+    # LL lines are twice the payload: 1000 words -> 8000 B, so 4 KiB apart overlaps
+    close = [BASE + r * 4096 for r in range(n)]
+    assert _check(ar.AR_OP_LL_REDUCE, n, ins, close, 1000, dtype="f32") == ar.AR_ERR_INVALID
+    assert _check(ar.AR_OP_LL_REDUCE, n, ins, close, 500, dtype="f32") == ar.AR_OK
+
+
+def test_calls_reject_a_null_handle(lib):
+    p = _bufs(8)
+    assert ar.ar_one_shot(0, p, p, 10, "bf16") == ar.AR_ERR_INVALID
+    assert ar.ar_two_shot(0, p, p, 10, "bf16") == ar.AR_ERR_INVALID
+    assert ar.ar_ring(0, p, p, 10, "bf16") == ar.AR_ERR_INVALID
+    assert ar.ar_ll_pack(0, p[0], p[1], 10, 1) == ar.AR_ERR_INVALID
+    assert ar.ar_ll128_reduce(0, p, p, 10, 1) == ar.AR_ERR_INVALID
+    assert ar.ar_destroy(0) == ar.AR_ERR_INVALID
+    assert ar.ar_status(0) == ar.AR_ERR_INVALID
+    assert ar.ar_set_option(0, ar.AR_OPT_SPIN_NS, 10) == ar.AR_ERR_INVALID
+    with pytest.raises(ar.ArError):
+        ar.ar_traffic(0)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_create_without_a_device_fails_cleanly(lib):
+    with pytest.raises(ar.ArError) as e:
+        ar.ar_create(8, 1 << 20)
+    assert e.value.code == ar.AR_ERR_CUDA
+    with pytest.raises(ar.ArError) as e:
+        ar.ar_create(1, 1 << 20)
+    assert e.value.code == ar.AR_ERR_INVALID

@@ -1,0 +1,253 @@
+"""Parity of ar_one_shot / ar_two_shot / ar_ring against the CPU oracle,
+through the C-ABI, on seeded inputs.
+
+Bar: one-shot and two-shot keep the oracle's rank order, so they must be
+bit-exact to oracle.all_reduce; the ring must be bit-exact to oracle.ring
+(its own order) and within 1 payload ulp, or 2^-8 of sum|x| (1e-6 relative
+for fp32), of the one-shot result.  Every buffer carries canary bands that
+must be untouched afterwards.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_reduction_rank_gb300 as ar
+import oracle
+import workloads
+from gpu_util import Buf, Handle, bits, empty_ranks, payload_np_dtype, ptrs, upload_ranks
+
+pytestmark = pytest.mark.gpu
+
+CALLS = {"one_shot": ar.ar_one_shot, "two_shot": ar.ar_two_shot, "ring": ar.ar_ring}
+E = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+def run(algo, xs, dtype, in_place=False, stream=None, h=None, max_bytes=None):
+    n, N = len(xs), xs[0].size
+    ins = upload_ranks(xs)
+    outs = ins if in_place else empty_ranks(n, xs[0].nbytes)
+    mb = max_bytes or max(16, N * E[dtype])
+
+    def call(handle):
+        rc = CALLS[algo](handle, ptrs(ins), ptrs(outs), N, dtype, stream)
+        assert rc == ar.AR_OK, ar.ar_strerror(rc)
+        assert ar.ar_status(handle) == ar.AR_OK
+
+    if h is None:
+        with Handle(n, mb) as handle:
+            call(handle)
+    else:
+        call(h)
+    torch.cuda.synchronize()
+    for b in ins + outs:
+        assert b.guards_intact()
+    return [o.download(payload_np_dtype(dtype)) for o in outs]
+
+
+def tolerance_ok(g, o, xs, dtype):
+    gf = oracle.to_f32(g, dtype).astype(np.float64)
+    of = oracle.to_f32(o, dtype).astype(np.float64)
+    abs_sum = sum(np.abs(oracle.to_f32(x, dtype)).astype(np.float64) for x in xs)
+    if dtype == "f32":
+        tol = 1e-6 * np.maximum(np.abs(of), abs_sum)
+    else:
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(of), 2.0**-126))) - (7 if dtype == "bf16" else 10))
+        tol = np.maximum(ulp, 2.0**-8 * abs_sum)
+    return bool(np.all(np.abs(gf - of) <= tol))
+
+
+# sizes: several tiles of 256 threads x 16 B and ragged tails of every length
+SIZES = [1, 3, 7, 8, 9, 15, 17, 100, 1000, 4096, 8191, 65536 + 5, 300_001]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("N", SIZES)
+def test_one_and_two_shot_bit_exact(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=n * 7919 + N)
+    want = oracle.all_reduce(xs, dtype)
+    for algo in ("one_shot", "two_shot"):
+        got = run(algo, xs, dtype)
+        for r in range(n):
+            np.testing.assert_array_equal(bits(got[r]), bits(want[r]), err_msg=f"{algo} rank {r}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("N", [1, 9, 1000, 4099, 65536 + 3, 300_001])
+def test_ring_matches_its_order_and_tolerance(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=n * 104729 + N)
+    want = oracle.ring(xs, dtype)
+    got = run("ring", xs, dtype)
+    for r in range(n):
+        np.testing.assert_array_equal(bits(got[r]), bits(want[r]), err_msg=f"rank {r}")
+    assert tolerance_ok(got[0], oracle.all_reduce(xs, dtype)[0], xs, dtype)
+
+
+@pytest.mark.parametrize("algo", ["one_shot", "two_shot", "ring"])
+@pytest.mark.parametrize("n", [2, 8, 16])
+def test_in_place(algo, n):
+    dtype, N = "bf16", 50_001
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=5 + n)
+    want = (oracle.ring if algo == "ring" else oracle.all_reduce)(xs, dtype)
+    got = run(algo, xs, dtype, in_place=True)
+    for r in range(n):
+        np.testing.assert_array_equal(bits(got[r]), bits(want[r]))
+
+
+def test_config1_n2_f32_integers_exact():
+    cfg = workloads.CONFIGS[1]
+    xs = workloads.rank_inputs(cfg["n"], cfg["counts"][0], "f32", cfg["dist"], workloads.seed_of(1))
+    exact = (xs[0].astype(np.int64) + xs[1].astype(np.int64)).astype(np.float32)
+    for algo in cfg["algos"]:
+        got = run(algo, xs, "f32")
+        for g in got:
+            np.testing.assert_array_equal(g, exact)
+
+
+@pytest.mark.parametrize("N", workloads.CONFIGS[2]["counts"])
+def test_config2_decode_sizes(N):
+    cfg = workloads.CONFIGS[2]
+    xs = workloads.rank_inputs(cfg["n"], N, "bf16", cfg["dist"], workloads.seed_of(2) + N)
+    want = oracle.all_reduce(xs, "bf16")
+    for algo in cfg["algos"]:
+        got = run(algo, xs, "bf16")
+        for r in range(cfg["n"]):
+            np.testing.assert_array_equal(got[r], want[r])
+
+
+@pytest.mark.parametrize("n", range(2, 17))
+def test_every_rank_count(n):
+    N = 4096 + 7
+    xs = workloads.rank_inputs(n, N, "bf16", "int8", seed=n)
+    exact = sum(oracle.to_f32(x, "bf16").astype(np.int64) for x in xs)
+    for algo in ("one_shot", "two_shot", "ring"):
+        got = run(algo, xs, "bf16")
+        for g in got:
+            np.testing.assert_array_equal(oracle.to_f32(g, "bf16").astype(np.int64), exact)
+
+
+def test_nccl_fill_pattern_zero_mismatches():
+    # the NCCL example's check: rank g holds g + i % 7, expect n(n-1)/2 + n (i % 7)
+    n, N = 8, (1 << 20) + 3
+    xs = workloads.rank_inputs(n, N, "f32", "fill7", seed=0)
+    i = np.arange(N)
+    want = np.float32(n * (n - 1) / 2) + np.float32(n) * (i % 7).astype(np.float32)
+    for algo in ("one_shot", "two_shot", "ring"):
+        got = run(algo, xs, "f32", in_place=True)
+        assert sum(int(np.count_nonzero(g != want)) for g in got) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_signed_zero_readings(dtype):
+    neg = np.full(64, 0x80000000 if dtype == "f32" else 0x8000, np.uint32 if dtype == "f32" else np.uint16)
+    x = neg.view(np.float32) if dtype == "f32" else neg
+    xs = [x.copy() for _ in range(3)]
+    for algo in ("one_shot", "two_shot"):
+        assert np.all(bits(run(algo, xs, dtype)[1]) == 0)         # accumulator starts at +0
+    assert np.all(bits(run("ring", xs, dtype)[1]) == bits(oracle.ring(xs, dtype)[1]))
+
+
+def test_inf_and_nan_propagate():
+    n, N = 4, 4096
+    xs = workloads.rank_inputs(n, N, "f32", "normal", seed=77)
+    xs[1][::7] = np.inf
+    xs[2][::11] = -np.inf
+    xs[3][::13] = np.nan
+    want = oracle.all_reduce(xs, "f32")[0]
+    for algo in ("one_shot", "two_shot", "ring"):
+        g = run(algo, xs, "f32")[0]
+        assert np.array_equal(np.isnan(g), np.isnan(want))
+        keep = ~np.isnan(want)
+        if algo == "ring":
+            assert np.array_equal(np.isinf(g[keep]), np.isinf(want[keep]))
+        else:
+            np.testing.assert_array_equal(bits(g[keep]), bits(want[keep]))
+
+
+def test_empty_count_is_a_no_op():
+    with Handle(8, 1 << 16) as h:
+        outs = empty_ranks(8, 64, byte=0x33)
+        for call in CALLS.values():
+            assert call(h, ptrs(outs), ptrs(outs), 0, "bf16") == ar.AR_OK
+            assert ar.ar_traffic(h).launches == 0
+        torch.cuda.synchronize()
+        assert all(bool((o.body() == 0x33).all()) for o in outs)
+
+
+def test_max_bytes_boundary_and_errors():
+    n, N = 4, 1 << 16
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=9)
+    want = oracle.all_reduce(xs, "bf16")
+    with Handle(n, N * 2) as h:                      # exactly one buffer's worth
+        for algo in CALLS:
+            got = run(algo, xs, "bf16", h=h)
+            if algo != "ring":
+                np.testing.assert_array_equal(got[2], want[2])
+        ins = upload_ranks(xs)
+        outs = empty_ranks(n, xs[0].nbytes, byte=0x11)
+        assert ar.ar_one_shot(h, ptrs(ins), ptrs(outs), N + 1, "bf16") == ar.AR_ERR_TOO_LARGE
+        bad = ptrs(outs)
+        bad[1] += 2
+        assert ar.ar_two_shot(h, ptrs(ins), bad, N - 8, "bf16") == ar.AR_ERR_ALIGN
+        assert ar.ar_ring(h, ptrs(ins), ptrs(outs), 10, 5) == ar.AR_ERR_INVALID
+        torch.cuda.synchronize()
+        assert all(bool((o.body() == 0x11).all()) for o in outs)   # nothing launched
+
+
+def test_traffic_reports_the_last_call():
+    n, N = 8, 12345
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=1)
+    with Handle(n, N * 2) as h:
+        for algo, op in (("one_shot", ar.AR_OP_ONE_SHOT), ("two_shot", ar.AR_OP_TWO_SHOT), ("ring", ar.AR_OP_RING)):
+            run(algo, xs, "bf16", h=h)
+            t = ar.ar_traffic(h).as_dict()
+            p = ar.ar_plan(op, n, N, "bf16").as_dict()
+            assert t == p and t["op"] == op
+
+
+def test_non_default_stream():
+    n, N = 8, 200_000
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=3)
+    want = oracle.all_reduce(xs, "bf16")
+    s = torch.cuda.Stream()
+    got = run("one_shot", xs, "bf16", stream=s)
+    np.testing.assert_array_equal(got[7], want[7])
+    got = run("ring", xs, "bf16", stream=s)
+    np.testing.assert_array_equal(got[0], oracle.ring(xs, "bf16")[0])
+
+
+def test_cuda_graph_capture_and_replay():
+    n, N = 8, 65536
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=4)
+    ys = workloads.rank_inputs(n, N, "bf16", "normal", seed=5)
+    ins = upload_ranks(xs)
+    outs = empty_ranks(n, xs[0].nbytes)
+    with Handle(n, N * 2) as h:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rc1 = ar.ar_one_shot(h, ptrs(ins), ptrs(outs), N, "bf16", s)
+            rc2 = ar.ar_ring(h, ptrs(ins), ptrs(outs), N, "bf16", s)
+            rc3 = ar.ar_two_shot(h, ptrs(ins), ptrs(outs), N, "bf16", s)
+        assert rc1 == rc2 == rc3 == ar.AR_OK
+        for src in (xs, ys):             # same addresses, new contents, replay
+            for b, a in zip(ins, src):
+                b.upload(a)
+            g.replay()
+            torch.cuda.synchronize()
+            want = oracle.all_reduce(src, "bf16")
+            for r in range(n):
+                np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
+        assert ar.ar_status(h) == ar.AR_OK
+
+
+def test_handle_is_reusable_across_sizes_and_types():
+    with Handle(8, 1 << 20) as h:
+        for dtype, N in (("bf16", 77), ("f32", 1 << 18), ("f16", 5000), ("bf16", 1 << 19)):
+            xs = workloads.rank_inputs(8, N, dtype, "normal", seed=N)
+            for algo in CALLS:
+                got = run(algo, xs, dtype, h=h)
+                want = (oracle.ring if algo == "ring" else oracle.all_reduce)(xs, dtype)
+                np.testing.assert_array_equal(bits(got[3]), bits(want[3]))

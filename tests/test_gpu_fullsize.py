@@ -1,0 +1,113 @@
+"""Full-size parity: the prefill workload (n = 8 bf16, 8..64 MiB per rank)
+in the launch configuration the bench times, and the n = 16 sweep's largest
+sizes.  The oracle computes sampled outputs one by one; properties that hold
+at any size (every rank identical, two-shot == one-shot bit for bit) cover
+the rest of each buffer."""
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_reduction_rank_gb300 as ar
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+MiB = 1 << 20
+
+
+def _sample_idx(N, C, rng, k=100_000):
+    edges = []
+    for c in range(0, N, max(C, 1)):          # chunk boundaries and the ragged end
+        edges += [c - 1, c, c + 1]
+    idx = np.concatenate([rng.integers(0, N, size=k), np.arange(min(N, 4096)),
+                          np.arange(max(0, N - 4096), N), np.array(edges)])
+    return np.unique(idx[(idx >= 0) & (idx < N)])
+
+
+def _cols(ts, idx, dtype):
+    ti = torch.from_numpy(idx).to(ts[0].device)
+    np_t = np.float32 if dtype == "f32" else np.uint16
+    return [t[ti].cpu().numpy().view(np_t) for t in ts]
+
+
+def _run(call, h, ins, outs, N, dtype):
+    rc = call(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], N, dtype)
+    assert rc == ar.AR_OK, ar.ar_strerror(rc)
+
+
+@pytest.mark.parametrize("S", [8 * MiB, 64 * MiB])
+def test_prefill_one_and_two_shot(S):
+    n, dtype = 8, "bf16"
+    N = S // 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(3) + S)
+    o1 = [torch.empty_like(t) for t in ins]
+    o2 = [torch.empty_like(t) for t in ins]
+    with_h = ar.ar_create(n, S)
+    try:
+        _run(ar.ar_one_shot, with_h, ins, o1, N, dtype)
+        _run(ar.ar_two_shot, with_h, ins, o2, N, dtype)
+        assert ar.ar_status(with_h) == ar.AR_OK
+    finally:
+        assert ar.ar_destroy(with_h) == ar.AR_OK
+    for r in range(1, n):
+        assert torch.equal(o1[r], o1[0]) and torch.equal(o2[r], o2[0])
+    assert torch.equal(o1[0], o2[0])
+    idx = _sample_idx(N, oracle.chunk_elems(n, N, dtype), np.random.default_rng(S))
+    want = oracle.all_reduce(_cols(ins, idx, dtype), dtype)[0]
+    np.testing.assert_array_equal(_cols([o1[0]], idx, dtype)[0], want)
+
+
+@pytest.mark.parametrize("dtype,S", [("bf16", 256 * MiB), ("f16", 64 * MiB)])
+def test_n16_sweep_largest(dtype, S):
+    n = 16
+    N = S // 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(5) + S)
+    out_r = [torch.empty_like(t) for t in ins]
+    out_1 = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, S)
+    try:
+        _run(ar.ar_ring, h, ins, out_r, N, dtype)
+        _run(ar.ar_one_shot, h, ins, out_1, N, dtype)
+        assert ar.ar_status(h) == ar.AR_OK
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+    for r in range(1, n):
+        assert torch.equal(out_r[r], out_r[0]) and torch.equal(out_1[r], out_1[0])
+    C = oracle.chunk_elems(n, N, dtype)
+    idx = _sample_idx(N, C, np.random.default_rng(S + 1))
+    cols = _cols(ins, idx, dtype)
+    want_ring = oracle.ring_order_sum(cols, (idx // C).astype(np.int32), dtype)
+    np.testing.assert_array_equal(_cols([out_r[5]], idx, dtype)[0], want_ring)
+    want_one = oracle.all_reduce(cols, dtype)[0]
+    np.testing.assert_array_equal(_cols([out_1[9]], idx, dtype)[0], want_one)
+    del ins, out_r, out_1
+    torch.cuda.empty_cache()
+
+
+def test_ll_largest_payload_in_the_bench_configuration():
+    n, count = 8, (1 * MiB) // 4
+    xs = workloads.rank_inputs_device(n, count, "f32", "uniform", workloads.seed_of(4))
+    h = ar.ar_create(n, 4 * count)
+    try:
+        for kind in ("ll", "ll128"):
+            nb = ar.ar_ll_bytes(4 * count) if kind == "ll" else ar.ar_ll128_bytes(4 * count)
+            pack = ar.ar_ll_pack if kind == "ll" else ar.ar_ll128_pack
+            reduce = ar.ar_ll_reduce if kind == "ll" else ar.ar_ll128_reduce
+            unpack = ar.ar_ll_unpack if kind == "ll" else ar.ar_ll128_unpack
+            lines = [torch.zeros(nb, dtype=torch.uint8, device="cuda") for _ in range(n)]
+            outs = [torch.zeros(nb, dtype=torch.uint8, device="cuda") for _ in range(n)]
+            dst = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+            for step in (11, 12):
+                for x, l in zip(xs, lines):
+                    assert pack(h, x.data_ptr(), l.data_ptr(), count, step) == ar.AR_OK
+                assert reduce(h, [l.data_ptr() for l in lines], [o.data_ptr() for o in outs], count, step) == 0
+                for o, d in zip(outs, dst):
+                    assert unpack(h, o.data_ptr(), d.data_ptr(), count, step) == ar.AR_OK
+                assert ar.ar_status(h) == ar.AR_OK
+                want = oracle.all_reduce([x.cpu().numpy() for x in xs], "f32")[0]
+                for d in dst:
+                    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK

@@ -97,3 +97,38 @@ CONFIGS = {
 
 def seed_of(config: int) -> int:
     return 1000 + config
+
+
+def rank_inputs_device(n: int, count: int, dtype: str, dist: str, seed: int, device="cuda"):
+    """Large seeded rank buffers drawn on the device (torch's Philox
+    generator, seeded per rank with ``seed * 1000 + r``), laid out with the
+    same recipe as ``rank_inputs``; returns torch tensors of payload bits
+    (int16 for bf16/fp16, float32 for fp32).  Used where host generation of
+    gigabytes would dominate the run; the oracle then reads sampled columns
+    of these inputs back from the device."""
+    import torch
+
+    out = []
+    for r in range(n):
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + r)
+        if dist == "normal":
+            x = torch.randn(count, generator=g, device=device, dtype=torch.float32)
+        elif dist == "normal_over_n":
+            x = torch.randn(count, generator=g, device=device, dtype=torch.float32) / n
+        elif dist == "uniform":
+            x = torch.rand(count, generator=g, device=device, dtype=torch.float32) * 2 - 1
+        elif dist == "int8":
+            x = torch.randint(-8, 9, (count,), generator=g, device=device).to(torch.float32)
+        else:
+            raise ValueError(f"unknown distribution {dist!r}")
+        if dtype == "f32":
+            out.append(x)
+        elif dtype == "bf16":
+            out.append(torch.bitwise_right_shift(x.view(torch.int32), 16).to(torch.int16))
+        elif dtype == "f16":
+            out.append(x.to(torch.float16).view(torch.int16))
+        else:
+            raise ValueError(f"unknown dtype {dtype!r}")
+        del x
+    return out
