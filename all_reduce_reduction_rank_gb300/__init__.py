@@ -23,10 +23,11 @@ LIB_PATH = _PKG / "libar_gb300.so"
 
 AR_F32, AR_BF16, AR_F16 = 0, 1, 2
 DTYPES = {"f32": AR_F32, "bf16": AR_BF16, "f16": AR_F16}
-AR_OK, AR_ERR_INVALID, AR_ERR_ALIGN, AR_ERR_TOO_LARGE, AR_ERR_CUDA, AR_ERR_FLAG_TIMEOUT = 0, -1, -2, -3, -4, -5
+AR_OK, AR_ERR_INVALID, AR_ERR_ALIGN, AR_ERR_TOO_LARGE, AR_ERR_CUDA, AR_ERR_FLAG_TIMEOUT, AR_ERR_WAIT_TIMEOUT = (
+    0, -1, -2, -3, -4, -5, -6)
 (AR_OP_NONE, AR_OP_ONE_SHOT, AR_OP_TWO_SHOT, AR_OP_RING, AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL_REDUCE,
  AR_OP_LL128_PACK, AR_OP_LL128_UNPACK, AR_OP_LL128_REDUCE) = range(10)
-AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING = 1, 2, 3, 4
+AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING, AR_OPT_TIMING_PAUSE = 1, 2, 3, 4, 5
 KERNELS = {1: "one_shot", 2: "reduce_scatter", 3: "all_gather", 4: "ring_rs_step", 5: "ring_ag_step",
            6: "ll_pack", 7: "ll_unpack", 8: "ll_reduce", 9: "ll128_pack", 10: "ll128_unpack",
            11: "ll128_reduce"}
@@ -36,7 +37,8 @@ EXPORTS = (
     "ar_create", "ar_destroy", "ar_set_option", "ar_one_shot", "ar_two_shot", "ar_ring",
     "ar_ll_bytes", "ar_ll128_bytes", "ar_ll_pack", "ar_ll_unpack", "ar_ll128_pack", "ar_ll128_unpack",
     "ar_ll_reduce", "ar_ll128_reduce", "ar_status", "ar_status_info", "ar_traffic", "ar_plan",
-    "ar_check_args", "ar_strerror", "ar_timing",
+    "ar_check_args", "ar_strerror", "ar_timing", "ar_ll_pack_n", "ar_ll_unpack_n", "ar_ll128_pack_n",
+    "ar_ll128_unpack_n",
 )
 
 
@@ -94,6 +96,10 @@ def lib() -> ctypes.CDLL:
                 "ar_ll_unpack": ([vp, vp, vp, sz, u32, vp], i32),
                 "ar_ll128_pack": ([vp, vp, vp, sz, u64, vp], i32),
                 "ar_ll128_unpack": ([vp, vp, vp, sz, u64, vp], i32),
+                "ar_ll_pack_n": ([vp, pp, pp, sz, u32, vp], i32),
+                "ar_ll_unpack_n": ([vp, pp, pp, sz, u32, vp], i32),
+                "ar_ll128_pack_n": ([vp, pp, pp, sz, u64, vp], i32),
+                "ar_ll128_unpack_n": ([vp, pp, pp, sz, u64, vp], i32),
                 "ar_ll_reduce": ([vp, pp, pp, sz, u32, vp], i32),
                 "ar_ll128_reduce": ([vp, pp, pp, sz, u64, vp], i32),
                 "ar_status": ([vp], i32),
@@ -195,6 +201,22 @@ def ar_ll128_pack(h, src, lines, count: int, step: int, stream=None) -> int:
 
 def ar_ll128_unpack(h, lines, dst, count: int, step: int, stream=None) -> int:
     return lib().ar_ll128_unpack(h, _addr(lines), _addr(dst), count, step, _stream(stream))
+
+
+def ar_ll_pack_n(h, srcs, lines, count: int, step: int, stream=None) -> int:
+    return lib().ar_ll_pack_n(h, _ptr_array(srcs), _ptr_array(lines), count, step, _stream(stream))
+
+
+def ar_ll_unpack_n(h, lines, dsts, count: int, step: int, stream=None) -> int:
+    return lib().ar_ll_unpack_n(h, _ptr_array(lines), _ptr_array(dsts), count, step, _stream(stream))
+
+
+def ar_ll128_pack_n(h, srcs, lines, count: int, step: int, stream=None) -> int:
+    return lib().ar_ll128_pack_n(h, _ptr_array(srcs), _ptr_array(lines), count, step, _stream(stream))
+
+
+def ar_ll128_unpack_n(h, lines, dsts, count: int, step: int, stream=None) -> int:
+    return lib().ar_ll128_unpack_n(h, _ptr_array(lines), _ptr_array(dsts), count, step, _stream(stream))
 
 
 def ar_ll_reduce(h, lines_in, lines_out, count: int, step: int, stream=None) -> int:

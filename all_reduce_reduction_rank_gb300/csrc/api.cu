@@ -86,6 +86,30 @@ int check_single(int op, size_t max_bytes, const void* src, const void* dst, siz
     return AR_OK;
 }
 
+// Checks of the rank-batched pack / unpack calls: n sources and n
+// destinations of different sizes (payload vs lines); sources may alias.
+int check_batch(int op, int n, size_t max_bytes, const void* const* src, const void* const* dst, size_t count)
+{
+    if (!src || !dst) return AR_ERR_INVALID;
+    for (int r = 0; r < n; ++r)
+        if (!src[r] || !dst[r]) return AR_ERR_INVALID;
+    if (int rc = check_size(count, AR_F32, max_bytes)) return rc;
+    for (int r = 0; r < n; ++r)
+        if (!aligned16(src[r]) || !aligned16(dst[r])) return AR_ERR_ALIGN;
+    const size_t lines = buffer_bytes(op, count, AR_F32), payload = 4u * count;
+    const bool src_is_lines = (op == AR_OP_LL_UNPACK || op == AR_OP_LL128_UNPACK);
+    const size_t sb = src_is_lines ? lines : payload, db = src_is_lines ? payload : lines;
+    if (!count) return AR_OK;
+    for (int r = 0; r < n; ++r) {
+        for (int q = 0; q < n; ++q) {
+            const uintptr_t s = (uintptr_t)src[q], d = (uintptr_t)dst[r];
+            if (s < d + db && d < s + sb) return AR_ERR_INVALID;
+            if (q != r && overlap(dst[r], dst[q], db)) return AR_ERR_INVALID;
+        }
+    }
+    return AR_OK;
+}
+
 void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
 {
     std::memset(t, 0, sizeof(*t));
@@ -127,13 +151,13 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         break;
     case AR_OP_LL_PACK:
         t->launches = count ? 1 : 0;
-        t->hbm_read_bytes = 4 * N;
-        t->hbm_write_bytes = 8 * N;
+        t->hbm_read_bytes = nn * 4 * N;
+        t->hbm_write_bytes = nn * 8 * N;
         break;
     case AR_OP_LL_UNPACK:
         t->launches = count ? 1 : 0;
-        t->hbm_read_bytes = 8 * N;
-        t->hbm_write_bytes = 4 * N;
+        t->hbm_read_bytes = nn * 8 * N;
+        t->hbm_write_bytes = nn * 4 * N;
         break;
     case AR_OP_LL_REDUCE:
         t->steps = 1;
@@ -143,13 +167,13 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         break;
     case AR_OP_LL128_PACK:
         t->launches = count ? 1 : 0;
-        t->hbm_read_bytes = 4 * N;
-        t->hbm_write_bytes = 128 * L;
+        t->hbm_read_bytes = nn * 4 * N;
+        t->hbm_write_bytes = nn * 128 * L;
         break;
     case AR_OP_LL128_UNPACK:
         t->launches = count ? 1 : 0;
-        t->hbm_read_bytes = 128 * L;
-        t->hbm_write_bytes = 4 * N;
+        t->hbm_read_bytes = nn * 128 * L;
+        t->hbm_write_bytes = nn * 4 * N;
         break;
     case AR_OP_LL128_REDUCE:
         t->steps = 1;
@@ -252,6 +276,23 @@ static int single_call(int op, ar_handle hd, const void* src, const void* dst, s
 }
 
 template <typename F>
+static int batch_call(int op, ar_handle hd, const void* const* src, const void* const* dst, size_t count,
+                      uint64_t step, ar_stream_t stream, F&& launch)
+{
+    Handle* h = get(hd);
+    if (!h) return AR_ERR_INVALID;
+    if (step == 0) return AR_ERR_INVALID;
+    if (int rc = check_batch(op, h->n, h->max_bytes, src, dst, count)) return rc;
+    int rc = AR_OK;
+    h->timing.op = op;
+    if (count) rc = on_device(*h, [&] { return launch(*h, (cudaStream_t)stream); });
+    if (rc != AR_OK) return rc;
+    plan(op, h->n, count, AR_F32, &h->last);
+    h->last_stream = (cudaStream_t)stream;
+    return AR_OK;
+}
+
+template <typename F>
 static int reduce_call(int op, ar_handle hd, const void* const* in, void* const* out, size_t count, uint64_t step,
                        ar_stream_t stream, F&& launch)
 {
@@ -279,6 +320,7 @@ const char* ar_strerror(int code)
     case AR_ERR_TOO_LARGE: return "count x element size exceeds max_bytes";
     case AR_ERR_CUDA: return "CUDA runtime error";
     case AR_ERR_FLAG_TIMEOUT: return "LL/LL128 flag not seen within the spin limit";
+    case AR_ERR_WAIT_TIMEOUT: return "a kernel's bounded wait for its bulk copies ran out";
     default: return "unknown error code";
     }
 }
@@ -292,7 +334,7 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
     if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_LL128_REDUCE) return AR_ERR_INVALID;
     const bool multi = op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE;
     if (multi && (n_ranks < 2 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;
-    if (!multi) n_ranks = 1;
+    if (!multi && (n_ranks < 1 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;  // buffers packed
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
     plan(op, n_ranks, count, dt, t);
     return AR_OK;
@@ -301,6 +343,10 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
 int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in, void* const* out, size_t count,
                   ar_dtype dt)
 {
+    if (op == AR_OP_LL_PACK || op == AR_OP_LL_UNPACK || op == AR_OP_LL128_PACK || op == AR_OP_LL128_UNPACK) {
+        if (n_ranks < 1 || n_ranks > kMaxRanks || dt != AR_F32) return AR_ERR_INVALID;
+        return check_batch(op, n_ranks, max_bytes, in, out, count);
+    }
     if (op != AR_OP_ONE_SHOT && op != AR_OP_TWO_SHOT && op != AR_OP_RING && !is_ll_op(op))
         return AR_ERR_INVALID;
     return check_multi(op, n_ranks, max_bytes, in, out, count, dt);
@@ -365,7 +411,7 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
     if (!h) return AR_ERR_INVALID;
     switch (option) {
     case AR_OPT_CTAS_PER_SM:
-        if (value < 1 || value > 32) return AR_ERR_INVALID;
+        if (value < 0 || value > 1024) return AR_ERR_INVALID;
         h->ctas_per_sm = (int)value;
         return AR_OK;
     case AR_OPT_SPIN_NS:
@@ -375,6 +421,10 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
     case AR_OPT_ONE_SHOT_IMPL:
         if (value < 0 || value > 2) return AR_ERR_INVALID;
         h->one_shot_impl = (int)value;
+        return AR_OK;
+    case AR_OPT_TIMING_PAUSE:
+        if (value < 0 || value > 1 || h->timing.capacity == 0) return AR_ERR_INVALID;
+        h->timing.paused = (int)value;
         return AR_OK;
     case AR_OPT_TIMING:
         if (value < 0 || value > (1 << 20)) return AR_ERR_INVALID;
@@ -404,29 +454,59 @@ int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count, 
 int ar_ll_pack(ar_handle h, const float* src, void* lines, size_t count, uint32_t step, ar_stream_t s)
 {
     return single_call(AR_OP_LL_PACK, h, src, lines, count, step, s, [&](Handle& hh, cudaStream_t st) {
-        return launch_ll_pack(hh, src, lines, count, step, st);
+        return launch_ll_pack(hh, 1, &src, &lines, count, step, st);
     });
 }
 
 int ar_ll_unpack(ar_handle h, const void* lines, float* dst, size_t count, uint32_t step, ar_stream_t s)
 {
     return single_call(AR_OP_LL_UNPACK, h, lines, dst, count, step, s, [&](Handle& hh, cudaStream_t st) {
-        return launch_ll_unpack(hh, lines, dst, count, step, st);
+        return launch_ll_unpack(hh, 1, &lines, &dst, count, step, st);
     });
 }
 
 int ar_ll128_pack(ar_handle h, const float* src, void* lines, size_t count, uint64_t step, ar_stream_t s)
 {
     return single_call(AR_OP_LL128_PACK, h, src, lines, count, step, s, [&](Handle& hh, cudaStream_t st) {
-        return launch_ll128_pack(hh, src, lines, count, step, st);
+        return launch_ll128_pack(hh, 1, &src, &lines, count, step, st);
     });
 }
 
 int ar_ll128_unpack(ar_handle h, const void* lines, float* dst, size_t count, uint64_t step, ar_stream_t s)
 {
     return single_call(AR_OP_LL128_UNPACK, h, lines, dst, count, step, s, [&](Handle& hh, cudaStream_t st) {
-        return launch_ll128_unpack(hh, lines, dst, count, step, st);
+        return launch_ll128_unpack(hh, 1, &lines, &dst, count, step, st);
     });
+}
+
+int ar_ll_pack_n(ar_handle h, const float* const* src, void* const* lines, size_t count, uint32_t step,
+                 ar_stream_t s)
+{
+    return batch_call(AR_OP_LL_PACK, h, reinterpret_cast<const void* const*>(src), lines, count, step, s,
+                      [&](Handle& hh, cudaStream_t st) { return launch_ll_pack(hh, hh.n, src, lines, count, step, st); });
+}
+
+int ar_ll_unpack_n(ar_handle h, const void* const* lines, float* const* dst, size_t count, uint32_t step,
+                   ar_stream_t s)
+{
+    return batch_call(AR_OP_LL_UNPACK, h, lines, reinterpret_cast<const void* const*>(dst), count, step, s,
+                      [&](Handle& hh, cudaStream_t st) { return launch_ll_unpack(hh, hh.n, lines, dst, count, step, st); });
+}
+
+int ar_ll128_pack_n(ar_handle h, const float* const* src, void* const* lines, size_t count, uint64_t step,
+                    ar_stream_t s)
+{
+    return batch_call(AR_OP_LL128_PACK, h, reinterpret_cast<const void* const*>(src), lines, count, step, s,
+                      [&](Handle& hh, cudaStream_t st) { return launch_ll128_pack(hh, hh.n, src, lines, count, step, st); });
+}
+
+int ar_ll128_unpack_n(ar_handle h, const void* const* lines, float* const* dst, size_t count, uint64_t step,
+                      ar_stream_t s)
+{
+    return batch_call(AR_OP_LL128_UNPACK, h, lines, reinterpret_cast<const void* const*>(dst), count, step, s,
+                      [&](Handle& hh, cudaStream_t st) {
+                          return launch_ll128_unpack(hh, hh.n, lines, dst, count, step, st);
+                      });
 }
 
 int ar_ll_reduce(ar_handle h, const void* const* in, void* const* out, size_t count, uint32_t step, ar_stream_t s)

@@ -172,6 +172,11 @@ __device__ __forceinline__ void report_flag_timeout(DevStatus* st, int rank, uns
     atomicAdd(&st->skipped, 1ull);
 }
 
+__device__ __forceinline__ void report_wait_timeout(DevStatus* st)
+{
+    atomicCAS(&st->code, 0, AR_ERR_WAIT_TIMEOUT);
+}
+
 // Rank pointer tables, passed by value in the kernel parameters.
 template <int NR> struct CPtrs { const void* p[NR]; };
 template <int NR> struct MPtrs { void* p[NR]; };

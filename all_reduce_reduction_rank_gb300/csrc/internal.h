@@ -26,7 +26,8 @@ struct Timing {
     std::vector<cudaEvent_t> start, stop;
     std::vector<ar_launch_time_t> rec;
     size_t head = 0, count = 0;
-    int op = 0;  // the call being recorded
+    int op = 0;      // the call being recorded
+    int paused = 0;  // AR_OPT_TIMING_PAUSE: keep the events, record nothing
 };
 
 struct Handle {
@@ -34,7 +35,7 @@ struct Handle {
     size_t max_bytes = 0;
     int device = 0;
     int sm_count = 0;
-    int ctas_per_sm = 8;
+    int ctas_per_sm = 0;  // 0: one full wave, from each kernel's occupancy
     int64_t spin_ns = 1000000;
     int one_shot_impl = 0;
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
@@ -49,13 +50,13 @@ struct Handle {
 inline void rec_begin(Handle& h, cudaStream_t s)
 {
     Timing& t = h.timing;
-    if (t.capacity) cudaEventRecord(t.start[t.head], s);
+    if (t.capacity && !t.paused) cudaEventRecord(t.start[t.head], s);
 }
 
 inline void rec_end(Handle& h, cudaStream_t s, int kernel, uint64_t hbm_bytes)
 {
     Timing& t = h.timing;
-    if (!t.capacity) return;
+    if (!t.capacity || t.paused) return;
     cudaEventRecord(t.stop[t.head], s);
     t.rec[t.head] = ar_launch_time_t{kernel, t.op, 0.0f, hbm_bytes};
     t.head = (t.head + 1) % (size_t)t.capacity;
@@ -72,11 +73,45 @@ inline size_t chunk_elems(int n, size_t N, int dt)
     return (per + q - 1) / q * q;
 }
 
+// CTAs of `kernel` (kThreads threads, no dynamic shared memory) that fit on
+// one SM at once.  Callers cache it in a function-local static per kernel
+// instantiation.
+template <typename K>
+inline int blocks_per_sm(K kernel, size_t dyn_smem = 0)
+{
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, dyn_smem) != cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    return b;
+}
+
+// Grid sizing of the streaming kernels.  Measured on GB300 (n = 8 bf16,
+// 8 and 64 MiB per rank, CTAs/SM swept 1..1024): many short-lived CTAs, up
+// to about one tile each, beat one resident wave of grid-striding CTAs by
+// 5-14% (the block scheduler balances the SMs; a static split does not), and
+// the gain is flat from 32 to 1024 CTAs/SM.  So the default caps the grid at
+// kAutoCtasPerSm CTAs per SM and the kernels grid-stride past that.
+constexpr int kAutoCtasPerSm = 64;
+
 // CTAs for a streaming kernel that needs `work` thread-iterations.
 inline unsigned grid_for(const Handle& h, size_t work)
 {
     size_t want = (work + kThreads - 1) / kThreads;
-    size_t cap = (size_t)h.sm_count * (size_t)h.ctas_per_sm;
+    size_t cap = (size_t)h.sm_count * (size_t)(h.ctas_per_sm ? h.ctas_per_sm : kAutoCtasPerSm);
+    if (want > cap) want = cap;
+    return want ? (unsigned)want : 1u;
+}
+
+// blockIdx.x extent for a 2-D grid of `rows` rows (blockIdx.y) that each need
+// `work` thread-iterations, within the same CTA budget.
+inline unsigned grid_for_rows(const Handle& h, size_t work, int rows)
+{
+    size_t want = (work + kThreads - 1) / kThreads;
+    size_t total = (size_t)h.sm_count * (size_t)(h.ctas_per_sm ? h.ctas_per_sm : kAutoCtasPerSm);
+    size_t cap = total / (size_t)rows;
+    if (cap == 0) cap = 1;
     if (want > cap) want = cap;
     return want ? (unsigned)want : 1u;
 }
@@ -88,16 +123,16 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
                     cudaStream_t s, int* launches);
 int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                 cudaStream_t s, int* launches);
-int launch_ll_pack(Handle& h, const float* src, void* lines, size_t count, uint32_t step,
+int launch_ll_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint32_t step,
                    cudaStream_t s);
-int launch_ll_unpack(Handle& h, const void* lines, float* dst, size_t count, uint32_t step,
+int launch_ll_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count, uint32_t step,
                      cudaStream_t s);
 int launch_ll_reduce(Handle& h, const void* const* in, void* const* out, size_t count,
                      uint32_t step, cudaStream_t s);
-int launch_ll128_pack(Handle& h, const float* src, void* lines, size_t count, uint64_t step,
+int launch_ll128_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint64_t step,
                       cudaStream_t s);
-int launch_ll128_unpack(Handle& h, const void* lines, float* dst, size_t count, uint64_t step,
-                        cudaStream_t s);
+int launch_ll128_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count,
+                        uint64_t step, cudaStream_t s);
 int launch_ll128_reduce(Handle& h, const void* const* in, void* const* out, size_t count,
                         uint64_t step, cudaStream_t s);
 

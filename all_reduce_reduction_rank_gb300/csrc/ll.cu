@@ -49,9 +49,17 @@ __device__ __forceinline__ uint64_t max_polls(int64_t spin_ns) { return (uint64_
 
 // ---------------------------------------------------------------- LL -------
 
+// Pack / unpack kernels take a table of buffers; blockIdx.y picks one, so a
+// single launch serves one buffer or all n ranks' buffers.
+struct SrcTable { const void* p[kMaxRanks]; };
+struct DstTable { void* p[kMaxRanks]; };
+
 __global__ void __launch_bounds__(kThreads)
-ll_pack_kernel(const float* __restrict__ src, uint4* __restrict__ lines, size_t count, uint32_t step)
+ll_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__ DstTable outs, size_t count,
+               uint32_t step)
 {
+    const float* const src = static_cast<const float*>(srcs.p[blockIdx.y]);
+    uint4* const lines = static_cast<uint4*>(outs.p[blockIdx.y]);
     const size_t nq = count / 4;  // 4 payload words -> 2 x 16 B of lines
     for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nq; v += (size_t)gridDim.x * kThreads) {
         const uint4 x = ld16(src + 4 * v);
@@ -65,9 +73,12 @@ ll_pack_kernel(const float* __restrict__ src, uint4* __restrict__ lines, size_t 
 }
 
 __global__ void __launch_bounds__(kThreads)
-ll_unpack_kernel(const uint4* __restrict__ lines, float* __restrict__ dst, size_t count, uint32_t step,
-                 int64_t spin_ns, DevStatus* st)
+ll_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant__ DstTable dsts, size_t count,
+                 uint32_t step, int64_t spin_ns, DevStatus* st)
 {
+    const int rank = blockIdx.y;
+    const uint4* const lines = static_cast<const uint4*>(ins.p[rank]);
+    float* const dst = static_cast<float*>(dsts.p[rank]);
     const size_t nq = count / 4;
     for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nq; v += (size_t)gridDim.x * kThreads) {
         uint4 a = ld16(lines + 2 * v), b = ld16(lines + 2 * v + 1);
@@ -88,7 +99,7 @@ ll_unpack_kernel(const uint4* __restrict__ lines, float* __restrict__ dst, size_
             const uint32_t d[4] = {a.x, a.z, b.x, b.z}, f[4] = {a.y, a.w, b.y, b.w};
             for (int j = 0; j < 4; ++j) {
                 if (f[j] == step) dst[4 * v + j] = __uint_as_float(d[j]);
-                else report_flag_timeout(st, 0, 4 * v + j);
+                else report_flag_timeout(st, rank, 4 * v + j);
             }
         }
     }
@@ -104,7 +115,7 @@ ll_unpack_kernel(const uint4* __restrict__ lines, float* __restrict__ dst, size_
                 if ((int64_t)(globaltimer_ns() - t0) > spin_ns) break;
             }
             if (x.y == step) dst[i] = __uint_as_float(x.x);
-            else report_flag_timeout(st, 0, i);
+            else report_flag_timeout(st, rank, i);
         }
     }
 }
@@ -208,8 +219,11 @@ __device__ __forceinline__ uint64_t group_flag(const uint4& v, int leader)
 }
 
 __global__ void __launch_bounds__(kThreads)
-ll128_pack_kernel(const float* __restrict__ src, uint4* __restrict__ lines, size_t count, uint64_t step)
+ll128_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__ DstTable outs, size_t count,
+                  uint64_t step)
 {
+    const float* const src = static_cast<const float*>(srcs.p[blockIdx.y]);
+    uint4* const lines = static_cast<uint4*>(outs.p[blockIdx.y]);
     const size_t L = (count + 29) / 30;
     const size_t warp = ((size_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = ((size_t)gridDim.x * kThreads) >> 5;
@@ -241,9 +255,12 @@ ll128_pack_kernel(const float* __restrict__ src, uint4* __restrict__ lines, size
 }
 
 __global__ void __launch_bounds__(kThreads)
-ll128_unpack_kernel(const uint4* __restrict__ lines, float* __restrict__ dst, size_t count, uint64_t step,
-                    int64_t spin_ns, DevStatus* st)
+ll128_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant__ DstTable dsts, size_t count,
+                    uint64_t step, int64_t spin_ns, DevStatus* st)
 {
+    const int rank = blockIdx.y;
+    const uint4* const lines = static_cast<const uint4*>(ins.p[rank]);
+    float* const dst = static_cast<float*>(dsts.p[rank]);
     const size_t L = (count + 29) / 30;
     const size_t warp = ((size_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = ((size_t)gridDim.x * kThreads) >> 5;
@@ -278,7 +295,7 @@ ll128_unpack_kernel(const uint4* __restrict__ lines, float* __restrict__ dst, si
                     if (e0 + t < count) dst[e0 + t] = __uint_as_float(w[t]);
             }
         } else if (ln.j == 0) {
-            report_flag_timeout(st, 0, ln.k);
+            report_flag_timeout(st, rank, ln.k);
         }
     }
 }
@@ -346,20 +363,38 @@ ll128_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 
 }  // namespace
 
-int launch_ll_pack(Handle& h, const float* src, void* lines, size_t count, uint32_t step, cudaStream_t s)
+// Tables of `nb` buffers (1 for the single-buffer calls, n for the batched ones).
+static void tables(int nb, const void* const* src, void* const* dst, SrcTable& st, DstTable& dt)
 {
+    for (int i = 0; i < kMaxRanks; ++i) {
+        st.p[i] = i < nb ? src[i] : nullptr;
+        dt.p[i] = i < nb ? dst[i] : nullptr;
+    }
+}
+
+int launch_ll_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint32_t step,
+                   cudaStream_t s)
+{
+    SrcTable st;
+    DstTable dt;
+    tables(nb, reinterpret_cast<const void* const*>(src), lines, st, dt);
+    const dim3 grid(grid_for_rows(h, count / 4, nb), nb);
     rec_begin(h, s);
-    ll_pack_kernel<<<grid_for(h, count / 4), kThreads, 0, s>>>(src, static_cast<uint4*>(lines), count, step);
-    rec_end(h, s, AR_K_LL_PACK, 12ull * count);
+    ll_pack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step);
+    rec_end(h, s, AR_K_LL_PACK, 12ull * count * nb);
     return launch_status();
 }
 
-int launch_ll_unpack(Handle& h, const void* lines, float* dst, size_t count, uint32_t step, cudaStream_t s)
+int launch_ll_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count, uint32_t step,
+                     cudaStream_t s)
 {
+    SrcTable st;
+    DstTable dt;
+    tables(nb, lines, reinterpret_cast<void* const*>(dst), st, dt);
+    const dim3 grid(grid_for_rows(h, count / 4, nb), nb);
     rec_begin(h, s);
-    ll_unpack_kernel<<<grid_for(h, count / 4), kThreads, 0, s>>>(static_cast<const uint4*>(lines), dst, count,
-                                                                step, h.spin_ns, h.status);
-    rec_end(h, s, AR_K_LL_UNPACK, 12ull * count);
+    ll_unpack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step, h.spin_ns, h.status);
+    rec_end(h, s, AR_K_LL_UNPACK, 12ull * count * nb);
     return launch_status();
 }
 
@@ -375,30 +410,38 @@ int launch_ll_reduce(Handle& h, const void* const* in, void* const* out, size_t 
             op.p[q] = out[q];
         }
         rec_begin(h, s);
-        ll_reduce_kernel<NR><<<grid_for(h, (count + 1) / 2), kThreads, 0, s>>>(ip, op, count, step, h.spin_ns,
-                                                                               h.status);
+        ll_reduce_kernel<NR><<<grid_for(h, (count + 1) / 2), kThreads, 0, s>>>(ip, op, count, step,
+                                                                                       h.spin_ns, h.status);
         rec_end(h, s, AR_K_LL_REDUCE, 16ull * NR * count);
         return launch_status();
     });
 }
 
-int launch_ll128_pack(Handle& h, const float* src, void* lines, size_t count, uint64_t step, cudaStream_t s)
+int launch_ll128_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint64_t step,
+                      cudaStream_t s)
 {
+    SrcTable st;
+    DstTable dt;
+    tables(nb, reinterpret_cast<const void* const*>(src), lines, st, dt);
     const size_t L = (count + 29) / 30;
+    const dim3 grid(grid_for_rows(h, L * 8, nb), nb);
     rec_begin(h, s);
-    ll128_pack_kernel<<<grid_for(h, L * 8), kThreads, 0, s>>>(src, static_cast<uint4*>(lines), count, step);
-    rec_end(h, s, AR_K_LL128_PACK, 4ull * count + 128ull * L);
+    ll128_pack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step);
+    rec_end(h, s, AR_K_LL128_PACK, (4ull * count + 128ull * L) * nb);
     return launch_status();
 }
 
-int launch_ll128_unpack(Handle& h, const void* lines, float* dst, size_t count, uint64_t step,
-                        cudaStream_t s)
+int launch_ll128_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count,
+                        uint64_t step, cudaStream_t s)
 {
+    SrcTable st;
+    DstTable dt;
+    tables(nb, lines, reinterpret_cast<void* const*>(dst), st, dt);
     const size_t L = (count + 29) / 30;
+    const dim3 grid(grid_for_rows(h, L * 8, nb), nb);
     rec_begin(h, s);
-    ll128_unpack_kernel<<<grid_for(h, L * 8), kThreads, 0, s>>>(static_cast<const uint4*>(lines), dst, count,
-                                                                 step, h.spin_ns, h.status);
-    rec_end(h, s, AR_K_LL128_UNPACK, 4ull * count + 128ull * L);
+    ll128_unpack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step, h.spin_ns, h.status);
+    rec_end(h, s, AR_K_LL128_UNPACK, (4ull * count + 128ull * L) * nb);
     return launch_status();
 }
 
@@ -416,7 +459,7 @@ int launch_ll128_reduce(Handle& h, const void* const* in, void* const* out, size
         const size_t L = (count + 29) / 30;
         rec_begin(h, s);
         ll128_reduce_kernel<NR><<<grid_for(h, L * 8), kThreads, 0, s>>>(ip, op, count, step, h.spin_ns,
-                                                                        h.status);
+                                                                                h.status);
         rec_end(h, s, AR_K_LL128_REDUCE, 256ull * NR * L);
         return launch_status();
     });

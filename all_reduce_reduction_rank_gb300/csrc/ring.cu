@@ -25,97 +25,131 @@
 namespace argb {
 namespace {
 
-// Reduce-scatter step s of the ring.  Work item w = (r, k): vector k of the
-// chunk that rank r sends.  p_read / p_write: fp32 partials, rank-major, C
-// elements per rank.
+constexpr int kRsUnroll = 2;  // vectors per thread per iteration
+constexpr int kAgUnroll = 4;
+
+// Reduce-scatter step s.  Grid: blockIdx.y = sending rank r (block-uniform
+// chunk, pointers and step role), blockIdx.x strides over the chunk's 16-byte
+// vectors.  p_read / p_write: fp32 partials, rank-major, C elements per rank.
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
-ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, const float* __restrict__ p_read,
-                    float* __restrict__ p_write, size_t C, size_t count, int s)
+ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
+                    const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s)
 {
     constexpr int VE = kVecElems<DT>;
+    constexpr int PW = VE / 4;          // 16-byte words of fp32 partial per payload vector
+    constexpr int U = kRsUnroll;
     using T = typename Payload<DT>::scalar_t;
+    const int r = blockIdx.y;
+    const int d = (r + 1) % NR;
+    const int c = (r - s + NR) % NR;
     const bool first = (s == 0), last = (s == NR - 2);
-    const size_t cvec = C / VE;
-    const size_t total = (size_t)NR * cvec;
-    for (size_t w = (size_t)blockIdx.x * kThreads + threadIdx.x; w < total;
-         w += (size_t)gridDim.x * kThreads) {
-        const int r = (int)(w / cvec);
-        const size_t k = w - (size_t)r * cvec;
-        const int d = (r + 1) % NR;
-        const int c = (r - s + NR) % NR;
-        const size_t e0 = (size_t)c * C + k * VE;  // first element of this vector
-        if (e0 >= count) continue;
-        const float* pr = p_read + (size_t)r * C + k * VE;
-        float* pw = p_write + (size_t)d * C + k * VE;
-        float a[VE];
-        if (e0 + VE <= count) {
-            // upstream partial (the sender's payload at step 0) ...
-            if (first) {
-                const uint4 xr = ld16(static_cast<const T*>(in.p[r]) + e0);
+    const size_t e_lo = (size_t)c * C;
+    if (e_lo >= count) return;
+    const size_t len = count - e_lo < C ? count - e_lo : C;   // elements of chunk c
+    const size_t nv = len / VE;                                 // whole vectors
+    const T* const xr = static_cast<const T*>(in.p[r]) + e_lo;
+    const T* const xd = static_cast<const T*>(in.p[d]) + e_lo;
+    T* const od = static_cast<T*>(out.p[d]) + e_lo;
+    const float* const pr = p_read + (size_t)r * C;
+    float* const pw = p_write + (size_t)d * C;
+    const size_t span = (size_t)kThreads * U;
+    for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
+        uint4 up[U][PW], own[U];
 #pragma unroll
-                for (int j = 0; j < VE; ++j) a[j] = 0.0f;
-                // 0 + x is x except for -0: widen exactly instead of adding.
+        for (int u = 0; u < U; ++u) {
+            const size_t k = base + (size_t)u * kThreads + threadIdx.x;
+            if (k < nv) {
+                // the partial rank r sends (its own payload at step 0) ...
+                if (first) {
+                    up[u][0] = ld16(xr + k * VE);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(xr, j), a + j * Payload<DT>::kPerWord);
-            } else {
+                    for (int j = 0; j < PW; ++j) up[u][j] = ld16(pr + k * VE + 4 * j);
+                }
+                // ... and the receiver's own chunk
+                own[u] = ld16(xd + k * VE);
+            }
+        }
 #pragma unroll
-                for (int j = 0; j < VE / 4; ++j) {
-                    const uint4 t = ld16(pr + 4 * j);
-                    a[4 * j + 0] = __uint_as_float(t.x);
-                    a[4 * j + 1] = __uint_as_float(t.y);
-                    a[4 * j + 2] = __uint_as_float(t.z);
-                    a[4 * j + 3] = __uint_as_float(t.w);
+        for (int u = 0; u < U; ++u) {
+            const size_t k = base + (size_t)u * kThreads + threadIdx.x;
+            if (k < nv) {
+                float a[VE];
+                if (first) {
+                    // widen exactly (no zero start: the first hop adds two raw values)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        Payload<DT>::widen(word(up[u][0], j), a + j * Payload<DT>::kPerWord);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < PW; ++j) {
+                        a[4 * j + 0] = __uint_as_float(up[u][j].x);
+                        a[4 * j + 1] = __uint_as_float(up[u][j].y);
+                        a[4 * j + 2] = __uint_as_float(up[u][j].z);
+                        a[4 * j + 3] = __uint_as_float(up[u][j].w);
+                    }
+                }
+                accumulate<DT>(a, own[u]);
+                if (last) {
+                    st16(od + k * VE, round_vec<DT>(a));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < PW; ++j)
+                        st16(pw + k * VE + 4 * j,
+                             make_uint4(__float_as_uint(a[4 * j]), __float_as_uint(a[4 * j + 1]),
+                                        __float_as_uint(a[4 * j + 2]), __float_as_uint(a[4 * j + 3])));
                 }
             }
-            // ... plus the receiver's own chunk
-            const uint4 xd = ld16(static_cast<const T*>(in.p[d]) + e0);
-            accumulate<DT>(a, xd);
-            if (last) {
-                st16(static_cast<T*>(out.p[d]) + e0, round_vec<DT>(a));
-            } else {
-#pragma unroll
-                for (int j = 0; j < VE / 4; ++j)
-                    st16(pw + 4 * j, make_uint4(__float_as_uint(a[4 * j]), __float_as_uint(a[4 * j + 1]),
-                                                __float_as_uint(a[4 * j + 2]), __float_as_uint(a[4 * j + 3])));
-            }
-        } else {
-            // the ragged end of the last chunk: element by element
-            const size_t m = count - e0;
-            for (size_t j = 0; j < m; ++j) {
-                const float up = first ? Payload<DT>::widen1(static_cast<const T*>(in.p[r])[e0 + j]) : pr[j];
-                const float sum = up + Payload<DT>::widen1(static_cast<const T*>(in.p[d])[e0 + j]);
-                if (last) static_cast<T*>(out.p[d])[e0 + j] = Payload<DT>::narrow1(sum);
-                else pw[j] = sum;
-            }
+        }
+    }
+    // the ragged end of the last chunk: one element per thread
+    if (blockIdx.x == gridDim.x - 1) {
+        const size_t j = nv * VE + threadIdx.x;
+        if (j < len) {
+            const float upv = first ? Payload<DT>::widen1(xr[j]) : pr[j];
+            const float sum = upv + Payload<DT>::widen1(xd[j]);
+            if (last) od[j] = Payload<DT>::narrow1(sum);
+            else pw[j] = sum;
         }
     }
 }
 
 // All-gather step s: out[r+1][chunk (r+1-s)] = out[r][chunk (r+1-s)].
+// Grid: blockIdx.y = sending rank r.
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
 ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t count, int s)
 {
     constexpr int VE = kVecElems<DT>;
+    constexpr int U = kAgUnroll;
     using T = typename Payload<DT>::scalar_t;
-    const size_t cvec = C / VE;
-    const size_t total = (size_t)NR * cvec;
-    for (size_t w = (size_t)blockIdx.x * kThreads + threadIdx.x; w < total;
-         w += (size_t)gridDim.x * kThreads) {
-        const int r = (int)(w / cvec);
-        const size_t k = w - (size_t)r * cvec;
-        const int d = (r + 1) % NR;
-        const int c = (r + 1 - s + NR) % NR;
-        const size_t e0 = (size_t)c * C + k * VE;
-        if (e0 >= count) continue;
-        const T* src = static_cast<const T*>(out.p[r]) + e0;
-        T* dst = static_cast<T*>(out.p[d]) + e0;
-        if (e0 + VE <= count) {
-            st16(dst, ld16(src));
-        } else {
-            for (size_t j = 0; j < count - e0; ++j) dst[j] = src[j];
+    const int r = blockIdx.y;
+    const int d = (r + 1) % NR;
+    const int c = (r + 1 - s + NR) % NR;
+    const size_t e_lo = (size_t)c * C;
+    if (e_lo >= count) return;
+    const size_t len = count - e_lo < C ? count - e_lo : C;
+    const size_t nv = len / VE;
+    const T* const src = static_cast<const T*>(out.p[r]) + e_lo;
+    T* const dst = static_cast<T*>(out.p[d]) + e_lo;
+    const size_t span = (size_t)kThreads * U;
+    for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t k = base + (size_t)u * kThreads + threadIdx.x;
+            if (k < nv) x[u] = ld16(src + k * VE);
         }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const size_t k = base + (size_t)u * kThreads + threadIdx.x;
+            if (k < nv) st16(dst + k * VE, x[u]);
+        }
+    }
+    if (blockIdx.x == gridDim.x - 1) {
+        const size_t j = nv * VE + threadIdx.x;
+        if (j < len) dst[j] = src[j];
     }
 }
 
@@ -136,7 +170,9 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
             }
             const size_t C = chunk_elems(NR, count, DT);
             if (C > h.ring_chunk_max) return AR_ERR_TOO_LARGE;
-            const unsigned grid = grid_for(h, (size_t)NR * (C / kVecElems<DT>));
+            const size_t cvec = C / kVecElems<DT>;
+            const dim3 g_rs(grid_for_rows(h, (cvec + kRsUnroll - 1) / kRsUnroll, NR), NR);
+            const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
             float* buf[2] = {h.ring_scratch, h.ring_scratch + (size_t)NR * C};
             int n_launch = 0;
             // per step every chunk moves once: N elements in all
@@ -145,7 +181,7 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
                 const uint64_t rd = (step == 0 ? e : 4) * N + e * N;
                 const uint64_t wr = (step == NR - 2 ? e : 4) * N;
                 rec_begin(h, s);
-                ring_rs_step_kernel<NR, DT><<<grid, kThreads, 0, s>>>(
+                ring_rs_step_kernel<NR, DT><<<g_rs, kThreads, 0, s>>>(
                     ip, op, buf[(step + 1) & 1], buf[step & 1], C, count, step);
                 rec_end(h, s, AR_K_RING_RS_STEP, rd + wr);
                 ++n_launch;
@@ -153,7 +189,7 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
             }
             for (int step = 0; step < NR - 1; ++step) {
                 rec_begin(h, s);
-                ring_ag_step_kernel<NR, DT><<<grid, kThreads, 0, s>>>(op, C, count, step);
+                ring_ag_step_kernel<NR, DT><<<g_ag, kThreads, 0, s>>>(op, C, count, step);
                 rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;

@@ -20,19 +20,27 @@ namespace {
 template <int NR> __host__ __device__ constexpr int rs_unroll() { return NR <= 4 ? 4 : NR <= 8 ? 2 : 1; }
 constexpr int kAgUnroll = 4;
 
+// Grid: blockIdx.y = chunk r (block-uniform output pointer, no per-vector
+// division), blockIdx.x strides over the chunk's 16-byte vectors.
+
 // out[r][v] = rank-order sum of in[*][v] for v in chunk r.
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
-reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count, size_t cvec)
+reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
+                      size_t count, size_t cvec)
 {
     constexpr int U = rs_unroll<NR>();
+    const int r = blockIdx.y;
+    const size_t lo = (size_t)r * cvec;
+    const size_t hi = lo + cvec < nvec ? lo + cvec : nvec;
+    uint4* const dst = static_cast<uint4*>(out.p[r]);
     const size_t span = (size_t)kThreads * U;
-    for (size_t base = (size_t)blockIdx.x * span; base < nvec; base += (size_t)gridDim.x * span) {
+    for (size_t base = lo + (size_t)blockIdx.x * span; base < hi; base += (size_t)gridDim.x * span) {
         uint4 x[U][NR];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const size_t v = base + (size_t)u * kThreads + threadIdx.x;
-            if (v < nvec) {
+            if (v < hi) {
 #pragma unroll
                 for (int q = 0; q < NR; ++q) x[u][q] = ld16(static_cast<const uint4*>(in.p[q]) + v);
             }
@@ -40,13 +48,11 @@ reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constan
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const size_t v = base + (size_t)u * kThreads + threadIdx.x;
-            if (v < nvec) {
-                const uint4 r = reduce_rank_order<DT, NR>(x[u]);
-                st16(static_cast<uint4*>(out.p[v / cvec]) + v, r);
-            }
+            if (v < hi) st16(dst + v, reduce_rank_order<DT, NR>(x[u]));
         }
     }
-    if (blockIdx.x == gridDim.x - 1) {
+    // elements past the last whole vector, handled once by the grid's last block
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1) {
         using T = typename Payload<DT>::scalar_t;
         const size_t i = nvec * kVecElems<DT> + threadIdx.x;
         if (i < count) {
@@ -64,34 +70,37 @@ __global__ void __launch_bounds__(kThreads)
 all_gather_kernel(const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count, size_t cvec)
 {
     constexpr int U = kAgUnroll;
+    const int j = blockIdx.y;
+    const size_t lo = (size_t)j * cvec;
+    const size_t hi = lo + cvec < nvec ? lo + cvec : nvec;
+    const uint4* const src = static_cast<const uint4*>(out.p[j]);
     const size_t span = (size_t)kThreads * U;
-    for (size_t base = (size_t)blockIdx.x * span; base < nvec; base += (size_t)gridDim.x * span) {
+    for (size_t base = lo + (size_t)blockIdx.x * span; base < hi; base += (size_t)gridDim.x * span) {
         uint4 x[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const size_t v = base + (size_t)u * kThreads + threadIdx.x;
-            if (v < nvec) x[u] = ld16(static_cast<const uint4*>(out.p[v / cvec]) + v);
+            if (v < hi) x[u] = ld16(src + v);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const size_t v = base + (size_t)u * kThreads + threadIdx.x;
-            if (v < nvec) {
-                const int j = (int)(v / cvec);
+            if (v < hi) {
 #pragma unroll
                 for (int q = 0; q < NR; ++q)
                     if (q != j) st16(static_cast<uint4*>(out.p[q]) + v, x[u]);
             }
         }
     }
-    if (blockIdx.x == gridDim.x - 1) {
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1) {
         using T = typename Payload<DT>::scalar_t;
         const size_t i = nvec * kVecElems<DT> + threadIdx.x;
         if (i < count) {
-            const int j = (int)(i / (cvec * kVecElems<DT>));
-            const T x = static_cast<const T*>(out.p[j])[i];
+            const int jt = (int)(i / (cvec * kVecElems<DT>));
+            const T x = static_cast<const T*>(out.p[jt])[i];
 #pragma unroll
             for (int q = 0; q < NR; ++q)
-                if (q != j) static_cast<T*>(out.p[q])[i] = x;
+                if (q != jt) static_cast<T*>(out.p[q])[i] = x;
         }
     }
 }
@@ -115,14 +124,14 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
             const size_t cvec = chunk_elems(NR, count, DT) / kVecElems<DT>;  // >= 1 for count >= 1
             constexpr int U = rs_unroll<NR>();
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            const dim3 g_rs(grid_for_rows(h, (cvec + U - 1) / U, NR), NR);
+            const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
             rec_begin(h, s);
-            reduce_scatter_kernel<NR, DT><<<grid_for(h, (nvec + U - 1) / U), kThreads, 0, s>>>(
-                ip, op, nvec, count, cvec);
+            reduce_scatter_kernel<NR, DT><<<g_rs, kThreads, 0, s>>>(ip, op, nvec, count, cvec);
             rec_end(h, s, AR_K_REDUCE_SCATTER, (uint64_t)(NR + 1) * S);
             if (launch_status() != AR_OK) return AR_ERR_CUDA;
             rec_begin(h, s);
-            all_gather_kernel<NR, DT><<<grid_for(h, (nvec + kAgUnroll - 1) / kAgUnroll), kThreads, 0, s>>>(
-                op, nvec, count, cvec);
+            all_gather_kernel<NR, DT><<<g_ag, kThreads, 0, s>>>(op, nvec, count, cvec);
             rec_end(h, s, AR_K_ALL_GATHER, (uint64_t)NR * S);
             *launches = 2;
             return launch_status();

@@ -92,9 +92,9 @@ def step_bytes(n: int, N: int, e: int, ll_count: int) -> dict:
     for kind, (pk, rd, up) in (("ll", (ar.AR_OP_LL_PACK, ar.AR_OP_LL_REDUCE, ar.AR_OP_LL_UNPACK)),
                                ("ll128", (ar.AR_OP_LL128_PACK, ar.AR_OP_LL128_REDUCE, ar.AR_OP_LL128_UNPACK))):
         b = 0
-        for op, k in ((pk, n), (rd, 1), (up, n)):
+        for op in (pk, rd, up):          # pack / unpack over all n buffers in one call
             t = ar.ar_plan(op, n, ll_count, "f32")
-            b += k * (t.hbm_read_bytes + t.hbm_write_bytes)
+            b += t.hbm_read_bytes + t.hbm_write_bytes
         rows[kind] = b
     return rows
 
@@ -245,9 +245,11 @@ class Workload:
         self.p_in, self.p_out = P(self.ins), P(self.outs)
         self.p_ll, self.p_llr = P(self.ll_lines), P(self.ll_red)
         self.p_l128, self.p_l128r = P(self.l128_lines), P(self.l128_red)
+        self.p_pay = P(self.pay)
+        self.p_lld, self.p_l128d = P(self.ll_dst), P(self.l128_dst)
         self.L = ar.lib()
         self.step_id = 0
-        self.launches_per_step = 1 + 2 + 2 * (n - 1) + 2 * (2 * n + 1)
+        self.launches_per_step = 1 + 2 + 2 * (n - 1) + 2 * 3
 
     def run(self):
         L, h, s, n, N, c = self.L, self.h, self.s, self.n, self.N, self.ll_count
@@ -256,16 +258,12 @@ class Workload:
         rc = L.ar_one_shot(h, self.p_in, self.p_out, N, 1, s)
         rc |= L.ar_two_shot(h, self.p_in, self.p_out, N, 1, s)
         rc |= L.ar_ring(h, self.p_in, self.p_out, N, 1, s)
-        for r in range(n):
-            rc |= L.ar_ll_pack(h, self.pay[r].data_ptr(), self.ll_lines[r].data_ptr(), c, k, s)
+        rc |= L.ar_ll_pack_n(h, self.p_pay, self.p_ll, c, k, s)
         rc |= L.ar_ll_reduce(h, self.p_ll, self.p_llr, c, k, s)
-        for r in range(n):
-            rc |= L.ar_ll_unpack(h, self.ll_red[r].data_ptr(), self.ll_dst[r].data_ptr(), c, k, s)
-        for r in range(n):
-            rc |= L.ar_ll128_pack(h, self.pay[r].data_ptr(), self.l128_lines[r].data_ptr(), c, k, s)
+        rc |= L.ar_ll_unpack_n(h, self.p_llr, self.p_lld, c, k, s)
+        rc |= L.ar_ll128_pack_n(h, self.p_pay, self.p_l128, c, k, s)
         rc |= L.ar_ll128_reduce(h, self.p_l128, self.p_l128r, c, k, s)
-        for r in range(n):
-            rc |= L.ar_ll128_unpack(h, self.l128_red[r].data_ptr(), self.l128_dst[r].data_ptr(), c, k, s)
+        rc |= L.ar_ll128_unpack_n(h, self.p_l128r, self.p_l128d, c, k, s)
         if rc:
             raise RuntimeError(f"a C-ABI call failed in step {k}")
 
@@ -274,19 +272,24 @@ class Workload:
         ar.check(ar.ar_destroy(self.h), "ar_destroy")
 
 
-def time_steps(wl, K: int) -> float:
-    """Device ms of exactly K steps, bracketed by a barrier + synchronize."""
+def time_steps(wl, K: int, before_step=None) -> tuple[float, float]:
+    """Device ms of exactly K steps, bracketed by a barrier + synchronize, and
+    the host ms spent issuing them."""
     import torch
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     ev0.record(wl.stream)
-    for _ in range(K):
+    t0 = time.perf_counter()
+    for i in range(K):
+        if before_step is not None:
+            before_step(i)
         wl.run()
+    host_ms = 1e3 * (time.perf_counter() - t0)
     ev1.record(wl.stream)
     torch.cuda.synchronize()
     barrier()
-    return ev0.elapsed_time(ev1)
+    return ev0.elapsed_time(ev1), host_ms
 
 
 def per_kernel(records, K: int, peak: float) -> dict:
@@ -308,14 +311,16 @@ def per_kernel(records, K: int, peak: float) -> dict:
 
 def sweep(wl, peak: float, iters_small: int = 200, iters_large: int = 50) -> dict:
     """one-shot and two-shot over the decode and prefill message sizes (n = 8,
-    bf16): per size the median of CUDA-event-timed calls, L2 flushed (a
-    256 MiB write) before every call, outside the timed interval."""
+    bf16): per size the median of CUDA-event-timed calls.  Before every call,
+    outside the timed interval, a 256 MiB buffer (2x L2) is read, which
+    evicts the previous call's lines (writing back the dirty ones) and leaves
+    the L2 clean, so no call starts with its data, or with dirty lines, in L2."""
     import torch
 
     import all_reduce_reduction_rank_gb300 as ar
     import workloads
 
-    flush = torch.empty(256 * MiB, dtype=torch.uint8, device=wl.dev)
+    flush = torch.ones(64 * MiB, dtype=torch.int32, device=wl.dev)
     sizes = sorted({2 * c for c in workloads.CONFIGS[2]["counts"]} | {2 * c for c in workloads.CONFIGS[3]["counts"]})
     res = {"one_shot": [], "two_shot": []}
     n = wl.n
@@ -331,7 +336,7 @@ def sweep(wl, peak: float, iters_small: int = 200, iters_large: int = 50) -> dic
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
             with torch.cuda.stream(wl.stream):
                 for e0, e1 in evs:
-                    flush.fill_(0x5A)
+                    flush.sum()
                     e0.record(wl.stream)
                     ar.check(call(wl.h, wl.p_in, wl.p_out, N, 1, wl.s), algo)
                     e1.record(wl.stream)
@@ -397,6 +402,8 @@ def run_ours(args):
     ar.lib()                                   # fails loudly if the library is not built
     n, S, ll_count = 8, args.size_mib * MiB, (1 * MiB) // 4
     wl = Workload(n, S, ll_count, dev, seed=1003)
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_ONE_SHOT_IMPL, args.one_shot_impl))
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_CTAS_PER_SM, args.ctas_per_sm))
     peak, peak_src = measured_peak()
     rows = step_bytes(n, wl.N, 2, ll_count)
     bytes_step = sum(rows.values())
@@ -404,7 +411,15 @@ def run_ours(args):
         wl.run()
     torch.cuda.synchronize()
     ar.check(ar.ar_status(wl.h), "warm-up status")
-    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_TIMING, min(1 << 20, wl.launches_per_step * args.steps)))
+    # per-launch events on every k-th timed step only (each event pair costs a
+    # little device time between launches); the others run unrecorded
+    every = max(1, args.timing_every)
+    sampled = (args.steps + every - 1) // every
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_TIMING, min(1 << 20, wl.launches_per_step * sampled)))
+    L = ar.lib()
+
+    def sample(i):
+        L.ar_set_option(wl.h, ar.AR_OPT_TIMING_PAUSE, 0 if i % every == 0 else 1)
 
     try:
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
@@ -413,7 +428,7 @@ def run_ours(args):
     clocks = ClockSampler(bus)
     clocks.start()
     t_wall0 = time.time()
-    ms = time_steps(wl, args.steps)
+    ms, host_ms = time_steps(wl, args.steps, sample)
     t_wall1 = time.time()
     clocks.stop()
     records = ar.ar_timing(wl.h)
@@ -422,7 +437,7 @@ def run_ours(args):
     ms_max = reduce_scalar(ms, "max")
     total_bytes = reduce_scalar(bytes_step * args.steps, "sum")
     value = total_bytes / (ms_max * 1e-3) / 1e9
-    kernels = per_kernel(records, args.steps, peak)
+    kernels = per_kernel(records, sampled, peak)
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     dk = kernels[dom]
     traffic = ncu_traffic(dom, dk["bytes_per_launch"])
@@ -448,7 +463,9 @@ def run_ours(args):
                    "l2": "inputs larger than L2: 1.3 GiB touched per step vs 129 MB L2; no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "frac_of_peak": round(value / world / peak, 4), "frac_of_8tbs": round(value / world / NOMINAL_PEAK_GBS, 4),
-        "roofline": roofline, "kernels": kernels, "gpu_launches": len(records),
+        "roofline": roofline, "kernels": kernels, "gpu_launches": wl.launches_per_step * args.steps,
+        "launch_timing": {"steps_sampled": sampled, "every": every, "launches_recorded": len(records)},
+        "host_issue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "sweep": sw,
     }
     if rank == 0:
@@ -541,6 +558,10 @@ def main(argv=None):
     p.add_argument("--no-sweep", dest="sweep", action="store_false")
     p.add_argument("--no-e2e", dest="e2e", action="store_false")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--timing-every", type=int, default=10,
+                   help="record per-launch events on every k-th timed step")
+    p.add_argument("--one-shot-impl", type=int, default=0, help="AR_OPT_ONE_SHOT_IMPL (0 auto, 1, 2)")
+    p.add_argument("--ctas-per-sm", type=int, default=0, help="AR_OPT_CTAS_PER_SM (0 auto)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-budget", type=float, default=150.0,

@@ -58,7 +58,8 @@ enum {
     AR_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned */
     AR_ERR_TOO_LARGE = -3,    /* count x element size > max_bytes */
     AR_ERR_CUDA = -4,         /* a CUDA runtime call or a launch failed */
-    AR_ERR_FLAG_TIMEOUT = -5  /* an LL/LL128 line never showed the expected flag */
+    AR_ERR_FLAG_TIMEOUT = -5, /* an LL/LL128 line never showed the expected flag */
+    AR_ERR_WAIT_TIMEOUT = -6  /* a kernel's bounded wait for its own bulk copies ran out */
 };
 
 /* Which call an ar_traffic_t describes. */
@@ -100,7 +101,7 @@ typedef struct {
 
 /* The sticky device-side error of a handle. */
 typedef struct {
-    int code;                /* AR_OK or AR_ERR_FLAG_TIMEOUT */
+    int code;                /* AR_OK, AR_ERR_FLAG_TIMEOUT or AR_ERR_WAIT_TIMEOUT */
     int rank;                /* rank whose line lacked the flag (-1: none) */
     uint64_t line;           /* index of the first line found without its flag */
     uint64_t lines_skipped;  /* lines left unconsumed (their outputs untouched) */
@@ -108,13 +109,18 @@ typedef struct {
 
 /* Options for ar_set_option. */
 enum {
-    AR_OPT_CTAS_PER_SM = 1,  /* CTAs per SM for the streaming kernels, 1..32 (default 8) */
+    AR_OPT_CTAS_PER_SM = 1,  /* cap on CTAs per SM of a launch, 1..1024; 0 (default): 64
+                                (many short-lived CTAs; measured best), and one resident
+                                wave for the bulk-copy one-shot */
     AR_OPT_SPIN_NS = 2,      /* LL/LL128 bounded wait per line, ns, 1..10^10 (default 10^6) */
     AR_OPT_ONE_SHOT_IMPL = 3,/* 0 auto, 1 vector loads/stores, 2 bulk-copy staging */
-    AR_OPT_TIMING = 4        /* 0 off (default); k in 1..2^20: record a CUDA event pair
+    AR_OPT_TIMING = 4,       /* 0 off (default); k in 1..2^20: record a CUDA event pair
                                 around each launch, keeping the last k launches.  Setting
                                 it creates the events (not a hot-path call); do not time
                                 calls that are being captured into a CUDA graph. */
+    AR_OPT_TIMING_PAUSE = 5  /* with AR_OPT_TIMING on: 1 stops recording (no event
+                                records at all), 0 resumes; a cheap host-side switch,
+                                e.g. to sample every k-th pass of a timed loop */
 };
 
 /* Kernels, as ar_timing reports them. */
@@ -225,6 +231,19 @@ int ar_ll128_pack(ar_handle h, const float* src, void* lines, size_t count, uint
 int ar_ll128_unpack(ar_handle h, const void* lines, float* dst, size_t count, uint64_t step,
                     ar_stream_t stream);
 
+/* The same for all n_ranks buffers of the handle in one launch: src / lines /
+ * dst are host arrays of n_ranks device pointers (each checked as in the
+ * single-buffer call; sources may alias, destinations may not overlap
+ * anything).  Results are those of n single-buffer calls. */
+int ar_ll_pack_n(ar_handle h, const float* const* src, void* const* lines, size_t count, uint32_t step,
+                 ar_stream_t stream);
+int ar_ll_unpack_n(ar_handle h, const void* const* lines, float* const* dst, size_t count, uint32_t step,
+                   ar_stream_t stream);
+int ar_ll128_pack_n(ar_handle h, const float* const* src, void* const* lines, size_t count, uint64_t step,
+                    ar_stream_t stream);
+int ar_ll128_unpack_n(ar_handle h, const void* const* lines, float* const* dst, size_t count, uint64_t step,
+                      ar_stream_t stream);
+
 /* Flag-checked reduce: a line is consumed when every rank's copy carries
  * `step`; its words are summed in rank order (fp32, from +0) and written to
  * every rank's output line with flag `step`.  lines_in / lines_out: host
@@ -253,12 +272,16 @@ int ar_traffic(ar_handle h, ar_traffic_t* t);
 int ar_timing(ar_handle h, ar_launch_time_t* out, int max, int* n_out);
 
 /* Host only, no GPU needed: the traffic a call of `op` would have (as
- * ar_traffic reports it after the call). */
+ * ar_traffic reports it after the call).  For the pack / unpack ops n_ranks
+ * is the number of buffers (1 for the single-buffer calls). */
 int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
 
-/* Host only, no GPU needed: the code an all-reduce call (AR_OP_ONE_SHOT,
- * AR_OP_TWO_SHOT, AR_OP_RING, AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE) would
- * return for these arguments before launching anything.  Pointers are
+/* Host only, no GPU needed: the code a call would return for these
+ * arguments before launching anything.  op AR_OP_ONE_SHOT, AR_OP_TWO_SHOT,
+ * AR_OP_RING, AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls
+ * (n_ranks in [2, 16]); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
+ * AR_OP_LL128_UNPACK: the batched pack / unpack calls over n_ranks buffers
+ * (in = sources, out = destinations; n_ranks in [1, 16]).  Pointers are
  * compared, never dereferenced.  For the LL ops dt must be AR_F32. */
 int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in,
                   void* const* out, size_t count, ar_dtype dt);

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_strerror_names_every_code(lib):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert ar.ar_strerror(code) != "unknown error code"
     assert ar.ar_strerror(-99) == "unknown error code"
 
@@ -88,6 +88,17 @@ def test_plan_ll_matches_closed_forms(lib, count):
 
 def _rw(t):
     return t.hbm_read_bytes, t.hbm_write_bytes
+
+
+@pytest.mark.parametrize("nb", [1, 8, 16])
+def test_plan_batched_pack_scales_with_buffers(lib, nb):
+    c = 1000
+    for op, f in ((ar.AR_OP_LL_PACK, model.hbm_ll_pack), (ar.AR_OP_LL_UNPACK, model.hbm_ll_unpack),
+                  (ar.AR_OP_LL128_PACK, model.hbm_ll128_pack), (ar.AR_OP_LL128_UNPACK, model.hbm_ll128_unpack)):
+        rd, wr = f(c)
+        assert _rw(ar.ar_plan(op, nb, c, "f32")) == (nb * rd, nb * wr)
+    with pytest.raises(ar.ArError):
+        ar.ar_plan(ar.AR_OP_LL_PACK, 0, c, "f32")
 
 
 def test_plan_rejects_bad_arguments(lib):
@@ -154,6 +165,26 @@ def test_check_args_ll(lib):
     close = [BASE + r * 4096 for r in range(n)]
     assert _check(ar.AR_OP_LL_REDUCE, n, ins, close, 1000, dtype="f32") == ar.AR_ERR_INVALID
     assert _check(ar.AR_OP_LL_REDUCE, n, ins, close, 500, dtype="f32") == ar.AR_OK
+
+
+def test_check_args_batched_pack(lib):
+    n, c = 8, 1000                      # payload 4000 B, LL lines 8000 B, LL128 lines 4352 B
+    src = _bufs(n)
+    dst = _bufs(n, off=64 << 20)
+    for op in (ar.AR_OP_LL_PACK, ar.AR_OP_LL128_PACK, ar.AR_OP_LL_UNPACK, ar.AR_OP_LL128_UNPACK):
+        assert _check(op, n, src, dst, c, dtype="f32") == ar.AR_OK
+        assert _check(op, 1, src[:1], dst[:1], c, dtype="f32") == ar.AR_OK
+        assert _check(op, n, [src[0]] * n, dst, c, dtype="f32") == ar.AR_OK     # sources may alias
+        assert _check(op, n, src, dst, c, dtype="bf16") == ar.AR_ERR_INVALID
+        assert _check(op, 0, src, dst, c, dtype="f32") == ar.AR_ERR_INVALID
+        assert _check(op, n, src, [dst[0]] * n, c, dtype="f32") == ar.AR_ERR_INVALID   # destinations alias
+        assert _check(op, n, src, dst[:7] + [src[3]], c, dtype="f32") == ar.AR_ERR_INVALID
+        assert _check(op, n, src, dst[:7] + [dst[7] + 8], c, dtype="f32") == ar.AR_ERR_ALIGN
+        assert _check(op, n, src, dst, (1 << 18) + 1, dtype="f32") == ar.AR_ERR_TOO_LARGE
+    # LL lines are twice the payload: destinations 4 KiB apart overlap at 1000 words
+    close = [BASE + (64 << 20) + r * 4096 for r in range(n)]
+    assert _check(ar.AR_OP_LL_PACK, n, src, close, c, dtype="f32") == ar.AR_ERR_INVALID
+    assert _check(ar.AR_OP_LL_UNPACK, n, src, close, c, dtype="f32") == ar.AR_OK  # unpack writes 4000 B
 
 
 def test_calls_reject_a_null_handle(lib):

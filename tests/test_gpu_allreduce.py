@@ -251,3 +251,30 @@ def test_handle_is_reusable_across_sizes_and_types():
                 got = run(algo, xs, dtype, h=h)
                 want = (oracle.ring if algo == "ring" else oracle.all_reduce)(xs, dtype)
                 np.testing.assert_array_equal(bits(got[3]), bits(want[3]))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("N", [1, 7, 9, 2047, 2048, 4096 + 8, 300_001, 1 << 21])
+def test_one_shot_bulk_copy_variant_bit_exact(dtype, n, N):
+    # AR_OPT_ONE_SHOT_IMPL = 2: rank tiles staged in shared memory by bulk copies,
+    # tiles of 4 KiB per rank (several tiles, a partial last tile, a ragged tail)
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=n * 13 + N)
+    want = oracle.all_reduce(xs, dtype)
+    with Handle(n, max(16, N * E[dtype]), one_shot_impl=2) as h:
+        for in_place in (False, True):
+            got = run("one_shot", xs, dtype, h=h, in_place=in_place)
+            for r in range(n):
+                np.testing.assert_array_equal(bits(got[r]), bits(want[r]), err_msg=f"rank {r} in_place={in_place}")
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 16, 64])
+@pytest.mark.parametrize("impl", [1, 2])
+def test_grid_size_option_changes_nothing_but_speed(ctas, impl):
+    n, N = 8, 1 << 20
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=ctas)
+    with Handle(n, 2 * N, ctas_per_sm=ctas, one_shot_impl=impl) as h:
+        for algo in CALLS:
+            got = run(algo, xs, "bf16", h=h)
+            want = (oracle.ring if algo == "ring" else oracle.all_reduce)(xs, "bf16")
+            np.testing.assert_array_equal(got[5], want[5])

@@ -41,7 +41,7 @@ def test_pipeline_pack_reduce_unpack(kind, count):
     o_unpack = oracle.ll_unpack if kind == "ll" else oracle.ll128_unpack
     reduce = ar.ar_ll_reduce if kind == "ll" else ar.ar_ll128_reduce
     unpack = ar.ar_ll_unpack if kind == "ll" else ar.ar_ll128_unpack
-    with Handle(n, 4 * count) as h:
+    with Handle(n, max(16, 4 * count)) as h:               # a handle holds at least 16 B
         for step in (1, 2, 3):                                  # a fresh step id each pass
             srcs, lines = _pack_all(h, xs, step, kind)
             outs = [Buf(l.nbytes).fill(0) for l in lines]
@@ -143,5 +143,52 @@ def test_spin_option_bounds():
     with Handle(2, 64) as h:
         assert ar.ar_set_option(h, ar.AR_OPT_SPIN_NS, 0) == ar.AR_ERR_INVALID
         assert ar.ar_set_option(h, ar.AR_OPT_SPIN_NS, 10**10 + 1) == ar.AR_ERR_INVALID
-        assert ar.ar_set_option(h, ar.AR_OPT_CTAS_PER_SM, 33) == ar.AR_ERR_INVALID
+        assert ar.ar_set_option(h, ar.AR_OPT_CTAS_PER_SM, 1025) == ar.AR_ERR_INVALID
+        assert ar.ar_set_option(h, ar.AR_OPT_TIMING_PAUSE, 1) == ar.AR_ERR_INVALID   # timing is off
         assert ar.ar_set_option(h, 99, 1) == ar.AR_ERR_INVALID
+
+
+@pytest.mark.parametrize("kind", ["ll", "ll128"])
+@pytest.mark.parametrize("n,count", [(8, 262144), (8, 61), (16, 4099), (2, 1)])
+def test_batched_pack_and_unpack_equal_the_oracle(kind, n, count):
+    xs = workloads.payload_f32(n, count, seed=n * 31 + count)
+    o_pack = oracle.ll_pack if kind == "ll" else oracle.ll128_pack
+    nbytes = oracle.ll_bytes(count) if kind == "ll" else oracle.ll128_bytes(count)
+    pack_n = ar.ar_ll_pack_n if kind == "ll" else ar.ar_ll128_pack_n
+    unpack_n = ar.ar_ll_unpack_n if kind == "ll" else ar.ar_ll128_unpack_n
+    reduce = ar.ar_ll_reduce if kind == "ll" else ar.ar_ll128_reduce
+    step = 21
+    with Handle(n, max(16, 4 * count)) as h:
+        srcs = [Buf(x.nbytes).upload(x) for x in xs]
+        lines = [Buf(nbytes).fill(0) for _ in range(n)]
+        red = [Buf(nbytes).fill(0) for _ in range(n)]
+        dsts = [Buf(4 * count).fill(0) for _ in range(n)]
+        assert pack_n(h, ptrs(srcs), ptrs(lines), count, step) == ar.AR_OK
+        assert ar.ar_traffic(h).launches == 1
+        assert reduce(h, ptrs(lines), ptrs(red), count, step) == ar.AR_OK
+        assert unpack_n(h, ptrs(red), ptrs(dsts), count, step) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+        for l, x in zip(lines, xs):
+            np.testing.assert_array_equal(l.download(np.uint8), o_pack(x, step))
+        want = oracle.all_reduce(xs, "f32")[0]
+        for d in dsts:
+            np.testing.assert_array_equal(d.download(np.uint32), want.view(np.uint32))
+        for b in srcs + lines + red + dsts:
+            assert b.guards_intact()
+
+
+def test_batched_unpack_reports_the_rank_of_a_stale_buffer():
+    n, count, step = 4, 1000, 3
+    xs = workloads.payload_f32(n, count, seed=8)
+    with Handle(n, 4 * count, spin_ns=100_000) as h:
+        srcs = [Buf(x.nbytes).upload(x) for x in xs]
+        lines = [Buf(oracle.ll_bytes(count)).fill(0) for _ in range(n)]
+        assert ar.ar_ll_pack_n(h, ptrs(srcs), ptrs(lines), count, step) == ar.AR_OK
+        assert ar.ar_ll_pack(h, srcs[2].ptr, lines[2].ptr, count, step + 1) == ar.AR_OK   # rank 2 runs ahead
+        dsts = [Buf(4 * count).fill(0x7F) for _ in range(n)]
+        assert ar.ar_ll_unpack_n(h, ptrs(lines), ptrs(dsts), count, step) == ar.AR_OK
+        rc, info = ar.ar_status_info(h)
+        assert rc == ar.AR_ERR_FLAG_TIMEOUT and info.rank == 2 and info.lines_skipped == count
+        assert bool((dsts[2].body() == 0x7F).all())
+        for r in (0, 1, 3):
+            np.testing.assert_array_equal(dsts[r].download(np.uint32), xs[r].view(np.uint32))
