@@ -38,7 +38,7 @@ EXPORTS = (
     "ar_ll_bytes", "ar_ll128_bytes", "ar_ll_pack", "ar_ll_unpack", "ar_ll128_pack", "ar_ll128_unpack",
     "ar_ll_reduce", "ar_ll128_reduce", "ar_status", "ar_status_info", "ar_traffic", "ar_plan",
     "ar_check_args", "ar_strerror", "ar_timing", "ar_ll_pack_n", "ar_ll_unpack_n", "ar_ll128_pack_n",
-    "ar_ll128_unpack_n",
+    "ar_ll128_unpack_n", "ar_ring_noalloc",
 )
 
 
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
                 "ar_one_shot": ([vp, pp, pp, sz, i32, vp], i32),
                 "ar_two_shot": ([vp, pp, pp, sz, i32, vp], i32),
                 "ar_ring": ([vp, pp, pp, sz, i32, vp], i32),
+                "ar_ring_noalloc": ([i32, pp, pp, sz, i32, vp], i32),
                 "ar_ll_bytes": ([sz], sz),
                 "ar_ll128_bytes": ([sz], sz),
                 "ar_ll_pack": ([vp, vp, vp, sz, u32, vp], i32),
@@ -177,6 +178,11 @@ def ar_two_shot(h, ins, outs, count: int, dtype, stream=None) -> int:
 
 def ar_ring(h, ins, outs, count: int, dtype, stream=None) -> int:
     return lib().ar_ring(h, _ptr_array(ins), _ptr_array(outs), count, _dtype(dtype), _stream(stream))
+
+
+def ar_ring_noalloc(n_ranks: int, ins, outs, count: int, dtype, stream=None) -> int:
+    """ar_ring without a handle or any allocation (static 32 MiB scratch in the library)."""
+    return lib().ar_ring_noalloc(n_ranks, _ptr_array(ins), _ptr_array(outs), count, _dtype(dtype), _stream(stream))
 
 
 def ar_ll_bytes(payload_bytes: int) -> int:

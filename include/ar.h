@@ -198,6 +198,28 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
             ar_dtype dt, ar_stream_t stream);
 
+/* Ring all-reduce for callers that cannot allocate device memory (code that
+ * runs where cudaMalloc is not allowed or not wanted: inside a framework that
+ * owns the device heap, a memory-capped process, a plugin that is handed only
+ * its input and output buffers).  The pages have no counterpart; it is the
+ * same computation as ar_ring (same chunks, rotation and fp32 partials, same
+ * bits), without a handle.  The partials live in one static 32 MiB device
+ * array inside the library, which every GPU that loads the library holds
+ * until the process exits; the call itself allocates nothing.
+ *   - Size limit: 2 x n_ranks x C fp32 partials must fit in 32 MiB, with C =
+ *     ceil(count / n_ranks) rounded up to a 16-byte vector (about 4 Mi
+ *     elements in all: 8 MiB of bf16 per rank at n = 8); larger calls
+ *     return AR_ERR_TOO_LARGE.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address and the SM count once; make that first call
+ *     before any stream capture.
+ *   - Every call shares the array and leaves its partials in it; nothing in
+ *     it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     race on it: issue them in order on one stream.
+ * Arguments and errors otherwise as ar_ring. */
+int ar_ring_noalloc(int n_ranks, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                    ar_stream_t stream);
+
 /* ---- LL / LL128 protocol lines -------------------------------------------- */
 /* Handbook "集合通信：NCCL 的算法、协议…", §协议 table: LL puts 4 B of data
  * and a 4 B flag in every 8 B line, LL128 120 B of data and an 8 B flag in
