@@ -27,7 +27,7 @@ AR_OK, AR_ERR_INVALID, AR_ERR_ALIGN, AR_ERR_TOO_LARGE, AR_ERR_CUDA, AR_ERR_FLAG_
     0, -1, -2, -3, -4, -5, -6)
 (AR_OP_NONE, AR_OP_ONE_SHOT, AR_OP_TWO_SHOT, AR_OP_RING, AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL_REDUCE,
  AR_OP_LL128_PACK, AR_OP_LL128_UNPACK, AR_OP_LL128_REDUCE) = range(10)
-AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING, AR_OPT_TIMING_PAUSE = 1, 2, 3, 4, 5
+AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING, AR_OPT_TIMING_PAUSE, AR_OPT_PDL = 1, 2, 3, 4, 5, 6
 KERNELS = {1: "one_shot", 2: "reduce_scatter", 3: "all_gather", 4: "ring_rs_step", 5: "ring_ag_step",
            6: "ll_pack", 7: "ll_unpack", 8: "ll_reduce", 9: "ll128_pack", 10: "ll128_unpack",
            11: "ll128_reduce"}

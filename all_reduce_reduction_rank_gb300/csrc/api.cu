@@ -422,6 +422,10 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
         if (value < 0 || value > 2) return AR_ERR_INVALID;
         h->one_shot_impl = (int)value;
         return AR_OK;
+    case AR_OPT_PDL:
+        if (value < 0 || value > 1) return AR_ERR_INVALID;
+        h->pdl = (int)value;
+        return AR_OK;
     case AR_OPT_TIMING_PAUSE:
         if (value < 0 || value > 1 || h->timing.capacity == 0) return AR_ERR_INVALID;
         h->timing.paused = (int)value;

@@ -8,6 +8,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -175,6 +176,38 @@ __device__ __forceinline__ void report_flag_timeout(DevStatus* st, int rank, uns
 __device__ __forceinline__ void report_wait_timeout(DevStatus* st)
 {
     atomicCAS(&st->code, 0, AR_ERR_WAIT_TIMEOUT);
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel is launched with programmatic stream serialization allowed
+// (AR_OPT_PDL, default on), so the next kernel in the stream can be launched
+// while this one drains.  Each kernel starts by waiting for its predecessor's
+// completion and memory (griddepcontrol.wait, a hardware wait that returns at
+// once when there is no programmatic predecessor) before it touches global
+// memory, and lets its dependents launch once its own main loop is done
+// (pdl_release): early enough to hide their launch, late enough that their
+// CTAs, which wait on this grid, are spread over the SMs as this grid's tail
+// frees them rather than packed onto the first SMs to free up.
+
+__device__ __forceinline__ void pdl_acquire() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(const Handle& h, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args&&... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = h.pdl ? 1 : 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Rank pointer tables, passed by value in the kernel parameters.

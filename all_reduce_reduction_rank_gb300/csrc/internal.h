@@ -38,6 +38,7 @@ struct Handle {
     int ctas_per_sm = 0;  // 0: one full wave, from each kernel's occupancy
     int64_t spin_ns = 1000000;
     int one_shot_impl = 0;
+    int pdl = 1;  // programmatic dependent launch between consecutive kernels
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements
     DevStatus* status = nullptr;    // device

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kThreads)
 ll_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__ DstTable outs, size_t count,
                uint32_t step)
 {
+    pdl_acquire();
     const float* const src = static_cast<const float*>(srcs.p[blockIdx.y]);
     uint4* const lines = static_cast<uint4*>(outs.p[blockIdx.y]);
     const size_t nq = count / 4;  // 4 payload words -> 2 x 16 B of lines
@@ -66,6 +67,7 @@ ll_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__ Ds
         st16(lines + 2 * v, make_uint4(x.x, step, x.y, step));
         st16(lines + 2 * v + 1, make_uint4(x.z, step, x.w, step));
     }
+    pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
         const size_t i = nq * 4 + threadIdx.x;
         if (i < count) reinterpret_cast<uint2*>(lines)[i] = make_uint2(__float_as_uint(src[i]), step);
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(kThreads)
 ll_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant__ DstTable dsts, size_t count,
                  uint32_t step, int64_t spin_ns, DevStatus* st)
 {
+    pdl_acquire();
     const int rank = blockIdx.y;
     const uint4* const lines = static_cast<const uint4*>(ins.p[rank]);
     float* const dst = static_cast<float*>(dsts.p[rank]);
@@ -103,6 +106,7 @@ ll_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant__ D
             }
         }
     }
+    pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
         const size_t i = nq * 4 + threadIdx.x;
         if (i < count) {
@@ -126,6 +130,7 @@ template <int NR>
 __global__ void __launch_bounds__(kThreads)
 ll_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t count, uint32_t step, int64_t spin_ns, DevStatus* st)
 {
+    pdl_acquire();
     const size_t np = (count + 1) / 2;  // 16-byte pairs of lines, the last one maybe half used
     for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < np; v += (size_t)gridDim.x * kThreads) {
         const bool two = 2 * v + 1 < count;
@@ -193,6 +198,7 @@ ll_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ M
             }
         }
     }
+    pdl_release();
 }
 
 // -------------------------------------------------------------- LL128 ------
@@ -222,6 +228,7 @@ __global__ void __launch_bounds__(kThreads)
 ll128_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__ DstTable outs, size_t count,
                   uint64_t step)
 {
+    pdl_acquire();
     const float* const src = static_cast<const float*>(srcs.p[blockIdx.y]);
     uint4* const lines = static_cast<uint4*>(outs.p[blockIdx.y]);
     const size_t L = (count + 29) / 30;
@@ -252,12 +259,14 @@ ll128_pack_kernel(const __grid_constant__ SrcTable srcs, const __grid_constant__
         }
         st16(lines + 8 * ln.k + ln.j, make_uint4(w[0], w[1], w[2], w[3]));
     }
+    pdl_release();
 }
 
 __global__ void __launch_bounds__(kThreads)
 ll128_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant__ DstTable dsts, size_t count,
                     uint64_t step, int64_t spin_ns, DevStatus* st)
 {
+    pdl_acquire();
     const int rank = blockIdx.y;
     const uint4* const lines = static_cast<const uint4*>(ins.p[rank]);
     float* const dst = static_cast<float*>(dsts.p[rank]);
@@ -298,12 +307,14 @@ ll128_unpack_kernel(const __grid_constant__ SrcTable ins, const __grid_constant_
             report_flag_timeout(st, rank, ln.k);
         }
     }
+    pdl_release();
 }
 
 template <int NR>
 __global__ void __launch_bounds__(kThreads)
 ll128_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t count, uint64_t step, int64_t spin_ns, DevStatus* st)
 {
+    pdl_acquire();
     const size_t L = (count + 29) / 30;
     const size_t warp = ((size_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = ((size_t)gridDim.x * kThreads) >> 5;
@@ -359,6 +370,7 @@ ll128_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             report_flag_timeout(st, __ffs(bad) - 1, ln.k);
         }
     }
+    pdl_release();
 }
 
 }  // namespace
@@ -380,7 +392,7 @@ int launch_ll_pack(Handle& h, int nb, const float* const* src, void* const* line
     tables(nb, reinterpret_cast<const void* const*>(src), lines, st, dt);
     const dim3 grid(grid_for_rows(h, count / 4, nb), nb);
     rec_begin(h, s);
-    ll_pack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step);
+    launch_kernel(h, ll_pack_kernel, grid, kThreads, 0, s, st, dt, count, step);
     rec_end(h, s, AR_K_LL_PACK, 12ull * count * nb);
     return launch_status();
 }
@@ -393,7 +405,7 @@ int launch_ll_unpack(Handle& h, int nb, const void* const* lines, float* const* 
     tables(nb, lines, reinterpret_cast<void* const*>(dst), st, dt);
     const dim3 grid(grid_for_rows(h, count / 4, nb), nb);
     rec_begin(h, s);
-    ll_unpack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step, h.spin_ns, h.status);
+    launch_kernel(h, ll_unpack_kernel, grid, kThreads, 0, s, st, dt, count, step, h.spin_ns, h.status);
     rec_end(h, s, AR_K_LL_UNPACK, 12ull * count * nb);
     return launch_status();
 }
@@ -410,8 +422,8 @@ int launch_ll_reduce(Handle& h, const void* const* in, void* const* out, size_t 
             op.p[q] = out[q];
         }
         rec_begin(h, s);
-        ll_reduce_kernel<NR><<<grid_for(h, (count + 1) / 2), kThreads, 0, s>>>(ip, op, count, step,
-                                                                                       h.spin_ns, h.status);
+        launch_kernel(h, ll_reduce_kernel<NR>, grid_for(h, (count + 1) / 2), kThreads, 0, s, ip, op, count, step,
+                      h.spin_ns, h.status);
         rec_end(h, s, AR_K_LL_REDUCE, 16ull * NR * count);
         return launch_status();
     });
@@ -426,7 +438,7 @@ int launch_ll128_pack(Handle& h, int nb, const float* const* src, void* const* l
     const size_t L = (count + 29) / 30;
     const dim3 grid(grid_for_rows(h, L * 8, nb), nb);
     rec_begin(h, s);
-    ll128_pack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step);
+    launch_kernel(h, ll128_pack_kernel, grid, kThreads, 0, s, st, dt, count, step);
     rec_end(h, s, AR_K_LL128_PACK, (4ull * count + 128ull * L) * nb);
     return launch_status();
 }
@@ -440,7 +452,7 @@ int launch_ll128_unpack(Handle& h, int nb, const void* const* lines, float* cons
     const size_t L = (count + 29) / 30;
     const dim3 grid(grid_for_rows(h, L * 8, nb), nb);
     rec_begin(h, s);
-    ll128_unpack_kernel<<<grid, kThreads, 0, s>>>(st, dt, count, step, h.spin_ns, h.status);
+    launch_kernel(h, ll128_unpack_kernel, grid, kThreads, 0, s, st, dt, count, step, h.spin_ns, h.status);
     rec_end(h, s, AR_K_LL128_UNPACK, (4ull * count + 128ull * L) * nb);
     return launch_status();
 }
@@ -458,8 +470,8 @@ int launch_ll128_reduce(Handle& h, const void* const* in, void* const* out, size
         }
         const size_t L = (count + 29) / 30;
         rec_begin(h, s);
-        ll128_reduce_kernel<NR><<<grid_for(h, L * 8), kThreads, 0, s>>>(ip, op, count, step, h.spin_ns,
-                                                                                h.status);
+        launch_kernel(h, ll128_reduce_kernel<NR>, grid_for(h, L * 8), kThreads, 0, s, ip, op, count, step,
+                      h.spin_ns, h.status);
         rec_end(h, s, AR_K_LL128_REDUCE, 256ull * NR * L);
         return launch_status();
     });

@@ -24,6 +24,7 @@ template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
 one_shot_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count)
 {
+    pdl_acquire();
     constexpr int U = one_shot_unroll<NR>();
     const size_t span = (size_t)kThreads * U;
     for (size_t base = (size_t)blockIdx.x * span; base < nvec; base += (size_t)gridDim.x * span) {
@@ -46,6 +47,7 @@ one_shot_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MP
             }
         }
     }
+    pdl_release();
     // Elements after the last whole vector: same arithmetic, one per thread.
     if (blockIdx.x == gridDim.x - 1) {
         using T = typename Payload<DT>::scalar_t;
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 one_shot_bulk_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
                      size_t count, DevStatus* st)
 {
+    pdl_acquire();
     constexpr int P = bulk_stages<NR>();
     constexpr uint32_t T = kBulkTile;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -145,6 +148,7 @@ one_shot_bulk_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant
         }
         __syncthreads();
     }
+    pdl_release();
     if (tid == 0) {
         if (failed) {
             report_wait_timeout(st);
@@ -207,13 +211,13 @@ int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t c
                 if (grid > ntiles) grid = ntiles;
                 if (grid == 0) grid = 1;
                 rec_begin(h, s);
-                one_shot_bulk_kernel<NR, DT><<<(unsigned)grid, kThreads, smem, s>>>(ip, op, nvec, count, h.status);
+                launch_kernel(h, one_shot_bulk_kernel<NR, DT>, (unsigned)grid, kThreads, smem, s, ip, op, nvec, count, h.status);
                 rec_end(h, s, AR_K_ONE_SHOT, 2ull * NR * S);
             } else {
                 constexpr int U = one_shot_unroll<NR>();
                 const unsigned grid = grid_for(h, (nvec + U - 1) / U);
                 rec_begin(h, s);
-                one_shot_kernel<NR, DT><<<grid, kThreads, 0, s>>>(ip, op, nvec, count);
+                launch_kernel(h, one_shot_kernel<NR, DT>, grid, kThreads, 0, s, ip, op, nvec, count);
                 rec_end(h, s, AR_K_ONE_SHOT, 2ull * NR * S);
             }
             *launches = 1;

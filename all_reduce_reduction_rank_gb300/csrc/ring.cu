@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kThreads)
 ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                     const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s)
 {
+    pdl_acquire();
     constexpr int VE = kVecElems<DT>;
     constexpr int PW = VE / 4;          // 16-byte words of fp32 partial per payload vector
     constexpr int U = kRsUnroll;
@@ -103,6 +104,7 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             }
         }
     }
+    pdl_release();
     // the ragged end of the last chunk: one element per thread
     if (blockIdx.x == gridDim.x - 1) {
         const size_t j = nv * VE + threadIdx.x;
@@ -121,6 +123,7 @@ template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
 ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t count, int s)
 {
+    pdl_acquire();
     constexpr int VE = kVecElems<DT>;
     constexpr int U = kAgUnroll;
     using T = typename Payload<DT>::scalar_t;
@@ -147,6 +150,7 @@ ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t coun
             if (k < nv) st16(dst + k * VE, x[u]);
         }
     }
+    pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
         const size_t j = nv * VE + threadIdx.x;
         if (j < len) dst[j] = src[j];
@@ -181,15 +185,14 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
                 const uint64_t rd = (step == 0 ? e : 4) * N + e * N;
                 const uint64_t wr = (step == NR - 2 ? e : 4) * N;
                 rec_begin(h, s);
-                ring_rs_step_kernel<NR, DT><<<g_rs, kThreads, 0, s>>>(
-                    ip, op, buf[(step + 1) & 1], buf[step & 1], C, count, step);
+                launch_kernel(h, ring_rs_step_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1], buf[step & 1], C, count, step);
                 rec_end(h, s, AR_K_RING_RS_STEP, rd + wr);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }
             for (int step = 0; step < NR - 1; ++step) {
                 rec_begin(h, s);
-                ring_ag_step_kernel<NR, DT><<<g_ag, kThreads, 0, s>>>(op, C, count, step);
+                launch_kernel(h, ring_ag_step_kernel<NR, DT>, g_ag, kThreads, 0, s, op, C, count, step);
                 rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kThreads)
 reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
                       size_t count, size_t cvec)
 {
+    pdl_acquire();
     constexpr int U = rs_unroll<NR>();
     const int r = blockIdx.y;
     const size_t lo = (size_t)r * cvec;
@@ -51,6 +52,7 @@ reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constan
             if (v < hi) st16(dst + v, reduce_rank_order<DT, NR>(x[u]));
         }
     }
+    pdl_release();
     // elements past the last whole vector, handled once by the grid's last block
     if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1) {
         using T = typename Payload<DT>::scalar_t;
@@ -69,6 +71,7 @@ template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
 all_gather_kernel(const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count, size_t cvec)
 {
+    pdl_acquire();
     constexpr int U = kAgUnroll;
     const int j = blockIdx.y;
     const size_t lo = (size_t)j * cvec;
@@ -92,6 +95,7 @@ all_gather_kernel(const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t cou
             }
         }
     }
+    pdl_release();
     if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1) {
         using T = typename Payload<DT>::scalar_t;
         const size_t i = nvec * kVecElems<DT> + threadIdx.x;
@@ -127,11 +131,11 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
             const dim3 g_rs(grid_for_rows(h, (cvec + U - 1) / U, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
             rec_begin(h, s);
-            reduce_scatter_kernel<NR, DT><<<g_rs, kThreads, 0, s>>>(ip, op, nvec, count, cvec);
+            launch_kernel(h, reduce_scatter_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, nvec, count, cvec);
             rec_end(h, s, AR_K_REDUCE_SCATTER, (uint64_t)(NR + 1) * S);
             if (launch_status() != AR_OK) return AR_ERR_CUDA;
             rec_begin(h, s);
-            all_gather_kernel<NR, DT><<<g_ag, kThreads, 0, s>>>(op, nvec, count, cvec);
+            launch_kernel(h, all_gather_kernel<NR, DT>, g_ag, kThreads, 0, s, op, nvec, count, cvec);
             rec_end(h, s, AR_K_ALL_GATHER, (uint64_t)NR * S);
             *launches = 2;
             return launch_status();

@@ -118,9 +118,13 @@ enum {
                                 around each launch, keeping the last k launches.  Setting
                                 it creates the events (not a hot-path call); do not time
                                 calls that are being captured into a CUDA graph. */
-    AR_OPT_TIMING_PAUSE = 5  /* with AR_OPT_TIMING on: 1 stops recording (no event
+    AR_OPT_TIMING_PAUSE = 5, /* with AR_OPT_TIMING on: 1 stops recording (no event
                                 records at all), 0 resumes; a cheap host-side switch,
                                 e.g. to sample every k-th pass of a timed loop */
+    AR_OPT_PDL = 6           /* 1 (default): launch with programmatic stream
+                                serialization, so a kernel is scheduled while the one
+                                before it in the stream drains (each kernel waits for
+                                its predecessor before touching memory); 0: plain launches */
 };
 
 /* Kernels, as ar_timing reports them. */

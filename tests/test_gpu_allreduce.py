@@ -278,3 +278,23 @@ def test_grid_size_option_changes_nothing_but_speed(ctas, impl):
             got = run(algo, xs, "bf16", h=h)
             want = (oracle.ring if algo == "ring" else oracle.all_reduce)(xs, "bf16")
             np.testing.assert_array_equal(got[5], want[5])
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_programmatic_launch_on_and_off_give_the_same_bits(pdl):
+    # back-to-back calls that depend on each other through memory: in place,
+    # so each call reads what the previous one wrote
+    n, N = 8, (1 << 18) + 5
+    xs = workloads.rank_inputs(n, N, "f32", "int8", seed=pdl)
+    ins = upload_ranks(xs)
+    with Handle(n, 4 * N, pdl=pdl) as h:
+        for call in (ar.ar_one_shot, ar.ar_two_shot, ar.ar_ring, ar.ar_one_shot):
+            assert call(h, ptrs(ins), ptrs(ins), N, "f32") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    # integer inputs, |sum| <= 64 n^4 < 2^24: every pass is exact, and each
+    # pass after the first sums n equal copies
+    s = sum(x.astype(np.int64) for x in xs)
+    want = (s * n**3).astype(np.float32)
+    for b in ins:
+        np.testing.assert_array_equal(b.download(np.float32), want)
