@@ -3,6 +3,7 @@
 // the calls that launch the kernels of one_shot.cu, two_shot.cu, ring.cu and
 // ll.cu.  Host code only; nothing here allocates after ar_create.
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <new>
 
@@ -39,6 +40,13 @@ bool overlap(const void* a, const void* b, size_t bytes)
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// [a, a + an) and [b, b + bn) intersect.
+bool overlap_sized(const void* a, size_t an, const void* b, size_t bn)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return an && bn && x < y + bn && y < x + an;
+}
 
 int check_size(size_t count, int dt, size_t max_bytes)
 {
@@ -116,7 +124,8 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
     t->op = op;
     t->n_ranks = n;
     t->count = count;
-    t->elem_bytes = (op >= AR_OP_LL_PACK) ? 4u : elem_bytes(dt);
+    const bool ll = op >= AR_OP_LL_PACK && op <= AR_OP_LL128_REDUCE;  // fp32 payload words
+    t->elem_bytes = ll ? 4u : elem_bytes(dt);
     const uint64_t e = t->elem_bytes, N = count, S = N * e, nn = (uint64_t)n;
     const uint64_t L = ll128_lines(count);
     switch (op) {
@@ -174,6 +183,13 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         t->launches = count ? 1 : 0;
         t->hbm_read_bytes = nn * 128 * L;
         t->hbm_write_bytes = nn * 4 * N;
+        break;
+    case AR_OP_ALLREDUCE_RMSNORM:
+        t->link_bytes_per_rank = (double)(nn - 1) * (double)S;
+        t->steps = 1;
+        t->launches = count ? 1 : 0;
+        t->hbm_read_bytes = (nn + 1) * S;
+        t->hbm_write_bytes = (nn + 1) * S;
         break;
     case AR_OP_LL128_REDUCE:
         t->steps = 1;
@@ -331,8 +347,9 @@ size_t ar_ll128_bytes(size_t payload_bytes) { return 128u * ((payload_bytes + 11
 
 int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
 {
-    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_LL128_REDUCE) return AR_ERR_INVALID;
-    const bool multi = op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE;
+    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_ALLREDUCE_RMSNORM) return AR_ERR_INVALID;
+    const bool multi =
+        op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE || op == AR_OP_ALLREDUCE_RMSNORM;
     if (multi && (n_ranks < 2 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;
     if (!multi && (n_ranks < 1 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;  // buffers packed
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
@@ -421,6 +438,22 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
     case AR_OPT_ONE_SHOT_IMPL:
         if (value < 0 || value > 2) return AR_ERR_INVALID;
         h->one_shot_impl = (int)value;
+        return AR_OK;
+    case AR_OPT_AUTO_POLICY:
+        if (value != AR_AUTO_MODEL && value != AR_AUTO_EMULATED) return AR_ERR_INVALID;
+        h->auto_policy = (int)value;
+        return AR_OK;
+    case AR_OPT_AUTO_ALPHA_NS:
+        if (value < 0 || value > 1000000000LL) return AR_ERR_INVALID;
+        h->auto_alpha_ns = value;
+        return AR_OK;
+    case AR_OPT_AUTO_BETA_MBS:
+        if (value < 1 || value > 1000000000LL) return AR_ERR_INVALID;
+        h->auto_beta_mbs = value;
+        return AR_OK;
+    case AR_OPT_AUTO_HANDOFF:
+        if (value < 0) return AR_ERR_INVALID;
+        h->auto_handoff = value;
         return AR_OK;
     case AR_OPT_PDL:
         if (value < 0 || value > 1) return AR_ERR_INVALID;
@@ -526,6 +559,73 @@ int ar_ll128_reduce(ar_handle h, const void* const* in, void* const* out, size_t
     return reduce_call(AR_OP_LL128_REDUCE, h, in, out, count, step, s, [&](Handle& hh, cudaStream_t st) {
         return launch_ll128_reduce(hh, in, out, count, step, st);
     });
+}
+
+int ar_allreduce_rmsnorm(ar_handle hd, const void* const* in, const void* residual, const void* weight, float eps,
+                         void* const* norm_out, void* residual_out, size_t tokens, size_t hidden, ar_dtype dt,
+                         ar_stream_t stream)
+{
+    Handle* h = get(hd);
+    if (!h) return AR_ERR_INVALID;
+    if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
+    if (!(eps >= 0.0f) || eps == INFINITY) return AR_ERR_INVALID;
+    const size_t e = elem_bytes(dt);
+    if (hidden == 0 || hidden % (16u / e) != 0 || !rmsnorm_fits(hidden, dt)) return AR_ERR_INVALID;
+    if (tokens > SIZE_MAX / hidden / 128u) return AR_ERR_TOO_LARGE;
+    const size_t count = tokens * hidden;
+    if (int rc = check_multi(AR_OP_ONE_SHOT, h->n, h->max_bytes, in, norm_out, count, dt)) return rc;
+    if (!residual || !weight || !residual_out) return AR_ERR_INVALID;
+    if (!aligned16(residual) || !aligned16(weight) || !aligned16(residual_out)) return AR_ERR_ALIGN;
+    const size_t S = count * e, W = hidden * e;
+    if (residual_out != residual && overlap(residual_out, residual, S)) return AR_ERR_INVALID;
+    if (overlap_sized(residual_out, S, weight, W)) return AR_ERR_INVALID;
+    for (int r = 0; r < h->n; ++r)
+        if (overlap(residual_out, in[r], S) || overlap(residual_out, norm_out[r], S) ||
+            overlap(norm_out[r], residual, S) || overlap_sized(norm_out[r], S, weight, W))
+            return AR_ERR_INVALID;
+    int rc = AR_OK;
+    h->timing.op = AR_OP_ALLREDUCE_RMSNORM;
+    if (count)
+        rc = on_device(*h, [&] {
+            return launch_allreduce_rmsnorm(*h, in, residual, weight, eps, norm_out, residual_out, tokens, hidden, dt,
+                                            (cudaStream_t)stream);
+        });
+    if (rc != AR_OK) return rc;
+    plan(AR_OP_ALLREDUCE_RMSNORM, h->n, count, dt, &h->last);
+    if (count) h->last.hbm_read_bytes += W;
+    h->last_stream = (cudaStream_t)stream;
+    return AR_OK;
+}
+
+int ar_select(int policy, int n_ranks, size_t bytes_per_rank, double alpha_s, double beta, size_t handoff_bytes)
+{
+    if (n_ranks < 2 || n_ranks > kMaxRanks) return AR_ERR_INVALID;
+    if (policy == AR_AUTO_EMULATED) return AR_OP_ONE_SHOT;
+    if (policy != AR_AUTO_MODEL || !(alpha_s >= 0.0) || !(beta > 0.0)) return AR_ERR_INVALID;
+    if (handoff_bytes && bytes_per_rank > handoff_bytes) return AR_OP_RING;
+    // the alpha-beta model of the three algorithms (per-rank bytes S):
+    //   one-shot 2a + (n-1) S / b;  two-shot 4a + 2 (n-1)/n S / b;  ring 2(n-1) a + 2 (n-1)/n S / b
+    const double n = n_ranks, S = (double)bytes_per_rank;
+    const double t1 = 2.0 * alpha_s + (n - 1.0) * S / beta;
+    const double t2 = 4.0 * alpha_s + 2.0 * (n - 1.0) / n * S / beta;
+    const double tr = 2.0 * (n - 1.0) * alpha_s + 2.0 * (n - 1.0) / n * S / beta;
+    if (t1 <= t2 && t1 <= tr) return AR_OP_ONE_SHOT;  // ties keep the simpler call
+    return t2 <= tr ? AR_OP_TWO_SHOT : AR_OP_RING;
+}
+
+int ar_auto(ar_handle hd, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
+{
+    Handle* h = get(hd);
+    if (!h) return AR_ERR_INVALID;
+    if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
+    const int op = ar_select(h->auto_policy, h->n, count * elem_bytes(dt), (double)h->auto_alpha_ns * 1e-9,
+                             (double)h->auto_beta_mbs * 1e6, (size_t)h->auto_handoff);
+    switch (op) {
+    case AR_OP_ONE_SHOT: return ar_one_shot(hd, in, out, count, dt, s);
+    case AR_OP_TWO_SHOT: return ar_two_shot(hd, in, out, count, dt, s);
+    case AR_OP_RING: return ar_ring(hd, in, out, count, dt, s);
+    default: return op < 0 ? op : AR_ERR_INVALID;
+    }
 }
 
 int ar_status_info(ar_handle hd, ar_status_info_t* info)

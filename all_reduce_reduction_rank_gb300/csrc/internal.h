@@ -39,6 +39,10 @@ struct Handle {
     int64_t spin_ns = 1000000;
     int one_shot_impl = 0;
     int pdl = 1;  // programmatic dependent launch between consecutive kernels
+    int auto_policy = AR_AUTO_MODEL;
+    int64_t auto_alpha_ns = 1500;
+    int64_t auto_beta_mbs = 450000;
+    int64_t auto_handoff = 8 << 20;
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements
     DevStatus* status = nullptr;    // device
@@ -134,6 +138,11 @@ int launch_ll128_pack(Handle& h, int nb, const float* const* src, void* const* l
                       cudaStream_t s);
 int launch_ll128_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count,
                         uint64_t step, cudaStream_t s);
+size_t rmsnorm_slice_vecs(size_t hidden, int dt);
+bool rmsnorm_fits(size_t hidden, int dt);
+int launch_allreduce_rmsnorm(Handle& h, const void* const* in, const void* residual, const void* weight, float eps,
+                             void* const* out, void* residual_out, size_t tokens, size_t hidden, int dt,
+                             cudaStream_t s);
 int launch_ll128_reduce(Handle& h, const void* const* in, void* const* out, size_t count,
                         uint64_t step, cudaStream_t s);
 

@@ -1,0 +1,199 @@
+// All-reduce fused with residual add and RMSNorm: the decode epilogue of a
+// tensor-parallel layer in one launch.
+//
+// Handbook "集合通信：NCCL 的算法、协议与推理框架的定制 all-reduce",
+// §源码对照, names such a fused all-reduce + RMSNorm kernel (FlashInfer's)
+// without defining it; "多 GPU 与 NCCL", §为什么要多卡 puts the all-reduce at
+// the end of every tensor-parallel attention and MLP block.  The result is
+// that of the unfused chain:
+//   a = all-reduce of in[*] (rank-order fp32 sum, rounded to the payload)
+//   r = RN(a + residual)                          -> residual_out
+//   y = RN(r * 1/sqrt(mean(r^2) + eps) * weight)  -> norm_out[0..n-1]
+//
+// Layout: one thread-block cluster of kClusterCtas CTAs per token row; CTA c
+// of the cluster owns a contiguous slice of the row.  Pass 1 reads the n rank
+// slices once, writes r, keeps r (fp32) in shared memory and accumulates its
+// squares; the CTAs' partial sums are combined in a fixed order through
+// distributed shared memory; pass 2 scales r and writes every rank's output.
+// HBM: reads n S + S (+ the weight, H per launch), writes n S + S.
+#include "common.cuh"
+
+namespace argb {
+namespace {
+
+constexpr int kClusterCtas = 8;
+constexpr int kNormThreads = 128;
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Hardware barrier across the CTAs of a cluster (all of them are resident
+// together by construction), with release / acquire memory ordering.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A float in CTA `cta`'s shared memory, at the offset of `local` in ours.
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t cta)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(cta));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int NR, int DT>
+__global__ void __launch_bounds__(kNormThreads)
+allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __restrict__ residual,
+                         const void* __restrict__ weight, float eps, const __grid_constant__ MPtrs<NR> out,
+                         void* residual_out, size_t hidden, size_t slice_vecs)
+{
+    constexpr int VE = kVecElems<DT>;
+    extern __shared__ float r_slice[];                 // slice_vecs * VE floats
+    __shared__ float warp_part[kNormThreads / 32];
+    __shared__ float cta_part;
+    __shared__ float row_inv;
+    pdl_acquire();
+    const uint32_t c = cluster_ctarank();
+    const size_t t = blockIdx.x / kClusterCtas;        // token row of this cluster
+    const size_t nvec_row = hidden / VE;
+    const size_t v_lo = (size_t)c * slice_vecs;
+    const size_t v_hi = v_lo + slice_vecs < nvec_row ? v_lo + slice_vecs : nvec_row;
+    const size_t row = t * nvec_row;                   // first 16-byte vector of the row
+
+    // pass 1: all-reduce, residual add, squares
+    float ss = 0.0f;
+    for (size_t v = v_lo + threadIdx.x; v < v_hi; v += kNormThreads) {
+        uint4 x[NR];
+#pragma unroll
+        for (int q = 0; q < NR; ++q) x[q] = ld16(static_cast<const uint4*>(in.p[q]) + row + v);
+        const uint4 a = reduce_rank_order<DT, NR>(x);
+        const uint4 res = ld16(static_cast<const uint4*>(residual) + row + v);
+        float af[VE], rf[VE];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            Payload<DT>::widen(word(a, j), af + j * Payload<DT>::kPerWord);
+            Payload<DT>::widen(word(res, j), rf + j * Payload<DT>::kPerWord);
+        }
+#pragma unroll
+        for (int k = 0; k < VE; ++k) rf[k] = af[k] + rf[k];
+        const uint4 rr = round_vec<DT>(rf);
+        st16(static_cast<uint4*>(residual_out) + row + v, rr);
+        float rq[VE];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(rr, j), rq + j * Payload<DT>::kPerWord);
+        float* dst = r_slice + (v - v_lo) * VE;
+#pragma unroll
+        for (int k = 0; k < VE; ++k) {
+            dst[k] = rq[k];
+            ss = ss + rq[k] * rq[k];
+        }
+    }
+    // the CTA's sum of squares: warps, then the warps in order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = ss + __shfl_down_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.0f;
+        for (int w = 0; w < kNormThreads / 32; ++w) s = s + warp_part[w];
+        cta_part = s;
+    }
+    // the row's: the cluster's CTAs in order, read from their shared memory
+    cluster_sync();
+    if (threadIdx.x == 0) {
+        float s = 0.0f;
+        for (uint32_t k = 0; k < kClusterCtas; ++k) s = s + ld_cluster_f32(&cta_part, k);
+        row_inv = 1.0f / sqrtf(s / (float)hidden + eps);
+    }
+    cluster_sync();  // every CTA has read every partial before any CTA may exit
+    pdl_release();
+    const float inv = row_inv;
+
+    // pass 2: scale, weight, round, write every rank's output
+    for (size_t v = v_lo + threadIdx.x; v < v_hi; v += kNormThreads) {
+        const uint4 wv = ld16(static_cast<const uint4*>(weight) + v);
+        float wf[VE], y[VE];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(wv, j), wf + j * Payload<DT>::kPerWord);
+        const float* src = r_slice + (v - v_lo) * VE;
+#pragma unroll
+        for (int k = 0; k < VE; ++k) y[k] = (src[k] * inv) * wf[k];
+        const uint4 yo = round_vec<DT>(y);
+#pragma unroll
+        for (int q = 0; q < NR; ++q) st16(static_cast<uint4*>(out.p[q]) + row + v, yo);
+    }
+}
+
+}  // namespace
+
+// Largest slice of a row one CTA keeps in shared memory (fp32).
+constexpr size_t kRmsnormMaxSliceBytes = 160u << 10;
+
+size_t rmsnorm_slice_vecs(size_t hidden, int dt)
+{
+    const size_t ve = 16u / elem_bytes(dt);
+    const size_t nvec = hidden / ve;
+    return (nvec + kClusterCtas - 1) / kClusterCtas;
+}
+
+bool rmsnorm_fits(size_t hidden, int dt)
+{
+    const size_t ve = 16u / elem_bytes(dt);
+    return rmsnorm_slice_vecs(hidden, dt) * ve * sizeof(float) <= kRmsnormMaxSliceBytes;
+}
+
+int launch_allreduce_rmsnorm(Handle& h, const void* const* in, const void* residual, const void* weight, float eps,
+                             void* const* out, void* residual_out, size_t tokens, size_t hidden, int dt,
+                             cudaStream_t s)
+{
+    return dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            CPtrs<NR> ip;
+            MPtrs<NR> op;
+            for (int q = 0; q < NR; ++q) {
+                ip.p[q] = in[q];
+                op.p[q] = out[q];
+            }
+            const size_t slice = rmsnorm_slice_vecs(hidden, DT);
+            const size_t smem = slice * kVecElems<DT> * sizeof(float);
+            static const bool attr_ok =
+                cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kRmsnormMaxSliceBytes) == cudaSuccess;
+            if (!attr_ok) return AR_ERR_CUDA;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = kClusterCtas;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = h.pdl ? 1 : 0;
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3((unsigned)(tokens * kClusterCtas));
+            cfg.blockDim = dim3(kNormThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            const uint64_t S = (uint64_t)tokens * hidden * sizeof(typename Payload<DT>::scalar_t);
+            const uint64_t W = (uint64_t)hidden * sizeof(typename Payload<DT>::scalar_t);
+            rec_begin(h, s);
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, allreduce_rmsnorm_kernel<NR, DT>, ip, residual, weight, eps,
+                                                     op, residual_out, hidden, slice);
+            rec_end(h, s, AR_K_ALLREDUCE_RMSNORM, 2ull * (NR + 1) * S + W);
+            return e == cudaSuccess ? launch_status() : AR_ERR_CUDA;
+        });
+    });
+}
+
+}  // namespace argb

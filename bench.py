@@ -309,18 +309,21 @@ def per_kernel(records, K: int, peak: float) -> dict:
     return out
 
 
-def sweep(wl, peak: float, iters_small: int = 200, iters_large: int = 50) -> dict:
+def sweep(wl, peak: float, batches: int = 7, min_calls: int = 64) -> dict:
     """one-shot and two-shot over the decode and prefill message sizes (n = 8,
-    bf16): per size the median of CUDA-event-timed calls.  Before every call,
-    outside the timed interval, a 256 MiB buffer (2x L2) is read, which
-    evicts the previous call's lines (writing back the dirty ones) and leaves
-    the L2 clean, so no call starts with its data, or with dirty lines, in L2."""
+    bf16).  Each rank's 64 MiB input and output buffers are cut into slots of
+    the message size; a batch issues back-to-back calls on successive slots
+    (the batch's calls touch 1 GiB between two uses of a slot, so no call finds
+    its data in the 129 MB L2) and is timed with one pair of CUDA events, which
+    also avoids the ~2 us resolution of timing a single short call.  Reported:
+    the median over batches of the time per call."""
+    import ctypes
+
     import torch
 
     import all_reduce_reduction_rank_gb300 as ar
     import workloads
 
-    flush = torch.ones(64 * MiB, dtype=torch.int32, device=wl.dev)
     sizes = sorted({2 * c for c in workloads.CONFIGS[2]["counts"]} | {2 * c for c in workloads.CONFIGS[3]["counts"]})
     res = {"one_shot": [], "two_shot": []}
     n = wl.n
@@ -328,27 +331,84 @@ def sweep(wl, peak: float, iters_small: int = 200, iters_large: int = 50) -> dic
         if S > wl.S:
             continue
         N = S // 2
-        iters = iters_small if S <= MiB else iters_large
+        slots = wl.S // S
+        P = lambda ts, k: (ctypes.c_void_p * n)(*[t.data_ptr() + k * S for t in ts])
+        pin = [P(wl.ins, k) for k in range(slots)]
+        pout = [P(wl.outs, k) for k in range(slots)]
+        calls = max(min_calls, slots)
         for algo, call, op in (("one_shot", wl.L.ar_one_shot, ar.AR_OP_ONE_SHOT),
                                ("two_shot", wl.L.ar_two_shot, ar.AR_OP_TWO_SHOT)):
             t = ar.ar_plan(op, n, N, "bf16")
             b = t.hbm_read_bytes + t.hbm_write_bytes
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-            with torch.cuda.stream(wl.stream):
-                for e0, e1 in evs:
-                    flush.sum()
-                    e0.record(wl.stream)
-                    ar.check(call(wl.h, wl.p_in, wl.p_out, N, 1, wl.s), algo)
-                    e1.record(wl.stream)
-            torch.cuda.synchronize()
-            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+            for k in range(min(slots, 4)):
+                ar.check(call(wl.h, pin[k], pout[k], N, 1, wl.s), algo)
+            per_call = []
+            for _ in range(batches):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(wl.stream)
+                for i in range(calls):
+                    call(wl.h, pin[i % slots], pout[i % slots], N, 1, wl.s)
+                e1.record(wl.stream)
+                e1.synchronize()
+                per_call.append(e0.elapsed_time(e1) / calls)
+            ar.check(ar.ar_status(wl.h), algo)
+            ms = statistics.median(per_call)
             gbs = b / (ms * 1e-3) / 1e9
             algbw = S / (ms * 1e-3) / 1e9
             res[algo].append({"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
                               "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
-                              "busbw_GB/s": round(algbw * 2 * (n - 1) / n, 1), "iters": iters})
-    del flush
+                              "busbw_GB/s": round(algbw * 2 * (n - 1) / n, 1), "calls_per_batch": calls,
+                              "batches": batches})
     return res
+
+
+def fused_epilogue(wl, peak: float, batches: int = 7, calls: int = 200) -> list:
+    """ar_allreduce_rmsnorm on the decode shapes (n = 8 bf16, tokens {1, 8,
+    32, 64} x hidden {4096, 8192}), beside ar_one_shot on the same shape: the
+    fused epilogue's cost over a bare all-reduce.  Back-to-back calls on
+    rotating slots of the 64 MiB rank buffers, one event pair per batch."""
+    import ctypes
+
+    import torch
+
+    import all_reduce_reduction_rank_gb300 as ar
+
+    n, out = wl.n, []
+    res = torch.randn(64 * 8192, device=wl.dev).to(torch.bfloat16)
+    res_out = torch.empty_like(res)
+    w = torch.rand(8192, device=wl.dev).to(torch.bfloat16)
+    for T in (1, 8, 32, 64):
+        for H in (4096, 8192):
+            S = T * H * 2
+            slots = min(wl.S // S, 4096)
+            P = lambda ts, k: (ctypes.c_void_p * n)(*[t.data_ptr() + k * S for t in ts])
+            pin = [P(wl.ins, k) for k in range(slots)]
+            pout = [P(wl.outs, k) for k in range(slots)]
+            row = {"tokens": T, "hidden": H}
+            for name in ("fused", "one_shot"):
+                def call(k):
+                    if name == "fused":
+                        return wl.L.ar_allreduce_rmsnorm(wl.h, pin[k], res.data_ptr(), w.data_ptr(),
+                                                         ctypes.c_float(1e-6), pout[k], res_out.data_ptr(), T, H, 1,
+                                                         wl.s)
+                    return wl.L.ar_one_shot(wl.h, pin[k], pout[k], T * H, 1, wl.s)
+                ar.check(call(0), name)
+                per = []
+                for _ in range(batches):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(wl.stream)
+                    for i in range(calls):
+                        call(i % slots)
+                    e1.record(wl.stream)
+                    e1.synchronize()
+                    per.append(e0.elapsed_time(e1) / calls)
+                us = statistics.median(per) * 1e3
+                b = (2 * n + 2) * S + H * 2 if name == "fused" else 2 * n * S
+                row[name + "_us"] = round(us, 3)
+                row[name + "_GB/s"] = round(b / (us * 1e-6) / 1e9, 1)
+            ar.check(ar.ar_status(wl.h), "fused epilogue")
+            out.append(row)
+    return out
 
 
 def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
@@ -446,6 +506,7 @@ def run_ours(args):
                 "bytes_per_launch": dk["bytes_per_launch"], "peak_source": peak_src}
 
     sw = sweep(wl, peak) if args.sweep else None
+    fe = fused_epilogue(wl, peak) if args.sweep else None
     e2e = e2e_leg(wl, max(3, min(args.steps, args.e2e_steps)), bytes_step) if args.e2e else None
     cpu = None
     if world == 1 and rank == 0 and args.cpu_baseline:
@@ -467,6 +528,7 @@ def run_ours(args):
         "launch_timing": {"steps_sampled": sampled, "every": every, "launches_recorded": len(records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "sweep": sw,
+        "fused_epilogue": fe,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

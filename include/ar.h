@@ -73,7 +73,8 @@ typedef enum {
     AR_OP_LL_REDUCE = 6,
     AR_OP_LL128_PACK = 7,
     AR_OP_LL128_UNPACK = 8,
-    AR_OP_LL128_REDUCE = 9
+    AR_OP_LL128_REDUCE = 9,
+    AR_OP_ALLREDUCE_RMSNORM = 10
 } ar_op;
 
 /* Traffic of one call.
@@ -121,6 +122,11 @@ enum {
     AR_OPT_TIMING_PAUSE = 5, /* with AR_OPT_TIMING on: 1 stops recording (no event
                                 records at all), 0 resumes; a cheap host-side switch,
                                 e.g. to sample every k-th pass of a timed loop */
+    AR_OPT_AUTO_POLICY = 7,  /* ar_auto's policy: AR_AUTO_MODEL (default) or AR_AUTO_EMULATED */
+    AR_OPT_AUTO_ALPHA_NS = 8,/* model: fixed cost per step, ns (default 1500) */
+    AR_OPT_AUTO_BETA_MBS = 9,/* model: per-rank link bandwidth, MB/s (default 450000) */
+    AR_OPT_AUTO_HANDOFF = 10,/* model: bytes per rank above which the ring is used (the size
+                                of a pre-registered buffer; default 8 MiB; 0 = no hand-off) */
     AR_OPT_PDL = 6           /* 1 (default): launch with programmatic stream
                                 serialization, so a kernel is scheduled while the one
                                 before it in the stream drains (each kernel waits for
@@ -139,7 +145,8 @@ typedef enum {
     AR_K_LL_REDUCE = 8,
     AR_K_LL128_PACK = 9,
     AR_K_LL128_UNPACK = 10,
-    AR_K_LL128_REDUCE = 11
+    AR_K_LL128_REDUCE = 11,
+    AR_K_ALLREDUCE_RMSNORM = 12
 } ar_kernel;
 
 /* One recorded launch: which kernel, for which call, its device time
@@ -223,6 +230,59 @@ int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
  * Arguments and errors otherwise as ar_ring. */
 int ar_ring_noalloc(int n_ranks, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                     ar_stream_t stream);
+
+/* ---- all-reduce fused with residual add and RMSNorm --------------------------- */
+
+/* The decode epilogue of a tensor-parallel layer in one launch (handbook
+ * "集合通信：NCCL 的算法、协议…", §源码对照, names such a fused all-reduce +
+ * RMSNorm kernel; its result here is that of the unfused chain):
+ *   a = the all-reduce of in[*] (as ar_one_shot: rank-order fp32 sum, rounded)
+ *   r = RN(a + residual)                                   -> residual_out
+ *   y = RN(r * 1/sqrt(mean over the row of r^2 + eps) * w) -> norm_out[0..n-1]
+ * in, norm_out: host arrays of n_ranks device pointers to [tokens][hidden]
+ * row-major payloads; residual, residual_out: [tokens][hidden] (one copy:
+ * in tensor parallelism every rank holds the same residual; residual_out may
+ * equal residual); weight: [hidden].  hidden must be a whole number of
+ * 16-byte vectors and at most 327680 fp32 / 655360 bf16 or fp16 elements;
+ * eps >= 0.  In place (norm_out[r] == in[r]) is allowed; otherwise no output
+ * may overlap an input or another output.  Each token row is handled by a
+ * thread-block cluster of 8 CTAs, whose partial sums of squares are combined
+ * through distributed shared memory.  a and r match the unfused chain bit for
+ * bit; y within one payload ulp (the order of the sum of squares is the
+ * kernel's).  ar_plan(AR_OP_ALLREDUCE_RMSNORM) omits the weight's H bytes,
+ * which ar_traffic includes after a call. */
+int ar_allreduce_rmsnorm(ar_handle h, const void* const* in, const void* residual, const void* weight, float eps,
+                         void* const* norm_out, void* residual_out, size_t tokens, size_t hidden, ar_dtype dt,
+                         ar_stream_t stream);
+
+/* ---- size-based selection --------------------------------------------------- */
+
+enum {
+    /* The pages' choice for n real GPUs (handbook "集合通信：NCCL 的算法、协议…",
+     * §算法: small messages one-shot, medium two-shot, large ones handed to
+     * the ring of NCCL; the α-β model decides between the first two, the
+     * one-shot / two-shot crossover being S* = 2 α β / ((n-1)(1 - 2/n)), none
+     * at n = 2 (§练习 exercise 2); frameworks hand buffers above a
+     * pre-registered size (about 8 MB in vLLM) to NCCL): the fastest of
+     * one-shot, two-shot and ring under the α-β model, and the ring above the
+     * hand-off size. */
+    AR_AUTO_MODEL = 0,
+    /* The cheapest on this GPU: one-shot, which moves the fewest HBM bytes
+     * (2 n S) in a single launch at every size. */
+    AR_AUTO_EMULATED = 1
+};
+
+/* Host only: the call (AR_OP_ONE_SHOT, AR_OP_TWO_SHOT or AR_OP_RING) that
+ * `policy` picks for n_ranks buffers of bytes_per_rank bytes; alpha_s in
+ * seconds, beta in bytes/s, handoff_bytes 0 for none.  AR_ERR_INVALID for a
+ * bad n, policy, alpha or beta. */
+int ar_select(int policy, int n_ranks, size_t bytes_per_rank, double alpha_s, double beta_bytes_per_s,
+              size_t handoff_bytes);
+
+/* All-reduce with the call the handle's policy (AR_OPT_AUTO_*) selects for
+ * this size; then exactly that call.  ar_traffic reports the call chosen. */
+int ar_auto(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+            ar_stream_t stream);
 
 /* ---- LL / LL128 protocol lines -------------------------------------------- */
 /* Handbook "集合通信：NCCL 的算法、协议…", §协议 table: LL puts 4 B of data

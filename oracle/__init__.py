@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
                 "orc_ll128_pack": ([vp, vp, sz, u64], None),
                 "orc_ll128_unpack": ([vp, vp, sz, u64], sz),
                 "orc_ll128_reduce": ([i32, pp, pp, sz, u64], sz),
+                "orc_allreduce_rmsnorm": ([i32, pp, vp, vp, ctypes.c_double, vp, vp, sz, sz, i32], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -261,3 +262,19 @@ def ll128_reduce(lines_in: list, count: int, step: int, lines_out: list | None =
         lines_out = [np.zeros_like(lines_in[0]) for _ in range(n)]
     bad = lib().orc_ll128_reduce(n, _ptrs(lines_in), _ptrs(lines_out), count, step)
     return lines_out, bad
+
+
+# --- fused all-reduce + residual add + RMSNorm ------------------------------
+
+def allreduce_rmsnorm(inputs: list, residual: np.ndarray, weight: np.ndarray, eps: float, tokens: int,
+                      hidden: int, dtype: str):
+    """Returns (norm_out, residual_out), each [tokens * hidden] in the payload type."""
+    _check(inputs, dtype)
+    _check([residual], dtype)
+    _check([weight], dtype)
+    assert inputs[0].size == residual.size == tokens * hidden and weight.size == hidden
+    norm = np.empty_like(residual)
+    res_out = np.empty_like(residual)
+    lib().orc_allreduce_rmsnorm(len(inputs), _ptrs(inputs), _ptr(residual), _ptr(weight), eps, _ptr(norm),
+                                _ptr(res_out), tokens, hidden, _DT[dtype])
+    return norm, res_out

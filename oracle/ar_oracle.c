@@ -410,3 +410,42 @@ size_t orc_ll128_reduce(int n, const uint8_t* const* in, uint8_t* const* out, si
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* All-reduce fused with residual add and RMSNorm (the decode epilogue).     */
+/* ------------------------------------------------------------------------ */
+
+/* The handbook chapter "集合通信：NCCL 的算法、协议…" (§源码对照) names an
+ * all-reduce + RMSNorm fused kernel for tensor-parallel layers without
+ * defining it; the reading taken is that fusing changes nothing in the
+ * result of the unfused chain:
+ *   a[t][h]   = the all-reduce of in[*][t][h] (rank-order fp32 sum, rounded)
+ *   r[t][h]   = RN( a + residual[t][h] )            -> residual_out
+ *   y[t][h]   = RN( r * 1/sqrt(mean_h(r^2) + eps) * weight[h] ) -> norm_out
+ * The mean of squares and the scaling are computed here in double (the
+ * kernel's order of summation over h is its own); y is therefore compared
+ * within one payload ulp, a and r bit for bit. */
+void orc_allreduce_rmsnorm(int n, const void* const* in, const void* residual, const void* weight, double eps,
+                           void* norm_out, void* residual_out, size_t T, size_t H, int dt)
+{
+    for (size_t t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (size_t h = 0; h < H; ++h) {
+            size_t i = t * H + h;
+            float acc = 0.0f;
+            for (int r = 0; r < n; ++r)
+                acc = acc + widen(in[r], i, dt);
+            narrow(residual_out, i, acc, dt);                       /* a, rounded */
+            float rr = widen(residual_out, i, dt) + widen(residual, i, dt);
+            narrow(residual_out, i, rr, dt);                        /* r, rounded */
+            double rv = (double)widen(residual_out, i, dt);
+            ss += rv * rv;
+        }
+        double inv = 1.0 / sqrt(ss / (double)H + eps);
+        for (size_t h = 0; h < H; ++h) {
+            size_t i = t * H + h;
+            double y = (double)widen(residual_out, i, dt) * inv * (double)widen(weight, h, dt);
+            narrow(norm_out, i, (float)y, dt);
+        }
+    }
+}

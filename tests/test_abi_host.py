@@ -102,7 +102,7 @@ def test_plan_batched_pack_scales_with_buffers(lib, nb):
 
 
 def test_plan_rejects_bad_arguments(lib):
-    for op, n in [(0, 8), (10, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17)]:
+    for op, n in [(0, 8), (11, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17), (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]:
         with pytest.raises(ar.ArError):
             ar.ar_plan(op, n, 10, "f32")
     with pytest.raises(ar.ArError):
@@ -209,3 +209,60 @@ def test_create_without_a_device_fails_cleanly(lib):
     with pytest.raises(ar.ArError) as e:
         ar.ar_create(1, 1 << 20)
     assert e.value.code == ar.AR_ERR_INVALID
+
+
+# --- size-based selection ------------------------------------------------------
+
+def test_select_model_matches_the_printed_alpha_beta_table(lib):
+    # the fastest of ring / one-shot / two-shot in each printed row of the
+    # NCCL chapter's alpha-beta table (n = 8, beta = 450e9, alpha = 1.5e-6)
+    path = os.path.join(ROOT, "tests", "golden", "alpha_beta_table.txt")
+    rows = [ln.split() for ln in open(path) if ln.startswith("row ")]
+    assert len(rows) == 5
+    name_of = {ar.AR_OP_ONE_SHOT: "one-shot", ar.AR_OP_TWO_SHOT: "two-shot", ar.AR_OP_RING: "ring"}
+    for r in rows:
+        S = int(r[1])
+        printed = {"ring": float(r[2]), "one-shot": float(r[4]), "two-shot": float(r[5])}
+        want = min(printed, key=printed.get)
+        got = ar.ar_select(ar.AR_AUTO_MODEL, 8, S, 1.5e-6, 450e9, 0)
+        assert name_of[got] == want, (S, name_of[got], printed)
+        assert want == r[7]          # the page's own "fastest without NVLS" column
+
+
+def test_select_model_crossover_and_handoff(lib):
+    # S* = 2 alpha beta / ((n-1)(1-2/n)) = 257142.86 B at n = 8 (exercise 2)
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 8, 257142, 1.5e-6, 450e9, 0) == ar.AR_OP_ONE_SHOT
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 8, 257143, 1.5e-6, 450e9, 0) == ar.AR_OP_TWO_SHOT
+    # no crossover at n = 2: one-shot at every size
+    for S in (1, 1 << 20, 1 << 30):
+        assert ar.ar_select(ar.AR_AUTO_MODEL, 2, S, 1.5e-6, 450e9, 0) == ar.AR_OP_ONE_SHOT
+    # above the pre-registered size the ring takes over
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 8, 8 << 20, 1.5e-6, 450e9, 8 << 20) == ar.AR_OP_TWO_SHOT
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 8, (8 << 20) + 1, 1.5e-6, 450e9, 8 << 20) == ar.AR_OP_RING
+    # the emulated policy: one-shot always
+    for n in (2, 8, 16):
+        assert ar.ar_select(ar.AR_AUTO_EMULATED, n, 1 << 28, 0.0, 1.0, 0) == ar.AR_OP_ONE_SHOT
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 1, 10, 1e-6, 1e9, 0) == ar.AR_ERR_INVALID
+    assert ar.ar_select(7, 8, 10, 1e-6, 1e9, 0) == ar.AR_ERR_INVALID
+    assert ar.ar_select(ar.AR_AUTO_MODEL, 8, 10, 1e-6, 0.0, 0) == ar.AR_ERR_INVALID
+
+
+@pytest.mark.parametrize("n", [3, 4, 8, 16])
+def test_select_model_crossover_formula(lib, n):
+    from oracle import model
+    a, b = 1.5e-6, 450e9
+    s_star = model.one_two_shot_crossover(n, b, a)
+    if s_star is None:
+        return
+    below, above = int(s_star * 0.999), int(s_star * 1.001) + 1
+    assert ar.ar_select(ar.AR_AUTO_MODEL, n, below, a, b, 0) == ar.AR_OP_ONE_SHOT
+    assert ar.ar_select(ar.AR_AUTO_MODEL, n, above, a, b, 0) in (ar.AR_OP_TWO_SHOT, ar.AR_OP_RING)
+
+
+@pytest.mark.parametrize("n", [2, 8, 16])
+def test_plan_fused_epilogue(lib, n):
+    # reads n S of partial sums and S of residual, writes n normalized outputs and the residual
+    t = ar.ar_plan(ar.AR_OP_ALLREDUCE_RMSNORM, n, 64 * 8192, "bf16")
+    S = 64 * 8192 * 2
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == ((n + 1) * S, (n + 1) * S)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_one_shot(n, S)) and t.launches == 1

@@ -298,3 +298,22 @@ def test_programmatic_launch_on_and_off_give_the_same_bits(pdl):
     want = (s * n**3).astype(np.float32)
     for b in ins:
         np.testing.assert_array_equal(b.download(np.float32), want)
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+@pytest.mark.parametrize("N", [4096, 200_000, 5_000_000])
+def test_auto_runs_the_selected_call(policy, N):
+    n, dtype = 8, "bf16"
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=N + policy)
+    with Handle(n, 2 * N, auto_policy=policy, auto_handoff=4 << 20) as h:
+        got = run("one_shot", xs, dtype, h=h)  # warm the handle, then the auto call below
+        ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+        assert ar.ar_auto(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+        chosen = ar.ar_traffic(h).op
+    torch.cuda.synchronize()
+    want_op = ar.ar_select(policy, n, 2 * N, 1.5e-6, 450e9, 4 << 20)
+    assert chosen == want_op
+    want = (oracle.ring if chosen == ar.AR_OP_RING else oracle.all_reduce)(xs, dtype)
+    for r in range(n):
+        np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
