@@ -61,7 +61,7 @@ class StatusInfo(ctypes.Structure):
 
 class LaunchTime(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("op", ctypes.c_int), ("ms", ctypes.c_float),
-                ("hbm_bytes", ctypes.c_uint64)]
+                ("hbm_bytes", ctypes.c_uint64), ("launches", ctypes.c_int)]
 
 
 class ArError(RuntimeError):
@@ -285,15 +285,15 @@ def ar_check_args(op: int, n_ranks: int, max_bytes: int, ins, outs, count: int, 
     return lib().ar_check_args(op, n_ranks, max_bytes, pin, pout, count, _dtype(dtype))
 
 
-def ar_timing(h, max_records: int = 1 << 20) -> list[tuple[str, int, float, int]]:
-    """Recorded launches, oldest first: (kernel name, op, ms, hbm bytes)."""
+def ar_timing(h, max_records: int = 1 << 20) -> list[tuple[str, int, float, int, int]]:
+    """Timing records, oldest first: (kernel name, op, ms, hbm bytes, launches)."""
     buf = (LaunchTime * max_records)()
     n = ctypes.c_int(0)
     rc = lib().ar_timing(h, buf, max_records, ctypes.byref(n))
     if rc != AR_OK:
         raise ArError(rc, "ar_timing")
-    return [(KERNELS.get(buf[i].kernel, str(buf[i].kernel)), buf[i].op, buf[i].ms, buf[i].hbm_bytes)
-            for i in range(n.value)]
+    return [(KERNELS.get(buf[i].kernel, str(buf[i].kernel)), buf[i].op, buf[i].ms, buf[i].hbm_bytes,
+             buf[i].launches) for i in range(n.value)]
 
 
 def check(rc: int, what: str = "") -> None:

@@ -51,19 +51,20 @@ struct Handle {
     Timing timing;
 };
 
-// Bracket one launch with the timing events (no-ops when timing is off).
+// Bracket one launch, or a run of consecutive launches of one kernel, with the
+// timing events (no-ops when timing is off).
 inline void rec_begin(Handle& h, cudaStream_t s)
 {
     Timing& t = h.timing;
     if (t.capacity && !t.paused) cudaEventRecord(t.start[t.head], s);
 }
 
-inline void rec_end(Handle& h, cudaStream_t s, int kernel, uint64_t hbm_bytes)
+inline void rec_end(Handle& h, cudaStream_t s, int kernel, uint64_t hbm_bytes, int launches = 1)
 {
     Timing& t = h.timing;
     if (!t.capacity || t.paused) return;
     cudaEventRecord(t.stop[t.head], s);
-    t.rec[t.head] = ar_launch_time_t{kernel, t.op, 0.0f, hbm_bytes};
+    t.rec[t.head] = ar_launch_time_t{kernel, t.op, 0.0f, hbm_bytes, launches};
     t.head = (t.head + 1) % (size_t)t.capacity;
     if (t.count < (size_t)t.capacity) ++t.count;
 }

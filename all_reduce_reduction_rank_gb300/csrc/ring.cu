@@ -181,22 +181,24 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
             int n_launch = 0;
             // per step every chunk moves once: N elements in all
             const uint64_t N = count, e = sizeof(typename Payload<DT>::scalar_t);
+            // one timing record per phase: the n-1 steps run back to back
+            uint64_t rs_bytes = 0;
+            rec_begin(h, s);
             for (int step = 0; step < NR - 1; ++step) {
-                const uint64_t rd = (step == 0 ? e : 4) * N + e * N;
-                const uint64_t wr = (step == NR - 2 ? e : 4) * N;
-                rec_begin(h, s);
-                launch_kernel(h, ring_rs_step_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1], buf[step & 1], C, count, step);
-                rec_end(h, s, AR_K_RING_RS_STEP, rd + wr);
+                rs_bytes += (step == 0 ? e : 4) * N + e * N + (step == NR - 2 ? e : 4) * N;
+                launch_kernel(h, ring_rs_step_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1],
+                              buf[step & 1], C, count, step);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }
+            rec_end(h, s, AR_K_RING_RS_STEP, rs_bytes, NR - 1);
+            rec_begin(h, s);
             for (int step = 0; step < NR - 1; ++step) {
-                rec_begin(h, s);
                 launch_kernel(h, ring_ag_step_kernel<NR, DT>, g_ag, kThreads, 0, s, op, C, count, step);
-                rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }
+            rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N * (NR - 1), NR - 1);
             *launches = n_launch;
             return AR_OK;
         });

@@ -149,15 +149,17 @@ typedef enum {
     AR_K_ALLREDUCE_RMSNORM = 12
 } ar_kernel;
 
-/* One recorded launch: which kernel, for which call, its device time
- * (cudaEventElapsedTime between events recorded on the call's stream right
- * before and after the launch) and the HBM bytes it must move
- * (algorithmic). */
+/* One timing record: `launches` consecutive launches of one kernel within
+ * one call (1, or the n-1 steps of a ring phase), the device time between
+ * events recorded on the call's stream right before the first and right after
+ * the last (cudaEventElapsedTime), and the HBM bytes they must move
+ * (algorithmic).  Average launch time = ms / launches. */
 typedef struct {
     int kernel;              /* ar_kernel */
     int op;                  /* ar_op of the call that launched it */
     float ms;
     uint64_t hbm_bytes;
+    int launches;
 } ar_launch_time_t;
 
 /* ---- handle --------------------------------------------------------------- */

@@ -317,3 +317,25 @@ def test_auto_runs_the_selected_call(policy, N):
     want = (oracle.ring if chosen == ar.AR_OP_RING else oracle.all_reduce)(xs, dtype)
     for r in range(n):
         np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
+
+
+def test_launch_timing_records():
+    n, N = 8, 1 << 20
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=12)
+    ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, 2 * N, timing=64) as h:
+        assert ar.ar_one_shot(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK
+        assert ar.ar_ring(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK
+        assert ar.ar_set_option(h, ar.AR_OPT_TIMING_PAUSE, 1) == ar.AR_OK
+        assert ar.ar_two_shot(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK     # not recorded
+        assert ar.ar_set_option(h, ar.AR_OPT_TIMING_PAUSE, 0) == ar.AR_OK
+        recs = ar.ar_timing(h)
+        assert ar.ar_timing(h) == []                                               # read clears
+        assert ar.ar_status(h) == ar.AR_OK
+    names = [r[0] for r in recs]
+    assert names == ["one_shot", "ring_rs_step", "ring_ag_step"]
+    assert [r[4] for r in recs] == [1, n - 1, n - 1]
+    assert all(r[2] > 0 for r in recs)
+    plan_ring = ar.ar_plan(ar.AR_OP_RING, n, N, "bf16")
+    assert recs[0][3] == 2 * n * N * 2
+    assert recs[1][3] + recs[2][3] == plan_ring.hbm_read_bytes + plan_ring.hbm_write_bytes

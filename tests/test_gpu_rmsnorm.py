@@ -71,7 +71,8 @@ def test_fused_epilogue_matches_the_unfused_chain(dtype, n, T, H):
     np.testing.assert_array_equal(bits(got_r), bits(want_r))
     ok = _within_one_ulp(got_y[0], want_y, dtype)
     assert ok.all(), f"{(~ok).sum()} elements beyond one ulp"
-    assert np.mean(bits(got_y[0]) == bits(want_y)) > 0.95
+    if dtype != "f32":   # rounding to 8 / 11 bits hides the fp32-level differences
+        assert np.mean(bits(got_y[0]) == bits(want_y)) > 0.95
     for y in got_y[1:]:
         np.testing.assert_array_equal(bits(y), bits(got_y[0]))
     S = T * H * E[dtype]
