@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
                 "orc_ll128_pack": ([vp, vp, sz, u64], None),
                 "orc_ll128_unpack": ([vp, vp, sz, u64], sz),
                 "orc_ll128_reduce": ([i32, pp, pp, sz, u64], sz),
+                "orc_ring_rounded": ([i32, pp, pp, sz, i32], i32),
+                "orc_tree": ([i32, pp, pp, sz, i32], i32),
+                "orc_all_gather_ring": ([i32, pp, sz, i32], i32),
                 "orc_allreduce_rmsnorm": ([i32, pp, vp, vp, ctypes.c_double, vp, vp, sz, sz, i32], None),
             }
             for name, (args, res) in sig.items():
@@ -182,6 +185,29 @@ def ring(inputs: list, dtype: str) -> list:
     rc = lib().orc_ring(n, _ptrs(inputs), _ptrs(out), N, _DT[dtype])
     if rc != 0:
         raise MemoryError("oracle ring: out of host memory")
+    return out
+
+
+def ring_rounded(inputs: list, dtype: str) -> list:
+    """The ring with partials rounded to the payload type at every hop."""
+    _check(inputs, dtype)
+    n, N = len(inputs), inputs[0].size
+    out = _outs(inputs, n)
+    if lib().orc_ring_rounded(n, _ptrs(inputs), _ptrs(out), N, _DT[dtype]) != 0:
+        raise MemoryError("oracle ring: out of host memory")
+    return out
+
+
+def tree(inputs: list, dtype: str) -> list:
+    """The pairwise (recursive-doubling) tree, each level rounded to the payload type."""
+    _check(inputs, dtype)
+    n, N = len(inputs), inputs[0].size
+    out = _outs(inputs, n)
+    rc = lib().orc_tree(n, _ptrs(inputs), _ptrs(out), N, _DT[dtype])
+    if rc == -1:
+        raise ValueError("the pairwise tree needs a power-of-two number of ranks")
+    if rc != 0:
+        raise MemoryError("oracle tree: out of host memory")
     return out
 
 

@@ -228,6 +228,33 @@ void orc_all_gather(int n, void* const* out, size_t N, int dt)
 /* Ring: the 2(n-1) steps of [MGPU] §ring all-reduce, simulated literally.  */
 /* ------------------------------------------------------------------------ */
 
+/* The ring's all-gather phase, steps s = 0..n-2: every rank r passes the
+ * completed chunk (r + 1 - s) mod n it holds to rank r + 1.  All sends of a
+ * step are taken from the state before the step.  On entry rank r holds
+ * chunk (r + 1) mod n complete in out[r]. */
+int orc_all_gather_ring(int n, void* const* out, size_t N, int dt)
+{
+    size_t C = orc_chunk_elems(n, N, dt), lo, hi, e = elem_size(dt);
+    char* snap = (char*)malloc(e * (size_t)n * (C ? C : 1));
+    if (!snap) return -1;
+    for (int s = 0; s < n - 1; ++s) {
+        for (int r = 0; r < n; ++r) {
+            int c = ((r + 1 - s) % n + n) % n;
+            chunk_range(c, C, N, &lo, &hi);
+            if (hi > lo)
+                memcpy(snap + (size_t)r * C * e, (const char*)out[r] + lo * e, (hi - lo) * e);
+        }
+        for (int r = 0; r < n; ++r) {
+            int d = (r + 1) % n, c = ((r + 1 - s) % n + n) % n;
+            chunk_range(c, C, N, &lo, &hi);
+            if (hi > lo)
+                memcpy((char*)out[d] + lo * e, snap + (size_t)r * C * e, (hi - lo) * e);
+        }
+    }
+    free(snap);
+    return 0;
+}
+
 /* Each rank keeps an fp32 working copy of its buffer.  Reduce-scatter step
  * s = 0..n-2: every rank r sends its chunk c = (r - s) mod n to rank
  * d = (r + 1) mod n, which adds it to its own chunk c.  After n-1 steps rank
@@ -240,8 +267,7 @@ int orc_ring(int n, const void* const* in, void* const* out, size_t N, int dt)
     size_t C = orc_chunk_elems(n, N, dt), lo, hi, e = elem_size(dt);
     float* work = (float*)malloc(sizeof(float) * (size_t)n * (N ? N : 1));
     float* sent = (float*)malloc(sizeof(float) * (size_t)n * (C ? C : 1));
-    char* snap = (char*)malloc(e * (size_t)n * (C ? C : 1));
-    if (!work || !sent || !snap) { free(work); free(sent); free(snap); return -1; }
+    if (!work || !sent) { free(work); free(sent); return -1; }
 
     for (int r = 0; r < n; ++r)
         for (size_t i = 0; i < N; ++i)
@@ -266,23 +292,9 @@ int orc_ring(int n, const void* const* in, void* const* out, size_t N, int dt)
         for (size_t i = lo; i < hi; ++i)
             narrow(out[r], i, work[(size_t)r * N + i], dt);
     }
-    for (int s = 0; s < n - 1; ++s) {
-        for (int r = 0; r < n; ++r) {
-            int c = ((r + 1 - s) % n + n) % n;
-            chunk_range(c, C, N, &lo, &hi);
-            if (hi > lo)
-                memcpy(snap + (size_t)r * C * e, (const char*)out[r] + lo * e, (hi - lo) * e);
-        }
-        for (int r = 0; r < n; ++r) {
-            int d = (r + 1) % n, c = ((r + 1 - s) % n + n) % n;
-            chunk_range(c, C, N, &lo, &hi);
-            if (hi > lo)
-                memcpy((char*)out[d] + lo * e, snap + (size_t)r * C * e, (hi - lo) * e);
-        }
-    }
     free(work);
     free(sent);
-    free(snap);
+    orc_all_gather_ring(n, out, N, dt);
     return 0;
 }
 
@@ -448,4 +460,87 @@ void orc_allreduce_rmsnorm(int n, const void* const* in, const void* residual, c
             narrow(norm_out, i, (float)y, dt);
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ring with partials rounded to the payload type at every hop.             */
+/* ------------------------------------------------------------------------ */
+
+/* The same 2(n-1) steps as orc_ring, but what a rank sends on is its
+ * partial sum rounded to the payload type, as a library that keeps its
+ * buffers in the payload type does: chunk c gets
+ *   RN( ... RN( RN(x_c + x_{c+1}) + x_{c+2} ) ... + x_{c+n-1} )
+ * with each + one binary32 addition.  For fp32 payloads it equals orc_ring. */
+int orc_ring_rounded(int n, const void* const* in, void* const* out, size_t N, int dt)
+{
+    size_t C = orc_chunk_elems(n, N, dt), lo, hi, e = elem_size(dt);
+    char* work = (char*)malloc(e * (size_t)n * (N ? N : 1));  /* each rank's buffer, payload type */
+    char* sent = (char*)malloc(e * (size_t)n * (C ? C : 1));
+    if (!work || !sent) { free(work); free(sent); return -1; }
+    for (int r = 0; r < n; ++r)
+        memcpy(work + (size_t)r * N * e, in[r], N * e);
+    for (int s = 0; s < n - 1; ++s) {
+        for (int r = 0; r < n; ++r) {
+            int c = ((r - s) % n + n) % n;
+            chunk_range(c, C, N, &lo, &hi);
+            if (hi > lo)
+                memcpy(sent + (size_t)r * C * e, work + ((size_t)r * N + lo) * e, (hi - lo) * e);
+        }
+        for (int r = 0; r < n; ++r) {
+            int d = (r + 1) % n, c = ((r - s) % n + n) % n;
+            chunk_range(c, C, N, &lo, &hi);
+            for (size_t i = lo; i < hi; ++i) {
+                float v = widen(sent, (size_t)r * C + (i - lo), dt) + widen(work, (size_t)d * N + i, dt);
+                narrow(work, (size_t)d * N + i, v, dt);
+            }
+        }
+    }
+    /* rank r holds chunk r+1 complete; the all-gather passes the chunks on */
+    for (int r = 0; r < n; ++r) {
+        chunk_range((r + 1) % n, C, N, &lo, &hi);
+        if (hi > lo)
+            memcpy((char*)out[r] + lo * e, work + ((size_t)r * N + lo) * e, (hi - lo) * e);
+    }
+    free(sent);
+    free(work);
+    orc_all_gather_ring(n, out, N, dt);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Pairwise (recursive-doubling) tree.                                      */
+/* ------------------------------------------------------------------------ */
+
+/* The PCIe-IPC blog post (bhfrc.com/news/61376, §3.1 算法骨架) pairs the
+ * ranks up and, in each of log2(n) levels, lets each rank read its own and its peer's data, add, and
+ * write the sum back to both.  Reading: at level l rank r pairs with
+ * r XOR 2^l; the buffers hold the payload type, so each level's sum is one
+ * binary32 add of the two widened values, rounded to the payload type.  n
+ * must be a power of two.  Both members of a pair add the same two values
+ * (a + b == b + a), so every rank ends with the same bits.  Returns -1 when
+ * n is not a power of two. */
+int orc_tree(int n, const void* const* in, void* const* out, size_t N, int dt)
+{
+    if (n < 2 || (n & (n - 1))) return -1;
+    size_t e = elem_size(dt);
+    char* cur = (char*)malloc(e * (size_t)n * (N ? N : 1));
+    char* nxt = (char*)malloc(e * (size_t)n * (N ? N : 1));
+    if (!cur || !nxt) { free(cur); free(nxt); return -2; }
+    for (int r = 0; r < n; ++r)
+        memcpy(cur + (size_t)r * N * e, in[r], N * e);
+    for (int d = 1; d < n; d <<= 1) {
+        for (int r = 0; r < n; ++r) {
+            int p = r ^ d;
+            for (size_t i = 0; i < N; ++i) {
+                float v = widen(cur, (size_t)r * N + i, dt) + widen(cur, (size_t)p * N + i, dt);
+                narrow(nxt, (size_t)r * N + i, v, dt);
+            }
+        }
+        char* t = cur; cur = nxt; nxt = t;
+    }
+    for (int r = 0; r < n; ++r)
+        memcpy(out[r], cur + (size_t)r * N * e, N * e);
+    free(cur);
+    free(nxt);
+    return 0;
 }

@@ -148,3 +148,15 @@ def hbm_ll128_unpack(count: int) -> tuple[int, int]:
 
 def hbm_ll128_reduce(n: int, count: int) -> tuple[int, int]:
     return n * 128 * ll128_lines(count), n * 128 * ll128_lines(count)
+
+
+def hbm_ring_rounded(n: int, N: int, e: int) -> tuple[int, int]:
+    """Partials in the payload type: every reduce-scatter step reads two
+    payloads and writes one; every all-gather step reads one and writes one."""
+    return 2 * e * N * (n - 1) + e * N * (n - 1), e * N * (n - 1) + e * N * (n - 1)
+
+
+def hbm_tree(n: int, N: int, e: int) -> tuple[int, int]:
+    """log2(n) levels; each reads and writes every rank's buffer once."""
+    levels = n.bit_length() - 1
+    return levels * n * e * N, levels * n * e * N

@@ -10,6 +10,7 @@
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import workloads
@@ -89,3 +90,58 @@ def test_ring_negative_zero_reading():
     out = oracle.ring([x.copy() for _ in range(3)], "f32")
     assert np.all(out[0].view(np.uint32) == 0x80000000)
     assert np.all(oracle.all_reduce([x.copy() for _ in range(3)], "f32")[0].view(np.uint32) == 0)
+
+
+# --- the ring with partials rounded at every hop --------------------------
+
+def test_rounded_ring_hand_worked_bf16():
+    # n = 3 bf16, N = 24 -> C = 8: chunk 0 = elements 0..7, 1 = 8..15, 2 = 16..23.
+    # Rank 0 holds 256, ranks 1 and 2 hold 1; bf16 spacing at 256 is 2.
+    #   chunk 0 (order 0,1,2): RN(RN(256 + 1) + 1) = RN(256 + 1) = 256   (257 ties to even)
+    #   chunk 1 (order 1,2,0): RN(RN(1 + 1) + 256) = 258
+    #   chunk 2 (order 2,0,1): RN(RN(1 + 256) + 1) = 256
+    # while fp32 partials give 258 everywhere.
+    b = lambda v: oracle.f32_to_bf16(np.full(24, v, np.float32))
+    xs = [b(256.0), b(1.0), b(1.0)]
+    want = np.array([256.0] * 8 + [258.0] * 8 + [256.0] * 8, np.float32)
+    for o in oracle.ring_rounded(xs, "bf16"):
+        np.testing.assert_array_equal(oracle.bf16_to_f32(o), want)
+    for o in oracle.ring(xs, "bf16"):
+        np.testing.assert_array_equal(oracle.bf16_to_f32(o), np.full(24, 258.0, np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("n", [2, 5, 8])
+def test_rounded_ring_per_element_with_library_arithmetic(dtype, n):
+    # chunk c: p = x_c; p = round(p + x_{c+j}) for j = 1..n-1, with numpy's
+    # float32 add and torch's / numpy's rounding to the payload type
+    N = 999
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=60 + n)
+    C = oracle.chunk_elems(n, N, dtype)
+    f = [oracle.to_f32(x, dtype) for x in xs]
+
+    def rnd(v):
+        if dtype == "bf16":
+            return torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+        return v.astype(np.float16).astype(np.float32)
+
+    want = np.empty(N, np.float32)
+    for c in range(n):
+        lo, hi = min(c * C, N), min((c + 1) * C, N)
+        p = f[c][lo:hi].copy()
+        for j in range(1, n):
+            p = rnd(p + f[(c + j) % n][lo:hi])
+        want[lo:hi] = p
+    for o in oracle.ring_rounded(xs, dtype):
+        np.testing.assert_array_equal(oracle.to_f32(o, dtype), want)
+
+
+@pytest.mark.parametrize("n", [3, 8])
+def test_rounded_ring_equals_ring_for_f32_and_for_exact_integers(n):
+    xs = workloads.rank_inputs(n, 4099, "f32", "normal", seed=n)
+    for a, b in zip(oracle.ring_rounded(xs, "f32"), oracle.ring(xs, "f32")):
+        np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+    xi = workloads.rank_inputs(n, 4099, "bf16", "int8", seed=n)
+    exact = sum(oracle.to_f32(x, "bf16").astype(np.int64) for x in xi)
+    for o in oracle.ring_rounded(xi, "bf16"):
+        np.testing.assert_array_equal(oracle.to_f32(o, "bf16").astype(np.int64), exact)

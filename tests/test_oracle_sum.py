@@ -68,8 +68,10 @@ def test_brute_force_n2_bf16_all_a():
     a = np.repeat(a_all, b_set.size)
     b = np.tile(b_set, a_all.size)
     got = oracle.all_reduce([a, b], "bf16")
-    # one binary32 add (numpy) then one round-to-nearest-even to bf16 (torch)
-    s = oracle.bf16_to_f32(a) + oracle.bf16_to_f32(b)
+    # one binary32 add (numpy) then one round-to-nearest-even to bf16 (torch);
+    # sums beyond the binary32 range overflow to +-Inf on both sides
+    with np.errstate(over="ignore"):
+        s = oracle.bf16_to_f32(a) + oracle.bf16_to_f32(b)
     ref = torch.from_numpy(s).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     gf, rf = oracle.bf16_to_f32(got[0]), oracle.bf16_to_f32(ref)
     same = (got[0] == ref) | (np.isnan(gf) & np.isnan(rf))
