@@ -63,6 +63,7 @@ int check_multi(int op, int n, size_t max_bytes, const void* const* in, void* co
     if (n < 2 || n > kMaxRanks) return AR_ERR_INVALID;
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
     if (is_ll_op(op) && dt != AR_F32) return AR_ERR_INVALID;
+    if (op == AR_OP_TREE && (n & (n - 1))) return AR_ERR_INVALID;
     if (!in || !out) return AR_ERR_INVALID;
     for (int r = 0; r < n; ++r)
         if (!in[r] || !out[r]) return AR_ERR_INVALID;
@@ -183,6 +184,46 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         t->launches = count ? 1 : 0;
         t->hbm_read_bytes = nn * 128 * L;
         t->hbm_write_bytes = nn * 4 * N;
+        break;
+    case AR_OP_RING_ROUNDED:
+        t->link_bytes_per_rank = 2.0 * (double)(nn - 1) * (double)S / (double)nn;
+        t->steps = 2 * (n - 1);
+        t->launches = count ? 2 * (n - 1) : 0;
+        t->hbm_read_bytes = 2 * e * N * (nn - 1) + e * N * (nn - 1);
+        t->hbm_write_bytes = e * N * (nn - 1) + e * N * (nn - 1);
+        break;
+    case AR_OP_TREE: {
+        int levels = 0;
+        while ((1 << levels) < n) ++levels;
+        t->link_bytes_per_rank = (double)levels * (double)S;   // the peer's buffer, once per level
+        t->steps = levels;
+        t->launches = count ? levels : 0;
+        t->hbm_read_bytes = (uint64_t)levels * nn * S;
+        t->hbm_write_bytes = (uint64_t)levels * nn * S;
+        break;
+    }
+    case AR_OP_RING_PERSISTENT: {
+        const uint64_t lines = persist_lines_per_step(n, count, dt);
+        t->link_bytes_per_rank = 2.0 * (double)(nn - 1) * (double)S / (double)nn;
+        t->steps = 2 * (n - 1);
+        t->launches = count ? 1 : 0;
+        t->hbm_read_bytes = nn * S + (2 * nn - 2) * 128 * lines;
+        t->hbm_write_bytes = nn * S + (2 * nn - 2) * 128 * lines;
+        break;
+    }
+    case AR_OP_ONE_SHOT_PUSH:
+        t->link_bytes_per_rank = (double)(nn - 1) * (double)S;  // pushed to the peers
+        t->steps = 1;
+        t->launches = count ? 2 : 0;
+        t->hbm_read_bytes = nn * S + nn * nn * S;
+        t->hbm_write_bytes = nn * (nn - 1) * S + nn * S;
+        break;
+    case AR_OP_ONE_SHOT_COPYIN:
+        t->link_bytes_per_rank = (double)(nn - 1) * (double)S;
+        t->steps = 1;
+        t->launches = count ? 1 : 0;
+        t->hbm_read_bytes = 2 * nn * S;
+        t->hbm_write_bytes = 2 * nn * S;
         break;
     case AR_OP_ALLREDUCE_RMSNORM:
         t->link_bytes_per_rank = (double)(nn - 1) * (double)S;
@@ -347,10 +388,11 @@ size_t ar_ll128_bytes(size_t payload_bytes) { return 128u * ((payload_bytes + 11
 
 int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
 {
-    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_ALLREDUCE_RMSNORM) return AR_ERR_INVALID;
+    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_RING_PERSISTENT) return AR_ERR_INVALID;
     const bool multi =
-        op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE || op == AR_OP_ALLREDUCE_RMSNORM;
+        op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE || op >= AR_OP_ALLREDUCE_RMSNORM;
     if (multi && (n_ranks < 2 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;
+    if (op == AR_OP_TREE && (n_ranks & (n_ranks - 1))) return AR_ERR_INVALID;
     if (!multi && (n_ranks < 1 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;  // buffers packed
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
     plan(op, n_ranks, count, dt, t);
@@ -364,7 +406,9 @@ int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in, 
         if (n_ranks < 1 || n_ranks > kMaxRanks || dt != AR_F32) return AR_ERR_INVALID;
         return check_batch(op, n_ranks, max_bytes, in, out, count);
     }
-    if (op != AR_OP_ONE_SHOT && op != AR_OP_TWO_SHOT && op != AR_OP_RING && !is_ll_op(op))
+    if (op != AR_OP_ONE_SHOT && op != AR_OP_TWO_SHOT && op != AR_OP_RING && op != AR_OP_ONE_SHOT_PUSH &&
+        op != AR_OP_ONE_SHOT_COPYIN && op != AR_OP_RING_ROUNDED && op != AR_OP_TREE &&
+        op != AR_OP_RING_PERSISTENT && !is_ll_op(op))
         return AR_ERR_INVALID;
     return check_multi(op, n_ranks, max_bytes, in, out, count, dt);
 }
@@ -389,6 +433,7 @@ int ar_create(int n_ranks, size_t max_bytes, ar_handle* out)
         if (c_dt > cmax) cmax = c_dt;
     }
     h.ring_chunk_max = cmax;
+    h.stage_slot = (max_bytes + 255u) / 256u * 256u;
     if (rc == AR_OK && cudaMalloc(&h.ring_scratch, 2u * (size_t)n_ranks * cmax * sizeof(float)) != cudaSuccess)
         rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaMalloc(&h.status, sizeof(DevStatus)) != cudaSuccess) rc = AR_ERR_CUDA;
@@ -414,6 +459,9 @@ int ar_destroy(ar_handle hd)
         int r = cudaDeviceSynchronize() == cudaSuccess ? AR_OK : AR_ERR_CUDA;
         if (cudaFree(h->ring_scratch) != cudaSuccess) r = AR_ERR_CUDA;
         if (cudaFree(h->status) != cudaSuccess) r = AR_ERR_CUDA;
+        if (h->push_stage && cudaFree(h->push_stage) != cudaSuccess) r = AR_ERR_CUDA;
+        if (h->registered && cudaFree(h->registered) != cudaSuccess) r = AR_ERR_CUDA;
+        if (h->persist && cudaFree(h->persist) != cudaSuccess) r = AR_ERR_CUDA;
         free_timing(h->timing);
         return r;
     });
@@ -455,6 +503,49 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
         if (value < 0) return AR_ERR_INVALID;
         h->auto_handoff = value;
         return AR_OK;
+    case AR_OPT_PUSH_STAGING:
+    case AR_OPT_REGISTERED: {
+        if (value != 0 && value != 1) return AR_ERR_INVALID;
+        uint8_t** buf = option == AR_OPT_PUSH_STAGING ? &h->push_stage : &h->registered;
+        const size_t bytes = (option == AR_OPT_PUSH_STAGING ? (size_t)h->n * h->n : (size_t)h->n) * h->stage_slot;
+        return on_device(*h, [&] {
+            if (cudaDeviceSynchronize() != cudaSuccess) return (int)AR_ERR_CUDA;
+            if (*buf) {
+                cudaFree(*buf);
+                *buf = nullptr;
+            }
+            if (value == 1 && cudaMalloc(reinterpret_cast<void**>(buf), bytes) != cudaSuccess) {
+                cudaGetLastError();
+                *buf = nullptr;
+                return (int)AR_ERR_CUDA;
+            }
+            return (int)AR_OK;
+        });
+    }
+    case AR_OPT_PERSISTENT:
+        if (value != 0 && value != 1) return AR_ERR_INVALID;
+        return on_device(*h, [&] {
+            if (cudaDeviceSynchronize() != cudaSuccess) return (int)AR_ERR_CUDA;
+            if (h->persist) {
+                cudaFree(h->persist);
+                h->persist = nullptr;
+            }
+            if (value == 0) return (int)AR_OK;
+            const size_t bytes = persist_bytes(h->n, h->max_bytes, h->sm_count);
+            // zeroed: no flag, acknowledgement or abort word of a call matches 0
+            if (cudaMalloc(reinterpret_cast<void**>(&h->persist), bytes) != cudaSuccess ||
+                cudaMemset(h->persist, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                if (h->persist) cudaFree(h->persist);
+                h->persist = nullptr;
+                return (int)AR_ERR_CUDA;
+            }
+            return (int)AR_OK;
+        });
+    case AR_OPT_ABSENT_RANK:
+        if (value < -1 || value >= h->n) return AR_ERR_INVALID;
+        h->persist_absent = (int)value;
+        return AR_OK;
     case AR_OPT_PDL:
         if (value < 0 || value > 1) return AR_ERR_INVALID;
         h->pdl = (int)value;
@@ -476,6 +567,40 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
 int ar_one_shot(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
 {
     return all_reduce_call(AR_OP_ONE_SHOT, launch_one_shot, h, in, out, count, dt, s);
+}
+
+int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                     ar_stream_t s)
+{
+    Handle* hh = get(h);
+    if (!hh || !hh->push_stage) return AR_ERR_INVALID;
+    return all_reduce_call(AR_OP_ONE_SHOT_PUSH, launch_one_shot_push, h, in, out, count, dt, s);
+}
+
+int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                       ar_stream_t s)
+{
+    Handle* hh = get(h);
+    if (!hh || !hh->registered) return AR_ERR_INVALID;
+    return all_reduce_call(AR_OP_ONE_SHOT_COPYIN, launch_one_shot_copyin, h, in, out, count, dt, s);
+}
+
+int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
+{
+    return all_reduce_call(AR_OP_RING_ROUNDED, launch_ring_rounded, h, in, out, count, dt, s);
+}
+
+int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
+{
+    return all_reduce_call(AR_OP_TREE, launch_tree, h, in, out, count, dt, s);
+}
+
+int ar_ring_persistent(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                       ar_stream_t s)
+{
+    Handle* hh = get(h);
+    if (!hh || !hh->persist) return AR_ERR_INVALID;
+    return all_reduce_call(AR_OP_RING_PERSISTENT, launch_ring_persistent, h, in, out, count, dt, s);
 }
 
 int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)

@@ -43,6 +43,12 @@ struct Handle {
     int64_t auto_alpha_ns = 1500;
     int64_t auto_beta_mbs = 450000;
     int64_t auto_handoff = 8 << 20;
+    uint8_t* push_stage = nullptr;  // [n][n][stage_slot] (AR_OPT_PUSH_STAGING)
+    uint8_t* registered = nullptr;  // [n][stage_slot] (AR_OPT_REGISTERED)
+    size_t stage_slot = 0;          // max_bytes rounded up to 256
+    uint8_t* persist = nullptr;     // ar_ring_persistent's inboxes, acks, abort word (AR_OPT_PERSISTENT)
+    uint64_t persist_seq = 0;       // calls of ar_ring_persistent so far
+    int persist_absent = -1;        // AR_OPT_ABSENT_RANK
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements
     DevStatus* status = nullptr;    // device
@@ -129,6 +135,18 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
                     cudaStream_t s, int* launches);
 int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                 cudaStream_t s, int* launches);
+int launch_ring_rounded(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                        int* launches);
+int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                         int* launches);
+int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                           cudaStream_t s, int* launches);
+int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                int* launches);
+int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                           cudaStream_t s, int* launches);
+size_t persist_bytes(int n, size_t max_bytes, int sm_count);
+uint64_t persist_lines_per_step(int n, size_t count, int dt);
 int launch_ll_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint32_t step,
                    cudaStream_t s);
 int launch_ll_unpack(Handle& h, int nb, const void* const* lines, float* const* dst, size_t count, uint32_t step,

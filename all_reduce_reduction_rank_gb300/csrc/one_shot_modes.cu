@@ -1,0 +1,131 @@
+// Two other ways to run the one-shot all-reduce, both named by the pages.
+//
+// Push ("SGLang JIT custom all-reduce" notes, §实现: one-shot pull, one-shot
+// push and two-shot pull): every rank writes its buffer into a staging slot
+// of every peer, then every rank reduces its own staging slots locally.  The
+// emulation keeps one staging slot per (receiving rank, sending rank) pair in
+// the handle (n x n x max_bytes, allocated by AR_OPT_PUSH_STAGING).  Push
+// phase: reads n S, writes n (n-1) S; reduce phase: every rank reads its n
+// slots (its own input in place of its own slot) and writes its output:
+// reads n^2 S, writes n S.
+//
+// Copy-in (same notes, §5 写回: outside graph capture the kernel reads a
+// pre-registered pull buffer that cudaMemcpyAsync filled from the input, and
+// the output may then be the input itself): each rank's input is copied into
+// its registered buffer (AR_OPT_REGISTERED, n x max_bytes) with
+// cudaMemcpyAsync, as the pages do, and the one-shot kernel reads the
+// registered buffers.
+//
+// Both give the one-shot result bit for bit: fp32 sums in rank order from +0,
+// one rounding.
+#include "common.cuh"
+
+namespace argb {
+namespace {
+
+// stage[q][r] for r != q  <-  in[r].   Grid: blockIdx.y = sending rank r.
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads)
+push_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ stage, size_t slot_bytes, size_t nvec,
+            size_t count)
+{
+    pdl_acquire();
+    using T = typename Payload<DT>::scalar_t;
+    const int r = blockIdx.y;
+    const uint4* const src = static_cast<const uint4*>(in.p[r]);
+    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+        const uint4 x = ld16(src + v);
+#pragma unroll
+        for (int q = 0; q < NR; ++q)
+            if (q != r) st16(reinterpret_cast<uint4*>(stage + ((size_t)q * NR + r) * slot_bytes) + v, x);
+    }
+    pdl_release();
+    if (blockIdx.x == gridDim.x - 1) {
+        const size_t i = nvec * kVecElems<DT> + threadIdx.x;
+        if (i < count) {
+            const T x = static_cast<const T*>(in.p[r])[i];
+#pragma unroll
+            for (int q = 0; q < NR; ++q)
+                if (q != r) reinterpret_cast<T*>(stage + ((size_t)q * NR + r) * slot_bytes)[i] = x;
+        }
+    }
+}
+
+// out[q] = rank-order sum of stage[q][0..n-1], with in[q] as rank q's own term.
+// Grid: blockIdx.y = receiving rank q.
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads)
+push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
+                   const uint8_t* __restrict__ stage, size_t slot_bytes, size_t nvec, size_t count)
+{
+    pdl_acquire();
+    using T = typename Payload<DT>::scalar_t;
+    const int q = blockIdx.y;
+    auto slot = [&](int r) -> const void* {
+        return r == q ? in.p[q] : static_cast<const void*>(stage + ((size_t)q * NR + r) * slot_bytes);
+    };
+    uint4* const dst = static_cast<uint4*>(out.p[q]);
+    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+        uint4 x[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) x[r] = ld16(static_cast<const uint4*>(slot(r)) + v);
+        st16(dst + v, reduce_rank_order<DT, NR>(x));
+    }
+    pdl_release();
+    if (blockIdx.x == gridDim.x - 1) {
+        const size_t i = nvec * kVecElems<DT> + threadIdx.x;
+        if (i < count) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) acc = acc + Payload<DT>::widen1(static_cast<const T*>(slot(r))[i]);
+            static_cast<T*>(out.p[q])[i] = Payload<DT>::narrow1(acc);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                         int* launches)
+{
+    return dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            CPtrs<NR> ip;
+            MPtrs<NR> op;
+            for (int q = 0; q < NR; ++q) {
+                ip.p[q] = in[q];
+                op.p[q] = out[q];
+            }
+            const size_t nvec = count / kVecElems<DT>;
+            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            const dim3 grid(grid_for_rows(h, nvec, NR), NR);
+            rec_begin(h, s);
+            launch_kernel(h, push_kernel<NR, DT>, grid, kThreads, 0, s, ip, h.push_stage, h.stage_slot, nvec, count);
+            rec_end(h, s, AR_K_PUSH, (uint64_t)NR * S + (uint64_t)NR * (NR - 1) * S);
+            if (launch_status() != AR_OK) return AR_ERR_CUDA;
+            rec_begin(h, s);
+            launch_kernel(h, push_reduce_kernel<NR, DT>, grid, kThreads, 0, s, ip, op,
+                          (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
+            rec_end(h, s, AR_K_PUSH_REDUCE, (uint64_t)NR * NR * S + (uint64_t)NR * S);
+            *launches = 2;
+            return launch_status();
+        });
+    });
+}
+
+int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                           cudaStream_t s, int* launches)
+{
+    const size_t bytes = count * elem_bytes(dt);
+    const void* reg[kMaxRanks];
+    for (int r = 0; r < h.n; ++r) {
+        reg[r] = h.registered + (size_t)r * h.stage_slot;
+        if (cudaMemcpyAsync(const_cast<void*>(reg[r]), in[r], bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return AR_ERR_CUDA;
+    }
+    return launch_one_shot(h, reg, out, count, dt, s, launches);
+}
+
+}  // namespace argb

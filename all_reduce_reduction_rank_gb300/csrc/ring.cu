@@ -20,6 +20,11 @@
 // HBM traffic per reduce-scatter step: n chunk reads of the sender's partial
 // (payload at step 0), n of the receiver's payload, n partial writes
 // (payload at the last step); per all-gather step n chunk reads and writes.
+//
+// ar_ring_rounded runs the same steps with the partials kept in the payload
+// type, rounded at every hop (a library whose buffers hold the payload type
+// adds each received chunk to its own copy that way): 2 e N read and e N
+// written per reduce-scatter step.
 #include "common.cuh"
 
 namespace argb {
@@ -30,15 +35,16 @@ constexpr int kAgUnroll = 4;
 
 // Reduce-scatter step s.  Grid: blockIdx.y = sending rank r (block-uniform
 // chunk, pointers and step role), blockIdx.x strides over the chunk's 16-byte
-// vectors.  p_read / p_write: fp32 partials, rank-major, C elements per rank.
-template <int NR, int DT>
+// vectors.  p_read / p_write: partials, rank-major, C elements per rank; fp32,
+// or (HR, hop rounding) the payload type.
+template <int NR, int DT, bool HR>
 __global__ void __launch_bounds__(kThreads)
 ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                     const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s)
 {
     pdl_acquire();
     constexpr int VE = kVecElems<DT>;
-    constexpr int PW = VE / 4;          // 16-byte words of fp32 partial per payload vector
+    constexpr int PW = HR ? 1 : VE / 4;  // 16-byte words of partial per payload vector
     constexpr int U = kRsUnroll;
     using T = typename Payload<DT>::scalar_t;
     const int r = blockIdx.y;
@@ -54,6 +60,8 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     T* const od = static_cast<T*>(out.p[d]) + e_lo;
     const float* const pr = p_read + (size_t)r * C;
     float* const pw = p_write + (size_t)d * C;
+    const T* const prh = reinterpret_cast<const T*>(p_read) + (size_t)r * C;   // HR layout
+    T* const pwh = reinterpret_cast<T*>(p_write) + (size_t)d * C;
     const size_t span = (size_t)kThreads * U;
     for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
         uint4 up[U][PW], own[U];
@@ -64,6 +72,8 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                 // the partial rank r sends (its own payload at step 0) ...
                 if (first) {
                     up[u][0] = ld16(xr + k * VE);
+                } else if (HR) {
+                    up[u][0] = ld16(prh + k * VE);
                 } else {
 #pragma unroll
                     for (int j = 0; j < PW; ++j) up[u][j] = ld16(pr + k * VE + 4 * j);
@@ -77,7 +87,7 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             const size_t k = base + (size_t)u * kThreads + threadIdx.x;
             if (k < nv) {
                 float a[VE];
-                if (first) {
+                if (first || HR) {
                     // widen exactly (no zero start: the first hop adds two raw values)
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -94,6 +104,8 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                 accumulate<DT>(a, own[u]);
                 if (last) {
                     st16(od + k * VE, round_vec<DT>(a));
+                } else if (HR) {
+                    st16(pwh + k * VE, round_vec<DT>(a));
                 } else {
 #pragma unroll
                     for (int j = 0; j < PW; ++j)
@@ -109,9 +121,10 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     if (blockIdx.x == gridDim.x - 1) {
         const size_t j = nv * VE + threadIdx.x;
         if (j < len) {
-            const float upv = first ? Payload<DT>::widen1(xr[j]) : pr[j];
+            const float upv = first ? Payload<DT>::widen1(xr[j]) : HR ? Payload<DT>::widen1(prh[j]) : pr[j];
             const float sum = upv + Payload<DT>::widen1(xd[j]);
             if (last) od[j] = Payload<DT>::narrow1(sum);
+            else if (HR) pwh[j] = Payload<DT>::narrow1(sum);
             else pw[j] = sum;
         }
     }
@@ -159,8 +172,9 @@ ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t coun
 
 }  // namespace
 
-int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
-                cudaStream_t s, int* launches)
+template <bool HR>
+int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                     int* launches)
 {
     return dispatch_dtype(dt, [&](auto dtc) -> int {
         constexpr int DT = decltype(dtc)::value;
@@ -185,13 +199,14 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
             uint64_t rs_bytes = 0;
             rec_begin(h, s);
             for (int step = 0; step < NR - 1; ++step) {
-                rs_bytes += (step == 0 ? e : 4) * N + e * N + (step == NR - 2 ? e : 4) * N;
-                launch_kernel(h, ring_rs_step_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1],
+                const uint64_t pe = HR ? e : 4;   // bytes of one partial
+                rs_bytes += (step == 0 ? e : pe) * N + e * N + (step == NR - 2 ? e : pe) * N;
+                launch_kernel(h, ring_rs_step_kernel<NR, DT, HR>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1],
                               buf[step & 1], C, count, step);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }
-            rec_end(h, s, AR_K_RING_RS_STEP, rs_bytes, NR - 1);
+            rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, NR - 1);
             rec_begin(h, s);
             for (int step = 0; step < NR - 1; ++step) {
                 launch_kernel(h, ring_ag_step_kernel<NR, DT>, g_ag, kThreads, 0, s, op, C, count, step);
@@ -203,6 +218,18 @@ int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count
             return AR_OK;
         });
     });
+}
+
+int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                int* launches)
+{
+    return launch_ring_impl<false>(h, in, out, count, dt, s, launches);
+}
+
+int launch_ring_rounded(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                        int* launches)
+{
+    return launch_ring_impl<true>(h, in, out, count, dt, s, launches);
 }
 
 }  // namespace argb

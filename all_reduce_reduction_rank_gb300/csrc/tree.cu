@@ -1,0 +1,97 @@
+// Pairwise tree all-reduce (recursive doubling), emulated level by level.
+//
+// The PCIe-IPC blog post (bhfrc.com/news/61376, §3.1 算法骨架) pairs the
+// ranks up: in each of log2(n) levels every rank reads its own data
+// and its peer's, adds them, and writes the sum back to both.  At level l
+// rank r pairs with r XOR 2^l, so n must be a power of two.  The buffers hold
+// the payload type, so every level's sum is one binary32 add of the two
+// widened values, rounded to the payload type.  Both members of a pair add the
+// same two values, so one thread computes the sum once and writes it to both.
+//
+// Emulation: one launch per level.  Level 0 reads in[r], in[r ^ 1] and writes
+// out[r], out[r ^ 1]; later levels work in place on out[].  Every element of
+// every rank is read once and written once per level: HBM per level n S read,
+// n S write.
+#include "common.cuh"
+
+namespace argb {
+namespace {
+
+// One level.  Grid: blockIdx.y = pair j in [0, NR/2); its lower rank r has
+// bit `d` clear, its upper rank is r | d.
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads)
+tree_level_kernel(const __grid_constant__ CPtrs<NR> src, const __grid_constant__ MPtrs<NR> dst, int d, size_t nvec,
+                  size_t count)
+{
+    pdl_acquire();
+    using T = typename Payload<DT>::scalar_t;
+    constexpr int VE = kVecElems<DT>;
+    const int j = blockIdx.y;
+    const int r = ((j & ~(d - 1)) << 1) | (j & (d - 1));   // j with a 0 inserted at bit log2(d)
+    const int p = r | d;
+    const uint4* const a = static_cast<const uint4*>(src.p[r]);
+    const uint4* const b = static_cast<const uint4*>(src.p[p]);
+    uint4* const oa = static_cast<uint4*>(dst.p[r]);
+    uint4* const ob = static_cast<uint4*>(dst.p[p]);
+    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+        const uint4 xa = ld16(a + v), xb = ld16(b + v);
+        float fa[VE], fb[VE];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            Payload<DT>::widen(word(xa, w), fa + w * Payload<DT>::kPerWord);
+            Payload<DT>::widen(word(xb, w), fb + w * Payload<DT>::kPerWord);
+        }
+#pragma unroll
+        for (int k = 0; k < VE; ++k) fa[k] = fa[k] + fb[k];
+        const uint4 y = round_vec<DT>(fa);
+        st16(oa + v, y);
+        st16(ob + v, y);
+    }
+    pdl_release();
+    if (blockIdx.x == gridDim.x - 1) {   // the ragged tail (< VE elements)
+        const size_t i = nvec * VE + threadIdx.x;
+        if (i < count) {
+            const float y = Payload<DT>::widen1(static_cast<const T*>(src.p[r])[i]) +
+                            Payload<DT>::widen1(static_cast<const T*>(src.p[p])[i]);
+            static_cast<T*>(dst.p[r])[i] = Payload<DT>::narrow1(y);
+            static_cast<T*>(dst.p[p])[i] = Payload<DT>::narrow1(y);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                int* launches)
+{
+    if (h.n & (h.n - 1)) return AR_ERR_INVALID;
+    return dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            CPtrs<NR> ip, op_c;
+            MPtrs<NR> op;
+            for (int q = 0; q < NR; ++q) {
+                ip.p[q] = in[q];
+                op_c.p[q] = out[q];
+                op.p[q] = out[q];
+            }
+            const size_t nvec = count / kVecElems<DT>;
+            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            const dim3 grid(grid_for_rows(h, nvec, NR / 2), NR / 2);
+            int levels = 0;
+            rec_begin(h, s);
+            for (int d = 1; d < NR; d <<= 1, ++levels) {
+                if (launch_kernel(h, tree_level_kernel<NR, DT>, grid, kThreads, 0, s, d == 1 ? ip : op_c, op, d, nvec,
+                                  count) != cudaSuccess)
+                    return AR_ERR_CUDA;
+            }
+            rec_end(h, s, AR_K_TREE_LEVEL, 2ull * NR * S * (uint64_t)levels, levels);
+            *launches = levels;
+            return launch_status();
+        });
+    });
+}
+
+}  // namespace argb

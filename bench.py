@@ -411,6 +411,70 @@ def fused_epilogue(wl, peak: float, batches: int = 7, calls: int = 200) -> list:
     return out
 
 
+VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
+
+
+def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
+    """Every all-reduce call of the library on the same n = 8 bf16 buffers, at
+    64 KiB, 1 MiB, 8 MiB and 64 MiB per rank: one-shot, its push and copy-in
+    forms, two-shot, the ring (one launch per step), the ring with hop
+    rounding, the persistent single-launch LL128 ring and the pairwise tree.
+    Timing as in `sweep` (back-to-back calls on rotating slots, one event pair
+    per batch, median of the batches); bytes are each call's algorithmic HBM
+    bytes (ar_plan)."""
+    import ctypes
+
+    import torch
+
+    import all_reduce_reduction_rank_gb300 as ar
+
+    n, L, h = wl.n, wl.L, wl.h
+    for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
+        ar.check(ar.ar_set_option(h, opt, 1), "variant buffers")
+    algos = (("one_shot", L.ar_one_shot, ar.AR_OP_ONE_SHOT),
+             ("one_shot_push", L.ar_one_shot_push, ar.AR_OP_ONE_SHOT_PUSH),
+             ("one_shot_copyin", L.ar_one_shot_copyin, ar.AR_OP_ONE_SHOT_COPYIN),
+             ("two_shot", L.ar_two_shot, ar.AR_OP_TWO_SHOT),
+             ("ring", L.ar_ring, ar.AR_OP_RING),
+             ("ring_rounded", L.ar_ring_rounded, ar.AR_OP_RING_ROUNDED),
+             ("ring_persistent", L.ar_ring_persistent, ar.AR_OP_RING_PERSISTENT),
+             ("tree", L.ar_tree, ar.AR_OP_TREE))
+    res = {a[0]: [] for a in algos}
+    for S in VARIANT_SIZES:
+        if S > wl.S:
+            continue
+        N = S // 2
+        slots = wl.S // S
+        P = lambda ts, k: (ctypes.c_void_p * n)(*[t.data_ptr() + k * S for t in ts])
+        pin = [P(wl.ins, k) for k in range(slots)]
+        pout = [P(wl.outs, k) for k in range(slots)]
+        calls = max(min_calls, min(slots, 4096))
+        for name, call, op in algos:
+            t = ar.ar_plan(op, n, N, "bf16")
+            b = t.hbm_read_bytes + t.hbm_write_bytes
+            for k in range(min(slots, 4)):
+                ar.check(call(h, pin[k], pout[k], N, 1, wl.s), name)
+            per_call = []
+            for _ in range(batches):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(wl.stream)
+                for i in range(calls):
+                    call(h, pin[i % slots], pout[i % slots], N, 1, wl.s)
+                e1.record(wl.stream)
+                e1.synchronize()
+                per_call.append(e0.elapsed_time(e1) / calls)
+            ar.check(ar.ar_status(h), name)
+            ms = statistics.median(per_call)
+            gbs = b / (ms * 1e-3) / 1e9
+            algbw = S / (ms * 1e-3) / 1e9
+            res[name].append({"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
+                              "launches": t.launches, "calls_per_batch": calls})
+    for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
+        ar.check(ar.ar_set_option(h, opt, 0), "variant buffers")
+    return res
+
+
 def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     """The same step through the public API with HOST buffers: every step
     copies its inputs from pinned host memory, runs, and reads its results
@@ -508,6 +572,7 @@ def run_ours(args):
 
     sw = sweep(wl, peak) if args.sweep else None
     fe = fused_epilogue(wl, peak) if args.sweep else None
+    va = variants(wl, peak) if args.sweep else None
     e2e = e2e_leg(wl, max(3, min(args.steps, args.e2e_steps)), bytes_step) if args.e2e else None
     cpu = None
     if world == 1 and rank == 0 and args.cpu_baseline:
@@ -530,7 +595,7 @@ def run_ours(args):
                           "launches_recorded": sum(r[4] for r in records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),
         "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "sweep": sw,
-        "fused_epilogue": fe,
+        "fused_epilogue": fe, "variants": va,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -59,7 +59,8 @@ enum {
     AR_ERR_TOO_LARGE = -3,    /* count x element size > max_bytes */
     AR_ERR_CUDA = -4,         /* a CUDA runtime call or a launch failed */
     AR_ERR_FLAG_TIMEOUT = -5, /* an LL/LL128 line never showed the expected flag */
-    AR_ERR_WAIT_TIMEOUT = -6  /* a kernel's bounded wait for its own bulk copies ran out */
+    AR_ERR_WAIT_TIMEOUT = -6  /* a kernel's bounded wait for its own bulk copies, or the
+                                 persistent ring's wait for a peer's acknowledgement, ran out */
 };
 
 /* Which call an ar_traffic_t describes. */
@@ -74,7 +75,12 @@ typedef enum {
     AR_OP_LL128_PACK = 7,
     AR_OP_LL128_UNPACK = 8,
     AR_OP_LL128_REDUCE = 9,
-    AR_OP_ALLREDUCE_RMSNORM = 10
+    AR_OP_ALLREDUCE_RMSNORM = 10,
+    AR_OP_ONE_SHOT_PUSH = 11,
+    AR_OP_ONE_SHOT_COPYIN = 12,
+    AR_OP_RING_ROUNDED = 13,
+    AR_OP_TREE = 14,
+    AR_OP_RING_PERSISTENT = 15
 } ar_op;
 
 /* Traffic of one call.
@@ -127,6 +133,17 @@ enum {
     AR_OPT_AUTO_BETA_MBS = 9,/* model: per-rank link bandwidth, MB/s (default 450000) */
     AR_OPT_AUTO_HANDOFF = 10,/* model: bytes per rank above which the ring is used (the size
                                 of a pre-registered buffer; default 8 MiB; 0 = no hand-off) */
+    AR_OPT_PUSH_STAGING = 11,/* 1: allocate the staging slots ar_one_shot_push needs
+                                (n x n x max_bytes); 0 (default): free them */
+    AR_OPT_REGISTERED = 12,  /* 1: allocate the registered buffers ar_one_shot_copyin needs
+                                (n x max_bytes); 0 (default): free them */
+    AR_OPT_PERSISTENT = 13,  /* 1: allocate the LL128 inboxes ar_ring_persistent needs
+                                (two slots per rank, about 4.3 x max_bytes in all);
+                                0 (default): free them */
+    AR_OPT_ABSENT_RANK = 14, /* failure emulation for ar_ring_persistent: rank r (0..n-1)
+                                never joins, so its neighbours' waits run out after
+                                AR_OPT_SPIN_NS and the status reads AR_ERR_FLAG_TIMEOUT or
+                                AR_ERR_WAIT_TIMEOUT; -1 (default): every rank takes part */
     AR_OPT_PDL = 6           /* 1 (default): launch with programmatic stream
                                 serialization, so a kernel is scheduled while the one
                                 before it in the stream drains (each kernel waits for
@@ -146,7 +163,12 @@ typedef enum {
     AR_K_LL128_PACK = 9,
     AR_K_LL128_UNPACK = 10,
     AR_K_LL128_REDUCE = 11,
-    AR_K_ALLREDUCE_RMSNORM = 12
+    AR_K_ALLREDUCE_RMSNORM = 12,
+    AR_K_PUSH = 13,                 /* one-shot push, phase 1 */
+    AR_K_PUSH_REDUCE = 14,          /* one-shot push, phase 2 */
+    AR_K_RING_RS_STEP_ROUNDED = 15, /* ar_ring_rounded's reduce-scatter step */
+    AR_K_TREE_LEVEL = 16,           /* one level of ar_tree */
+    AR_K_RING_PERSISTENT = 17       /* ar_ring_persistent (all steps) */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -210,6 +232,63 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
  * Chunk c is summed in the order c, c+1, ..., c+n-1. */
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
             ar_dtype dt, ar_stream_t stream);
+
+/* One-shot push (custom all-reduce notes, §实现, where it is named beside
+ * one-shot pull): every rank first writes its buffer into a staging slot of
+ * every peer, then every rank sums its own slots (its own input for its own
+ * term) in rank order.  Needs AR_OPT_PUSH_STAGING (AR_ERR_INVALID
+ * otherwise).  Same bits as ar_one_shot.  HBM: reads n S + n^2 S, writes
+ * n (n-1) S + n S.  Two launches. */
+int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                     ar_stream_t stream);
+
+/* One-shot with copy-in (custom all-reduce notes, §5 写回: outside graph
+ * capture the input is first copied with cudaMemcpyAsync into a
+ * pre-registered buffer that the kernel reads, so the output may be the
+ * input itself): n cudaMemcpyAsync copies into the handle's registered
+ * buffers, then the one-shot kernel reads those.  Needs AR_OPT_REGISTERED
+ * (AR_ERR_INVALID otherwise).  Same bits as ar_one_shot.  HBM: reads 2 n S,
+ * writes 2 n S. */
+int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                       ar_stream_t stream);
+
+/* The ring of ar_ring with its partials kept in the payload type and rounded
+ * at every hop, the way a library whose buffers hold the payload type does it
+ * (each step adds the chunk a rank receives to its own copy, "多 GPU 与
+ * NCCL", §ring all-reduce): chunk c gets
+ *   RN( ... RN( RN(x_c + x_{c+1}) + x_{c+2} ) ... + x_{c+n-1} ).
+ * Equal to ar_ring for fp32; for bf16 / fp16 it may differ from it by the
+ * hops' roundings.  HBM: reads 2 e N and writes e N per reduce-scatter step,
+ * reads and writes e N per all-gather step. */
+int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                    ar_stream_t stream);
+
+/* Pairwise tree all-reduce (recursive doubling; PCIe-IPC blog post,
+ * bhfrc.com/news/61376, §3.1 算法骨架): in each of log2(n) levels, rank r and
+ * rank r XOR 2^l read each other's data, add, and both keep the sum rounded
+ * to the payload type.  Layout and in-place rules as ar_one_shot; the
+ * handle's n_ranks must be a power of two (2, 4, 8 or 16), else
+ * AR_ERR_INVALID.  Every rank ends with the same bits; for bf16 / fp16 they
+ * may differ from one-shot's by the levels' roundings, for fp32 by the order
+ * of the adds.  log2(n) launches; HBM per level: n S read, n S written. */
+int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t stream);
+
+/* The ring of ar_ring in a single (cooperative) launch, each hop carried as
+ * LL128 lines: 120 bytes of fp32 words and an 8-byte step flag per 128 bytes
+ * (handbook "集合通信：NCCL 的算法、协议…", §协议; "多 GPU 与 NCCL", §ring
+ * all-reduce).  A rank's CTAs poll the flags of the lines the previous rank
+ * sends instead of waiting for a kernel boundary, and acknowledge each
+ * consumed step so that its two inbox slots can be reused.  Same bits as
+ * ar_ring.  Needs AR_OPT_PERSISTENT (AR_ERR_INVALID otherwise).  Every wait
+ * is bounded by AR_OPT_SPIN_NS: a wait that runs out ends the call early,
+ * leaves the outputs incomplete and sets the status (ar_status) to
+ * AR_ERR_FLAG_TIMEOUT or AR_ERR_WAIT_TIMEOUT.  All of its CTAs must be
+ * resident at once: run nothing else on the device at the same time that
+ * could hold SMs for longer than AR_OPT_SPIN_NS.  HBM: reads n e N +
+ * 2(n-1) 128 L and writes the same, L = the sum over the n chunks of
+ * ceil(chunk length / 30). */
+int ar_ring_persistent(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                       ar_stream_t stream);
 
 /* Ring all-reduce for callers that cannot allocate device memory (code that
  * runs where cudaMalloc is not allowed or not wanted: inside a framework that
@@ -366,8 +445,10 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
 
 /* Host only, no GPU needed: the code a call would return for these
  * arguments before launching anything.  op AR_OP_ONE_SHOT, AR_OP_TWO_SHOT,
- * AR_OP_RING, AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls
- * (n_ranks in [2, 16]); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
+ * AR_OP_RING, AR_OP_ONE_SHOT_PUSH, AR_OP_ONE_SHOT_COPYIN, AR_OP_RING_ROUNDED,
+ * AR_OP_TREE (n_ranks a power of two), AR_OP_RING_PERSISTENT,
+ * AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls (n_ranks in
+ * [2, 16]; the handle's optional buffers are not checked); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
  * AR_OP_LL128_UNPACK: the batched pack / unpack calls over n_ranks buffers
  * (in = sources, out = destinations; n_ranks in [1, 16]).  Pointers are
  * compared, never dereferenced.  For the LL ops dt must be AR_F32. */

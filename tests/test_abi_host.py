@@ -102,7 +102,9 @@ def test_plan_batched_pack_scales_with_buffers(lib, nb):
 
 
 def test_plan_rejects_bad_arguments(lib):
-    for op, n in [(0, 8), (11, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17), (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]:
+    bad = [(0, 8), (ar.AR_OP_RING_PERSISTENT + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
+           (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]
+    for op, n in bad:
         with pytest.raises(ar.ArError):
             ar.ar_plan(op, n, 10, "f32")
     with pytest.raises(ar.ArError):
@@ -266,3 +268,62 @@ def test_plan_fused_epilogue(lib, n):
     S = 64 * 8192 * 2
     assert (t.hbm_read_bytes, t.hbm_write_bytes) == ((n + 1) * S, (n + 1) * S)
     assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_one_shot(n, S)) and t.launches == 1
+
+
+@pytest.mark.parametrize("n", [2, 8, 16])
+def test_plan_push_and_copyin(lib, n):
+    N = 4099
+    S = N * 2
+    t = ar.ar_plan(ar.AR_OP_ONE_SHOT_PUSH, n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (n * S + n * n * S, n * (n - 1) * S + n * S)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_one_shot(n, S)) and t.launches == 2
+    t = ar.ar_plan(ar.AR_OP_ONE_SHOT_COPYIN, n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (2 * n * S, 2 * n * S)
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    for op in (ar.AR_OP_ONE_SHOT_PUSH, ar.AR_OP_ONE_SHOT_COPYIN):
+        assert _check(op, n, ins, outs, 1000) == ar.AR_OK
+        assert _check(op, n, ins, outs[:1] + [ins[0]] + outs[2:], 1000) == ar.AR_ERR_INVALID  # another rank's input
+
+
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("N", [1, 4099, 1 << 20])
+def test_plan_ring_rounded(lib, n, N):
+    t = ar.ar_plan(ar.AR_OP_RING_ROUNDED, n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == model.hbm_ring_rounded(n, N, 2)
+    assert t.steps == 2 * (n - 1) and t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16])
+@pytest.mark.parametrize("N", [0, 1, 4099, 1 << 20])
+def test_plan_tree(lib, n, N):
+    t = ar.ar_plan(ar.AR_OP_TREE, n, N, "f16")
+    levels = {2: 1, 4: 2, 8: 3, 16: 4}[n]
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == model.hbm_tree(n, N, 2)
+    assert t.steps == levels and t.launches == (levels if N else 0)
+    assert t.link_bytes_per_rank == pytest.approx(levels * 2 * N)
+
+
+@pytest.mark.parametrize("n", [3, 5, 6, 12, 15])
+def test_tree_refuses_other_rank_counts(lib, n):
+    with pytest.raises(ar.ArError):
+        ar.ar_plan(ar.AR_OP_TREE, n, 100, "bf16")
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    assert _check(ar.AR_OP_TREE, n, ins, outs, 1000) == ar.AR_ERR_INVALID
+    assert _check(ar.AR_OP_TREE, 8, _bufs(8), _bufs(8, off=64 << 20), 1000) == ar.AR_OK
+
+
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("N", [0, 1, 959, 4099, 1 << 20])
+def test_plan_ring_persistent(lib, n, N):
+    # per step the n chunks move once as LL128 lines of 30 words; the ranks'
+    # own elements are read in n steps and their outputs written in n steps
+    t = ar.ar_plan(ar.AR_OP_RING_PERSISTENT, n, N, "bf16")
+    C = -(-N // n)
+    C = -(-C // 8) * 8
+    lines = sum(-(-max(0, min(C, N - c * C)) // 30) for c in range(n))
+    want = n * 2 * N + (2 * n - 2) * 128 * lines
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (want, want)
+    assert t.steps == 2 * (n - 1) and t.launches == (1 if N else 0)
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    assert _check(ar.AR_OP_RING_PERSISTENT, n, ins, outs, 1000) == ar.AR_OK

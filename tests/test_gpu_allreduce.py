@@ -339,3 +339,71 @@ def test_launch_timing_records():
     plan_ring = ar.ar_plan(ar.AR_OP_RING, n, N, "bf16")
     assert recs[0][3] == 2 * n * N * 2
     assert recs[1][3] + recs[2][3] == plan_ring.hbm_read_bytes + plan_ring.hbm_write_bytes
+
+
+# --- the ring with per-hop rounding, and the pairwise tree -------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 9), (3, 1000), (8, 4099), (8, 300_001), (16, 65536 + 3)])
+def test_ring_rounded_matches_its_oracle(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=n * 3 + N)
+    want = oracle.ring_rounded(xs, dtype)
+    ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype])) as h:
+        assert ar.ar_ring_rounded(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+        assert ar.ar_traffic(h).op == ar.AR_OP_RING_ROUNDED
+    torch.cuda.synchronize()
+    for r in range(n):
+        np.testing.assert_array_equal(bits(outs[r].download(payload_np_dtype(dtype))), bits(want[r]))
+    for b in ins + outs:
+        assert b.guards_intact()
+    if dtype == "f32":
+        np.testing.assert_array_equal(bits(outs[0].download(np.float32)), bits(oracle.ring(xs, "f32")[0]))
+
+
+def test_ring_rounded_in_place_hand_worked():
+    # bf16, n = 3, 8 elements per chunk: rank 0 holds 256, ranks 1 and 2 hold 1
+    b = lambda v: oracle.f32_to_bf16(np.full(24, v, np.float32))
+    ins = upload_ranks([b(256.0), b(1.0), b(1.0)])
+    with Handle(3, 48) as h:
+        assert ar.ar_ring_rounded(h, ptrs(ins), ptrs(ins), 24, "bf16") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    want = np.array([256.0] * 8 + [258.0] * 8 + [256.0] * 8, np.float32)
+    for x in ins:
+        np.testing.assert_array_equal(oracle.bf16_to_f32(x.download(np.uint16)), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 9), (4, 1000), (8, 4099), (8, 300_001), (16, 65536 + 3), (16, 7)])
+def test_tree_matches_its_oracle(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=5 * n + N)
+    want = oracle.tree(xs, dtype)
+    ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype])) as h:
+        assert ar.ar_tree(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+        t = ar.ar_traffic(h)
+        assert t.op == ar.AR_OP_TREE and t.launches == n.bit_length() - 1
+    torch.cuda.synchronize()
+    for r in range(n):
+        np.testing.assert_array_equal(bits(outs[r].download(payload_np_dtype(dtype))), bits(want[r]))
+    for b in ins + outs:
+        assert b.guards_intact()
+
+
+def test_tree_in_place_hand_worked_and_refusals():
+    # bf16, n = 4: ranks hold 256, 1, 1, 0 -> 256 on every rank (one-shot gives 258)
+    b = lambda v: oracle.f32_to_bf16(np.full(40, v, np.float32))
+    ins = upload_ranks([b(256.0), b(1.0), b(1.0), b(0.0)])
+    with Handle(4, 80) as h:
+        assert ar.ar_tree(h, ptrs(ins), ptrs(ins), 40, "bf16") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for x in ins:
+        np.testing.assert_array_equal(oracle.bf16_to_f32(x.download(np.uint16)), np.full(40, 256.0, np.float32))
+    with Handle(3, 64) as h:
+        ins3, outs3 = empty_ranks(3, 64), empty_ranks(3, 64)
+        assert ar.ar_tree(h, ptrs(ins3), ptrs(outs3), 16, "bf16") == ar.AR_ERR_INVALID
+        assert ar.ar_tree(h, ptrs(ins3), ptrs(outs3), 0, "bf16") == ar.AR_ERR_INVALID

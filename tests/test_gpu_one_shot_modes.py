@@ -1,0 +1,87 @@
+"""ar_one_shot_push and ar_one_shot_copyin (custom all-reduce notes, §实现:
+one-shot push beside one-shot pull; §5 写回: copy-in to a registered buffer
+outside graph capture).  Both do one-shot's arithmetic (fp32 sum in rank
+order from +0, one rounding), so both are compared bit for bit with the
+oracle's all-reduce and with ar_one_shot; canary bands must stay intact."""
+
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_reduction_rank_gb300 as ar
+import oracle
+import workloads
+from gpu_util import Handle, bits, empty_ranks, payload_np_dtype, ptrs, upload_ranks
+
+pytestmark = pytest.mark.gpu
+
+E = {"f32": 4, "bf16": 2, "f16": 2}
+CALLS = {"push": (ar.ar_one_shot_push, "push_staging", ar.AR_OP_ONE_SHOT_PUSH, 2),
+         "copyin": (ar.ar_one_shot_copyin, "registered", ar.AR_OP_ONE_SHOT_COPYIN, 1)}
+
+
+@pytest.mark.parametrize("mode", ["push", "copyin"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 1), (2, 9), (3, 1000), (8, 4099), (8, 300_001), (16, 65536 + 3)])
+def test_mode_matches_one_shot_bit_for_bit(mode, dtype, n, N):
+    call, opt, op, launches = CALLS[mode]
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=17 * n + N)
+    want = oracle.all_reduce(xs, dtype)
+    ins, outs, ref = upload_ranks(xs), empty_ranks(n, xs[0].nbytes), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype]), **{opt: 1}) as h:
+        assert call(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+        t = ar.ar_traffic(h)
+        assert t.op == op and t.launches == launches
+        assert ar.ar_one_shot(h, ptrs(ins), ptrs(ref), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for r in range(n):
+        got = outs[r].download(payload_np_dtype(dtype))
+        np.testing.assert_array_equal(bits(got), bits(want[r]))
+        np.testing.assert_array_equal(bits(got), bits(ref[r].download(payload_np_dtype(dtype))))
+    for b in ins + outs + ref:
+        assert b.guards_intact()
+
+
+@pytest.mark.parametrize("mode", ["push", "copyin"])
+def test_mode_in_place(mode):
+    call, opt, _, _ = CALLS[mode]
+    n, N = 8, 100_003
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=4)
+    want = oracle.all_reduce(xs, "bf16")
+    ins = upload_ranks(xs)
+    with Handle(n, N * 2, **{opt: 1}) as h:
+        assert call(h, ptrs(ins), ptrs(ins), N, "bf16") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for r in range(n):
+        np.testing.assert_array_equal(ins[r].download(np.uint16), want[r])
+
+
+@pytest.mark.parametrize("mode", ["push", "copyin"])
+def test_mode_needs_its_buffers(mode):
+    call, opt, _, _ = CALLS[mode]
+    option = getattr(ar, "AR_OPT_" + opt.upper())
+    n, N = 4, 1000
+    ins, outs = empty_ranks(n, N * 4), empty_ranks(n, N * 4)
+    with Handle(n, N * 4) as h:
+        assert call(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_ERR_INVALID
+        assert ar.ar_set_option(h, option, 2) == ar.AR_ERR_INVALID
+        assert ar.ar_set_option(h, option, 1) == ar.AR_OK
+        assert call(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_OK
+        assert call(h, ptrs(ins), ptrs(outs), N + 1, "f32") == ar.AR_ERR_TOO_LARGE
+        assert ar.ar_set_option(h, option, 0) == ar.AR_OK
+        assert call(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_ERR_INVALID
+        assert ar.ar_status(h) == ar.AR_OK
+
+
+def test_push_timing_records_both_phases():
+    n, N = 8, 65536
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=8)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
+    with Handle(n, N * 2, push_staging=1, timing=8) as h:
+        assert ar.ar_one_shot_push(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK
+        recs = ar.ar_timing(h)
+    assert [r[0] for r in recs] == ["push", "push_reduce"]
+    t = ar.ar_plan(ar.AR_OP_ONE_SHOT_PUSH, n, N, "bf16")
+    assert recs[0][3] + recs[1][3] == t.hbm_read_bytes + t.hbm_write_bytes
