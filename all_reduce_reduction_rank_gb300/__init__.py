@@ -35,7 +35,8 @@ AR_AUTO_MODEL, AR_AUTO_EMULATED = 0, 1
 KERNELS = {1: "one_shot", 2: "reduce_scatter", 3: "all_gather", 4: "ring_rs_step", 5: "ring_ag_step",
            6: "ll_pack", 7: "ll_unpack", 8: "ll_reduce", 9: "ll128_pack", 10: "ll128_unpack",
            11: "ll128_reduce", 12: "allreduce_rmsnorm", 13: "push", 14: "push_reduce",
-           15: "ring_rs_step_rounded", 16: "tree_level", 17: "ring_persistent"}
+           15: "ring_rs_step_rounded", 16: "tree_level", 17: "ring_persistent",
+           18: "copyin"}
 
 # C symbols the header declares (checked by the CPU tests against include/ar.h)
 EXPORTS = (

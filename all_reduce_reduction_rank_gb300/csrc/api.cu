@@ -221,7 +221,7 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
     case AR_OP_ONE_SHOT_COPYIN:
         t->link_bytes_per_rank = (double)(nn - 1) * (double)S;
         t->steps = 1;
-        t->launches = count ? 1 : 0;
+        t->launches = count ? 2 : 0;
         t->hbm_read_bytes = 2 * nn * S;
         t->hbm_write_bytes = 2 * nn * S;
         break;

@@ -12,9 +12,11 @@
 // Copy-in (same notes, §5 写回: outside graph capture the kernel reads a
 // pre-registered pull buffer that cudaMemcpyAsync filled from the input, and
 // the output may then be the input itself): each rank's input is copied into
-// its registered buffer (AR_OPT_REGISTERED, n x max_bytes) with
-// cudaMemcpyAsync, as the pages do, and the one-shot kernel reads the
-// registered buffers.
+// its registered buffer (AR_OPT_REGISTERED, n x max_bytes), then the one-shot
+// kernel reads the registered buffers.  The pages issue one cudaMemcpyAsync
+// per rank; here one launch copies all n buffers (blockIdx.y = rank), which
+// costs one launch instead of n copies of a few microseconds each at decode
+// sizes.  HBM: the copy reads n S and writes n S.
 //
 // Both give the one-shot result bit for bit: fp32 sums in rank order from +0,
 // one rounding.
@@ -83,6 +85,26 @@ push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__
     }
 }
 
+// reg[r] <- in[r] for every rank r.  Grid: blockIdx.y = rank.
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads)
+copyin_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ reg, size_t slot_bytes, size_t nvec,
+              size_t count)
+{
+    pdl_acquire();
+    using T = typename Payload<DT>::scalar_t;
+    const int r = blockIdx.y;
+    const uint4* const src = static_cast<const uint4*>(in.p[r]);
+    uint4* const dst = reinterpret_cast<uint4*>(reg + (size_t)r * slot_bytes);
+    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads)
+        st16(dst + v, ld16(src + v));
+    pdl_release();
+    if (blockIdx.x == gridDim.x - 1) {
+        const size_t i = nvec * kVecElems<DT> + threadIdx.x;
+        if (i < count) reinterpret_cast<T*>(dst)[i] = static_cast<const T*>(in.p[r])[i];
+    }
+}
+
 }  // namespace
 
 int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
@@ -118,14 +140,28 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
 int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                            cudaStream_t s, int* launches)
 {
-    const size_t bytes = count * elem_bytes(dt);
+    const int rc = dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            CPtrs<NR> ip;
+            for (int q = 0; q < NR; ++q) ip.p[q] = in[q];
+            const size_t nvec = count / kVecElems<DT>;
+            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            rec_begin(h, s);
+            launch_kernel(h, copyin_kernel<NR, DT>, dim3(grid_for_rows(h, nvec, NR), NR), kThreads, 0, s, ip,
+                          h.registered, h.stage_slot, nvec, count);
+            rec_end(h, s, AR_K_COPYIN, 2ull * NR * S);
+            return launch_status();
+        });
+    });
+    if (rc != AR_OK) return rc;
     const void* reg[kMaxRanks];
-    for (int r = 0; r < h.n; ++r) {
-        reg[r] = h.registered + (size_t)r * h.stage_slot;
-        if (cudaMemcpyAsync(const_cast<void*>(reg[r]), in[r], bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-            return AR_ERR_CUDA;
-    }
-    return launch_one_shot(h, reg, out, count, dt, s, launches);
+    for (int r = 0; r < h.n; ++r) reg[r] = h.registered + (size_t)r * h.stage_slot;
+    int one = 0;
+    const int rc2 = launch_one_shot(h, reg, out, count, dt, s, &one);
+    *launches = 1 + one;
+    return rc2;
 }
 
 }  // namespace argb

@@ -31,19 +31,20 @@
 // Ordering follows the PTX memory model and does not assume that a 128-byte
 // line is stored atomically: a warp writes the data of 32 lines, then
 // __syncwarp, fence.acq_rel.gpu and one relaxed flag store per lane; a reader
-// polls one flag per lane (relaxed loads), then fence.acq_rel.gpu and
-// __syncwarp, and only then reads the data.
+// polls one flag per lane with acquire loads, then __syncwarp, and only then
+// reads the data.  A warp issues all loads of its 32 lines (and of the rank's
+// own elements) before it uses any, so a batch costs about one memory latency.
 //
 // Slot reuse: step t writes slot t % 2 of rank r+1, which step t-2 wrote
-// last.  The receiving CTA publishes ack = F(t') (release) once it has
-// consumed message t' of its slice; the sending CTA waits for
+// last.  Each receiving warp publishes ack = F(t') (release) once it has
+// consumed its batches of message t'; the sending warp waits for
 // ack >= F(t-2) before it writes.
 //
 // Every wait is bounded by spin_ns and a poll count.  A wait that runs out
 // records AR_ERR_FLAG_TIMEOUT (a line) or AR_ERR_WAIT_TIMEOUT (an ack) in the
 // status word and raises the call's abort word (= seq), on which every other
-// wait gives up at once; each CTA then leaves its step loop at a barrier that
-// all its threads reach.
+// wait gives up at once; a warp whose wait gave up returns (there is no
+// block-wide barrier to leave unmatched).
 #include "common.cuh"
 
 namespace argb {
@@ -62,9 +63,21 @@ __device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p)
     return v;
 }
 
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v)
 {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -105,30 +118,55 @@ __device__ __forceinline__ uint32_t ld4_plain(const void* p)
     return v;
 }
 
-// Elements e .. e+nw-1 (nw = 4 or 2) of a chunk of `len` elements, widened
-// to fp32; elements at or past len read as 0.  e is a multiple of 2, so a
-// pair of 16-bit elements is one aligned word and a pair of fp32 one aligned
-// 8-byte load.
+// Raw words of elements e .. e+nw-1 (zero past len): 4 fp32 words, or 2
+// words of two 16-bit elements each.  Loads only; widen_raw converts later,
+// so a warp can issue every load of a batch before it waits for any.
+template <int DT> constexpr int kRawWords = DT == AR_F32 ? 4 : 2;
+
 template <int DT>
-__device__ __forceinline__ void load_elems(const void* chunk, size_t e, int nw, size_t len, float* f)
+__device__ __forceinline__ void load_raw(const void* chunk, size_t e, int nw, size_t len, uint32_t* w)
 {
     using T = typename Payload<DT>::scalar_t;
     const T* x = static_cast<const T*>(chunk);
     if (e + (size_t)nw <= len) {
-#pragma unroll
-        for (int u = 0; u < 4; u += 2) {
-            if (u >= nw) break;
-            if constexpr (DT == AR_F32) {
-                const uint2 a = ld8_plain(x + e + u);
-                f[u] = __uint_as_float(a.x);
-                f[u + 1] = __uint_as_float(a.y);
-            } else {
-                Payload<DT>::widen(ld4_plain(x + e + u), f + u);
+        if constexpr (DT == AR_F32) {
+            const uint2 a = ld8_plain(x + e);
+            w[0] = a.x;
+            w[1] = a.y;
+            w[2] = w[3] = 0u;
+            if (nw == 4) {
+                const uint2 b = ld8_plain(x + e + 2);
+                w[2] = b.x;
+                w[3] = b.y;
             }
+        } else {
+            w[0] = ld4_plain(x + e);
+            w[1] = nw == 4 ? ld4_plain(x + e + 2) : 0u;
         }
     } else {
+        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(chunk);
+        const uint32_t* x32 = reinterpret_cast<const uint32_t*>(chunk);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) f[u] = u < nw && e + u < len ? Payload<DT>::widen1(x[e + u]) : 0.0f;
+        for (int u = 0; u < kRawWords<DT>; ++u) w[u] = 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (u < nw && e + u < len) {
+                if constexpr (DT == AR_F32) w[u] = x32[e + u];
+                else w[u >> 1] |= (uint32_t)x16[e + u] << (16 * (u & 1));
+            }
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_raw(const uint32_t* w, float* f)
+{
+    if constexpr (DT == AR_F32) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(w[u]);
+    } else {
+        Payload<DT>::widen(w[0], f);
+        Payload<DT>::widen(w[1], f + 2);
     }
 }
 
@@ -163,7 +201,7 @@ __device__ __forceinline__ uint64_t* flag_of(uint4* lines, size_t l)
 
 struct Persist {
     uint4* inbox;        // [n][2][lps] lines
-    uint64_t* acks;      // [n][kcap]
+    uint64_t* acks;      // [n][kcap][warps per CTA]
     uint64_t* abort_w;   // one word: == seq once a wait of this call gave up
     size_t lps;
     int kcap;
@@ -172,20 +210,22 @@ struct Persist {
 __device__ __forceinline__ bool aborted(const Persist& P, uint64_t seq) { return ld_relaxed(P.abort_w) == seq; }
 
 // Every lane of the warp: wait until the flag of its line (if `valid`) reads
-// `want`.  False (for the whole warp) if the wait ran out or the call was
-// aborted.
+// `want` (acquire).  False (for the whole warp) if the wait ran out or the
+// call was aborted.  The first polls spin; later ones sleep between reads.
 __device__ bool wait_lines(const Persist& P, uint64_t seq, const uint64_t* flag, bool valid, uint64_t want,
                            int64_t spin_ns, DevStatus* st, int rank, size_t line)
 {
-    bool ok = !valid || ld_relaxed(flag) == want;
+    bool ok = !valid || ld_acquire(flag) == want;
     if (__all_sync(kFull, ok)) return true;
-    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 32u + 64u;
+    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 32u + 1024u;
     for (uint64_t it = 0; it < cap; ++it) {
-        __nanosleep(32);
-        if (!ok) ok = ld_relaxed(flag) == want;
+        if (it >= 256) __nanosleep(64);
+        if (!ok) ok = ld_acquire(flag) == want;
         if (__all_sync(kFull, ok)) return true;
-        const bool stop = (int64_t)(globaltimer_ns() - t0) > spin_ns || aborted(P, seq);
-        if (__any_sync(kFull, stop)) break;
+        if ((it & 15) == 15) {
+            const bool stop = (int64_t)(globaltimer_ns() - t0) > spin_ns || aborted(P, seq);
+            if (__any_sync(kFull, stop)) break;
+        }
     }
     if (!ok && !aborted(P, seq)) {
         report_flag_timeout(st, rank, line);
@@ -194,39 +234,43 @@ __device__ bool wait_lines(const Persist& P, uint64_t seq, const uint64_t* flag,
     return false;
 }
 
-// One thread: wait until *ack >= want, then acquire.  False if the wait ran
-// out or the call was aborted.
+// Every lane of the warp: wait until *ack >= want (acquire).  False (for
+// the whole warp) if the wait ran out or the call was aborted.
 __device__ bool wait_ack(const Persist& P, uint64_t seq, const uint64_t* ack, uint64_t want, int64_t spin_ns,
                          DevStatus* st)
 {
-    if (ld_relaxed(ack) >= want) {
-        fence_gpu();   // the block's later stores follow it through the barrier
-        return true;
-    }
-    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 32u + 64u;
+    if (__all_sync(kFull, ld_acquire(ack) >= want)) return true;
+    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 32u + 1024u;
     for (uint64_t it = 0; it < cap; ++it) {
-        __nanosleep(32);
-        if (ld_relaxed(ack) >= want) {
-            fence_gpu();
-            return true;
+        if (it >= 256) __nanosleep(64);
+        if (__all_sync(kFull, ld_acquire(ack) >= want)) return true;
+        if ((it & 15) == 15) {
+            const bool stop = (int64_t)(globaltimer_ns() - t0) > spin_ns || aborted(P, seq);
+            if (__any_sync(kFull, stop)) break;
         }
-        if (aborted(P, seq)) return false;
-        if ((int64_t)(globaltimer_ns() - t0) > spin_ns) break;
     }
-    if (!aborted(P, seq)) {
+    if ((threadIdx.x & 31) == 0 && !aborted(P, seq)) {
         report_wait_timeout(st);
         st_relaxed(P.abort_w, seq);
     }
     return false;
 }
 
+// Work of one warp: batches b = warp, warp + 8, ... of its CTA's slice, the
+// same batches on every rank, so warp w of CTA k of rank r exchanges lines and
+// acknowledgements only with warp w of CTA k of ranks r-1 and r+1: the step
+// loop has no block-wide barrier.  Per batch, software-pipelined: load the
+// batch (lines + own elements), add and store (next rank's lines, outputs),
+// poll the next batch's flags (relaxed), then one fence that both releases
+// this batch's lines and acquires the next batch's, then the flags.
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads)
 ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                        const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, uint64_t seq,
-                       int64_t spin_ns, int absent, DevStatus* st)
+                       int64_t spin_ns, int absent, int prefetch, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
+    constexpr int kI = kBatchLines / 4;   // lines per lane group per batch
     const int r = blockIdx.y;
     const int k = blockIdx.x;
     if (r == absent) return;  // a rank that never joins (failure emulation)
@@ -236,62 +280,82 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
     const int nw = j < 7 ? 4 : 2;
     const size_t slice_lo = (size_t)k * epc;              // first element of the slice in a chunk
     const size_t line_lo = slice_lo / kLineWords;         // its first line
-    uint64_t* const my_ack = P.acks + (size_t)r * P.kcap + k;
-    const uint64_t* const next_ack = P.acks + (size_t)d * P.kcap + k;
+    uint64_t* const my_ack = P.acks + ((size_t)r * P.kcap + k) * kPWarps + warp;
+    const uint64_t* const next_ack = P.acks + ((size_t)d * P.kcap + k) * kPWarps + warp;
     auto inbox = [&](int q, int slot) { return P.inbox + ((size_t)q * 2 + slot) * P.lps * 8; };
-    auto chunk_len = [&](int c) -> size_t {
-        const size_t lo = (size_t)c * C;
-        return lo >= count ? 0 : (count - lo < C ? count - lo : C);
-    };
 
     // t in [0, 2n-2): send step t; t = 2n-2: only the last receive.
     for (int t = 0; t <= 2 * NR - 2; ++t) {
         const bool sends = t <= 2 * NR - 3;
-        bool fail = false;
-        if (sends && t >= 2 && threadIdx.x == 0)
-            fail = !wait_ack(P, seq, next_ack, 64 * seq + (uint64_t)(t - 2) + 1, spin_ns, st);
-        if (__syncthreads_or(fail)) break;
-
         // the chunk this step moves (received at t-1 and sent at t: the same)
         const int c = t <= NR - 2 ? ((r - t) % NR + NR) % NR : ((r + NR - t) % NR + NR) % NR;
-        const size_t len = chunk_len(c);
+        const size_t lo = (size_t)c * C;
+        const size_t len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
         const size_t slice_hi = slice_lo + epc < len ? slice_lo + epc : len;
         const size_t nlines = slice_hi > slice_lo ? (slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
         const size_t nbatch = (nlines + kBatchLines - 1) / kBatchLines;
-        const T* const x = static_cast<const T*>(in.p[r]) + (size_t)c * C;
-        T* const y = static_cast<T*>(out.p[r]) + (size_t)c * C;
+        const T* const x = static_cast<const T*>(in.p[r]) + lo;
+        T* const y = static_cast<T*>(out.p[r]) + lo;
         uint4* const rx = inbox(r, (t + 1) & 1);   // slot of message t-1
         uint4* const tx = inbox(d, t & 1);         // slot of message t
         const uint64_t f_in = 64 * seq + (uint64_t)t;        // F(t-1)
         const uint64_t f_out = 64 * seq + (uint64_t)t + 1;   // F(t)
+        auto flag_ptr = [&](size_t bb) { return flag_of(rx, line_lo + bb * kBatchLines + lane); };
+        auto flag_live = [&](size_t bb) { return (line_lo + bb * kBatchLines + lane) * kLineWords < slice_hi; };
 
-        for (size_t b = warp; b < nbatch; b += kPWarps) {
-            const size_t base = line_lo + b * kBatchLines;   // first line of the batch
-            if (t >= 1) {
-                const size_t fl = base + lane;
-                if (!wait_lines(P, seq, flag_of(rx, fl), fl * kLineWords < slice_hi, f_in, spin_ns, st, r, fl)) {
-                    fail = true;
-                    break;
-                }
-                fence_gpu();
-                __syncwarp();
+        // the rank's own elements of this step, pulled into L2 while the
+        // warp waits for the lines (small calls, whose steps are latency-bound)
+        if (prefetch && t >= 1 && t <= NR - 1) {
+            for (size_t bb = warp; bb < nbatch; bb += kPWarps) {
+                const size_t e0 = (line_lo + bb * kBatchLines) * kLineWords + (size_t)lane * (128 / sizeof(T));
+                if (e0 < slice_hi) prefetch_l2(x + e0);
             }
-#pragma unroll 2
-            for (int i = 0; i < kBatchLines / 4; ++i) {
+        }
+        // step prologue: the receiver's acknowledgement of step t-2 (slot
+        // reuse) and the first batch's flags, polled together, one acquire
+        size_t b = warp;
+        {
+            const bool need_ack = sends && t >= 2, need_fl = t >= 1 && b < nbatch;
+            const uint64_t want_ack = 64 * seq + (uint64_t)(t - 2) + 1;
+            bool ok_ack = !need_ack || ld_relaxed(next_ack) >= want_ack;
+            bool ok_fl = !need_fl || !flag_live(b) || ld_relaxed(flag_ptr(b)) == f_in;
+            if (!__all_sync(kFull, ok_ack && ok_fl)) {
+                if (!__all_sync(kFull, ok_ack) && !wait_ack(P, seq, next_ack, want_ack, spin_ns, st)) return;
+                if (need_fl && !wait_lines(P, seq, flag_ptr(b), flag_live(b), f_in, spin_ns, st, r,
+                                           line_lo + b * kBatchLines + lane))
+                    return;
+            }
+            fence_gpu();
+            __syncwarp();
+        }
+        while (b < nbatch) {
+            const size_t base = line_lo + b * kBatchLines;   // first line of the batch
+            // every load of the batch first: 8 lines and the rank's own elements
+            uint4 w[kI];
+            uint32_t xr[kI][kRawWords<DT>];
+#pragma unroll
+            for (int i = 0; i < kI; ++i) {
+                const size_t l = base + 4 * i + g;
+                w[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (t >= 1 && l * kLineWords < slice_hi) w[i] = ld16_cg(rx + 8 * l + j);
+            }
+            if (t <= NR - 1) {
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    load_raw<DT>(x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < slice_hi ? len : 0, xr[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
                 const size_t e = l * kLineWords + 4 * (size_t)j;
                 if (l * kLineWords >= slice_hi) continue;
-                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                if (t >= 1) {
-                    const uint4 w = ld16_cg(rx + 8 * l + j);
-                    v[0] = __uint_as_float(w.x);
-                    v[1] = __uint_as_float(w.y);
-                    v[2] = __uint_as_float(w.z);
-                    v[3] = __uint_as_float(w.w);
-                }
+                float v[4] = {__uint_as_float(w[i].x), __uint_as_float(w[i].y), __uint_as_float(w[i].z),
+                              __uint_as_float(w[i].w)};
                 if (t <= NR - 1) {   // reduce-scatter: add this rank's own chunk
                     float xv[4];
-                    load_elems<DT>(x, e, nw, len, xv);
+                    widen_raw<DT>(xr[i], xv);
                     if (t == 0) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) v[u] = xv[u];
@@ -315,23 +379,39 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
                         st8_plain(tx + 8 * l + j, __float_as_uint(v[0]), __float_as_uint(v[1]));
                 }
             }
+            // the next batch's flags, polled before the fence so that one
+            // fence releases this batch and acquires the next
+            const size_t nb = b + kPWarps;
+            const bool need_fl = t >= 1 && nb < nbatch;
+            const bool nready = __all_sync(kFull, !need_fl || !flag_live(nb) || ld_relaxed(flag_ptr(nb)) == f_in);
+            __syncwarp();
+            fence_gpu();
             if (sends) {
-                __syncwarp();
-                fence_gpu();
                 const size_t fl = base + lane;
                 if (fl * kLineWords < slice_hi) st_relaxed(flag_of(tx, fl), f_out);
             }
+            if (need_fl && !nready) {
+                if (!wait_lines(P, seq, flag_ptr(nb), flag_live(nb), f_in, spin_ns, st, r,
+                                line_lo + nb * kBatchLines + lane))
+                    return;
+            }
+            __syncwarp();
+            b = nb;
         }
-        if (threadIdx.x == 0 && !fail) fail = aborted(P, seq);
-        if (__syncthreads_or(fail)) break;
-        if (t >= 1 && sends && threadIdx.x == 0) {   // message t-1 of this slice consumed
-            fence_gpu();
+        // message t-1 of this warp's batches is consumed (the last fence
+        // followed its loads): acknowledge it for the sender's slot reuse
+        if (t >= 1 && sends && lane == 0) {
+            if (nbatch <= (size_t)warp) fence_gpu();
             st_relaxed(my_ack, f_in);
         }
     }
 }
 
 }  // namespace
+
+// Calls up to this many bytes per rank prefetch each step's own elements
+// into L2 (the step's elements of all ranks then take at most this much L2).
+constexpr uint64_t kPersistPrefetchBytes = 32ull << 20;
 
 // CTAs per SM the inboxes are sized for; launches never use more.
 constexpr int kPersistCtasPerSm = 8;
@@ -349,7 +429,7 @@ static size_t persist_lps(int n, size_t max_bytes, int sm_count)
 size_t persist_bytes(int n, size_t max_bytes, int sm_count)
 {
     return (size_t)n * 2 * persist_lps(n, max_bytes, sm_count) * 128 +
-           (size_t)n * (size_t)persist_kcap(n, sm_count) * sizeof(uint64_t) + 256;
+           (size_t)n * (size_t)persist_kcap(n, sm_count) * kPWarps * sizeof(uint64_t) + 256;
 }
 
 // Lines moved per step over all ranks: the sum over chunks of ceil(len / 30).
@@ -401,7 +481,7 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             P.lps = lps;
             P.kcap = persist_kcap(h.n, h.sm_count);
             P.acks = reinterpret_cast<uint64_t*>(h.persist + (size_t)h.n * 2 * lps * 128);
-            P.abort_w = P.acks + (size_t)h.n * P.kcap;
+            P.abort_w = P.acks + (size_t)h.n * P.kcap * kPWarps;
             const uint64_t seq = ++h.persist_seq;
 
             cudaLaunchAttribute attr[1];
@@ -419,7 +499,8 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             const uint64_t bytes = 2ull * ((uint64_t)NR * e * count + (uint64_t)(2 * NR - 2) * 128ull * L);
             rec_begin(h, s);
             const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_persistent_kernel<NR, DT>, ip, op, P, C, count,
-                                                       epc, seq, h.spin_ns, h.persist_absent, h.status);
+                                                       epc, seq, h.spin_ns, h.persist_absent,
+                                                       (int)(count * e <= kPersistPrefetchBytes), h.status);
             rec_end(h, s, AR_K_RING_PERSISTENT, bytes);
             *launches = 1;
             if (err != cudaSuccess) {

@@ -114,6 +114,9 @@ KERNEL_SOURCES = {
     "ring_rs_step": ["ring.cu"], "ring_ag_step": ["ring.cu"],
     "ll_pack": ["ll.cu"], "ll_unpack": ["ll.cu"], "ll_reduce": ["ll.cu"],
     "ll128_pack": ["ll.cu"], "ll128_unpack": ["ll.cu"], "ll128_reduce": ["ll.cu"],
+    "allreduce_rmsnorm": ["rmsnorm.cu"], "push": ["one_shot_modes.cu"], "push_reduce": ["one_shot_modes.cu"],
+    "copyin": ["one_shot_modes.cu"], "ring_rs_step_rounded": ["ring.cu"], "tree_level": ["tree.cu"],
+    "ring_persistent": ["ring_persistent.cu"],
 }
 
 

@@ -168,7 +168,8 @@ typedef enum {
     AR_K_PUSH_REDUCE = 14,          /* one-shot push, phase 2 */
     AR_K_RING_RS_STEP_ROUNDED = 15, /* ar_ring_rounded's reduce-scatter step */
     AR_K_TREE_LEVEL = 16,           /* one level of ar_tree */
-    AR_K_RING_PERSISTENT = 17       /* ar_ring_persistent (all steps) */
+    AR_K_RING_PERSISTENT = 17,      /* ar_ring_persistent (all steps) */
+    AR_K_COPYIN = 18                /* ar_one_shot_copyin's copy into the registered buffers */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -245,10 +246,10 @@ int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_
 /* One-shot with copy-in (custom all-reduce notes, §5 写回: outside graph
  * capture the input is first copied with cudaMemcpyAsync into a
  * pre-registered buffer that the kernel reads, so the output may be the
- * input itself): n cudaMemcpyAsync copies into the handle's registered
- * buffers, then the one-shot kernel reads those.  Needs AR_OPT_REGISTERED
- * (AR_ERR_INVALID otherwise).  Same bits as ar_one_shot.  HBM: reads 2 n S,
- * writes 2 n S. */
+ * input itself): one copy kernel fills the handle's n registered buffers
+ * (the pages use one cudaMemcpyAsync per rank), then the one-shot kernel
+ * reads those.  Needs AR_OPT_REGISTERED (AR_ERR_INVALID otherwise).  Same
+ * bits as ar_one_shot.  Two launches.  HBM: reads 2 n S, writes 2 n S. */
 int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
 

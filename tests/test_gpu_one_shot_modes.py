@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 E = {"f32": 4, "bf16": 2, "f16": 2}
 CALLS = {"push": (ar.ar_one_shot_push, "push_staging", ar.AR_OP_ONE_SHOT_PUSH, 2),
-         "copyin": (ar.ar_one_shot_copyin, "registered", ar.AR_OP_ONE_SHOT_COPYIN, 1)}
+         "copyin": (ar.ar_one_shot_copyin, "registered", ar.AR_OP_ONE_SHOT_COPYIN, 2)}
 
 
 @pytest.mark.parametrize("mode", ["push", "copyin"])
@@ -84,4 +84,16 @@ def test_push_timing_records_both_phases():
         recs = ar.ar_timing(h)
     assert [r[0] for r in recs] == ["push", "push_reduce"]
     t = ar.ar_plan(ar.AR_OP_ONE_SHOT_PUSH, n, N, "bf16")
+    assert recs[0][3] + recs[1][3] == t.hbm_read_bytes + t.hbm_write_bytes
+
+
+def test_copyin_timing_records_copy_and_one_shot():
+    n, N = 8, 65536
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", seed=9)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
+    with Handle(n, N * 2, registered=1, timing=8) as h:
+        assert ar.ar_one_shot_copyin(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK
+        recs = ar.ar_timing(h)
+    assert [r[0] for r in recs] == ["copyin", "one_shot"]
+    t = ar.ar_plan(ar.AR_OP_ONE_SHOT_COPYIN, n, N, "bf16")
     assert recs[0][3] + recs[1][3] == t.hbm_read_bytes + t.hbm_write_bytes
