@@ -481,40 +481,58 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
 def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     """The same step through the public API with HOST buffers: every step
     copies its inputs from pinned host memory, runs, and reads its results
-    (the n all-reduced buffers and the n LL and LL128 unpacked payloads) back."""
+    (the n all-reduced buffers and the n LL and LL128 unpacked payloads) back.
+
+    Steps alternate between two device buffer sets, each with its own stream
+    (copy in -> the step's calls -> copy out, in order on that stream), so
+    one step's copies overlap the other set's calls and copies in the other
+    direction; every step still moves all of its own bytes in and out."""
     import torch
     n = wl.n
+    wl2 = Workload(n, wl.S, wl.ll_count, wl.dev, seed=1004)
+    sets = (wl, wl2)
     h_in = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.ins]
     h_pay = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.pay]
     for h, d in zip(h_in + h_pay, wl.ins + wl.pay):
         h.copy_(d)
-    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.outs]
-    h_ll = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.ll_dst + wl.l128_dst]
+    h_outs = [[torch.empty_like(t, device="cpu").pin_memory() for t in w.outs + w.ll_dst + w.l128_dst]
+              for w in sets]
     h2d = sum(t.numel() * t.element_size() for t in h_in + h_pay)
-    d2h = sum(t.numel() * t.element_size() for t in h_out + h_ll)
+    d2h = sum(t.numel() * t.element_size() for t in h_outs[0])
 
-    def one():
-        with torch.cuda.stream(wl.stream):
-            for h, d in zip(h_in + h_pay, wl.ins + wl.pay):
+    def one(i):
+        w, hout = sets[i % 2], h_outs[i % 2]
+        with torch.cuda.stream(w.stream):
+            for h, d in zip(h_in + h_pay, w.ins + w.pay):
                 d.copy_(h, non_blocking=True)
-            wl.run()
-            for h, d in zip(h_out + h_ll, wl.outs + wl.ll_dst + wl.l128_dst):
+            w.run()
+            for h, d in zip(hout, w.outs + w.ll_dst + w.l128_dst):
                 h.copy_(d, non_blocking=True)
 
-    one()
+    one(0)
+    one(1)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     ev0.record(wl.stream)
-    for _ in range(K):
-        one()
+    wl2.stream.wait_event(ev0)
+    for i in range(K):
+        one(i)
+    done2 = torch.cuda.Event()
+    done2.record(wl2.stream)
+    wl.stream.wait_event(done2)
     ev1.record(wl.stream)
     torch.cuda.synchronize()
+    import all_reduce_reduction_rank_gb300 as ar
+    for w in sets:
+        ar.check(ar.ar_status(w.h), "e2e status")
+    wl2.close()
     ms = reduce_scalar(ev0.elapsed_time(ev1), "max") / K
     world = dist_env()[1]
     return {"value": round(world * bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelining": "2 buffer sets on 2 streams: copy in, calls, copy out per step"}
 
 
 def run_ours(args):
