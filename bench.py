@@ -414,6 +414,120 @@ def fused_epilogue(wl, peak: float, batches: int = 7, calls: int = 200) -> list:
     return out
 
 
+def _batched_us(stream, fn, calls: int, batches: int) -> float:
+    """Median over batches of the device time per call of `calls` back-to-back
+    calls fn(i), one CUDA event pair per batch, µs."""
+    import torch
+    per = []
+    for _ in range(batches):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(calls):
+            fn(i)
+        e1.record(stream)
+        e1.synchronize()
+        per.append(e0.elapsed_time(e1) / calls)
+    return statistics.median(per) * 1e3
+
+
+def ll_sweep(wl, peak: float, batches: int = 5) -> dict:
+    """The LL / LL128 workload over its payload sizes (n = 8 fp32 payloads of
+    8 B .. 1 MiB per rank, doubling): one pass = batched pack of the n
+    payloads, the flag-checked reduce, batched unpack, with a fresh step id
+    per pass.  Reported per size: µs per pass, payload GB/s (n P / t), the
+    lines' wire efficiency and the algorithmic HBM GB/s of the three calls."""
+    import all_reduce_reduction_rank_gb300 as ar
+    import workloads
+
+    n, L, h, s = wl.n, wl.L, wl.h, wl.s
+    out = {"ll": [], "ll128": []}
+    step = [1 << 20]
+    for count in workloads.CONFIGS[4]["counts"]:
+        P = 4 * count
+        for kind in ("ll", "ll128"):
+            if kind == "ll":
+                calls = (L.ar_ll_pack_n, L.ar_ll_reduce, L.ar_ll_unpack_n)
+                lines, red, dst = wl.p_ll, wl.p_llr, wl.p_lld
+                ops = (ar.AR_OP_LL_PACK, ar.AR_OP_LL_REDUCE, ar.AR_OP_LL_UNPACK)
+                wire = P / ar.ar_ll_bytes(P)
+            else:
+                calls = (L.ar_ll128_pack_n, L.ar_ll128_reduce, L.ar_ll128_unpack_n)
+                lines, red, dst = wl.p_l128, wl.p_l128r, wl.p_l128d
+                ops = (ar.AR_OP_LL128_PACK, ar.AR_OP_LL128_REDUCE, ar.AR_OP_LL128_UNPACK)
+                wire = P / ar.ar_ll128_bytes(P)
+
+            def one(_i, calls=calls, lines=lines, red=red, dst=dst):
+                step[0] += 1
+                k = step[0]
+                calls[0](h, wl.p_pay, lines, count, k, s)
+                calls[1](h, lines, red, count, k, s)
+                calls[2](h, red, dst, count, k, s)
+
+            b = 0
+            for op in ops:
+                t = ar.ar_plan(op, n, count, "f32")
+                b += t.hbm_read_bytes + t.hbm_write_bytes
+            one(0)
+            us = _batched_us(wl.stream, one, 200 if P <= 64 * 1024 else 50, batches)
+            ar.check(ar.ar_status(h), kind + " sweep")
+            out[kind].append({"payload_bytes": P, "us_per_pass": round(us, 3),
+                              "payload_GB/s": round(n * P / (us * 1e-6) / 1e9, 2),
+                              "wire_efficiency": round(wire, 4), "hbm_GB/s": round(b / (us * 1e-6) / 1e9, 1),
+                              "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4)})
+    return out
+
+
+def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
+    """The n = 16 doubling sweep (bf16 and fp16, 1 KiB .. 256 MiB per rank):
+    ring, one-shot and two-shot.  Inputs are 16 device buffers of 256 MiB;
+    smaller messages rotate over slots of them so that back-to-back calls do
+    not find their data in L2.  µs per call and algorithmic HBM GB/s."""
+    import ctypes
+
+    import torch
+
+    import all_reduce_reduction_rank_gb300 as ar
+    import workloads
+
+    n = 16
+    top = 256 * MiB
+    ins = workloads.rank_inputs_device(n, top // 2, "bf16", "normal_over_n", workloads.seed_of(5), device=dev)
+    outs = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, top)
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    L = ar.lib()
+    res = {}
+    try:
+        for dtype in ("bf16", "f16"):
+            dt = ar.DTYPES[dtype]
+            for name, call, op in (("ring", L.ar_ring, ar.AR_OP_RING), ("one_shot", L.ar_one_shot, ar.AR_OP_ONE_SHOT),
+                                   ("two_shot", L.ar_two_shot, ar.AR_OP_TWO_SHOT)):
+                rows = []
+                for count in workloads.CONFIGS[5]["counts"]:
+                    S = 2 * count
+                    slots = top // S
+                    P = lambda ts, k: (ctypes.c_void_p * n)(*[t.data_ptr() + k * S for t in ts])
+                    nslot = min(slots, 256)
+                    pin = [P(ins, k * (slots // nslot)) for k in range(nslot)]
+                    pout = [P(outs, k * (slots // nslot)) for k in range(nslot)]
+                    calls = max(8, min(nslot, 256))
+
+                    def one(i, call=call, pin=pin, pout=pout, count=count):
+                        call(h, pin[i % nslot], pout[i % nslot], count, dt, sp)
+
+                    ar.check(call(h, pin[0], pout[0], count, dt, sp), name)
+                    us = _batched_us(stream, one, calls, batches)
+                    t = ar.ar_plan(op, n, count, dtype)
+                    gbs = (t.hbm_read_bytes + t.hbm_write_bytes) / (us * 1e-6) / 1e9
+                    rows.append([S, round(us, 2), round(gbs, 1)])
+                ar.check(ar.ar_status(h), name)
+                res[f"{dtype}/{name}"] = rows
+    finally:
+        ar.ar_destroy(h)
+    return {"columns": ["bytes_per_rank", "us", "hbm_GB/s"], "peak": peak, **res}
+
+
 VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
 
 
@@ -594,10 +708,13 @@ def run_ours(args):
     sw = sweep(wl, peak) if args.sweep else None
     fe = fused_epilogue(wl, peak) if args.sweep else None
     va = variants(wl, peak) if args.sweep else None
+    lls = ll_sweep(wl, peak) if args.sweep else None
     e2e = e2e_leg(wl, max(3, min(args.steps, args.e2e_steps)), bytes_step) if args.e2e else None
-    cpu = None
+    n16 = n16_sweep(dev, peak) if args.sweep else None
+    cpu = cpu_par = None
     if world == 1 and rank == 0 and args.cpu_baseline:
         cpu = cpu_baseline(seconds=args.cpu_seconds)
+        cpu_par = cpu_parallel(seconds=args.cpu_seconds)
     wl.close()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -615,8 +732,8 @@ def run_ours(args):
         "launch_timing": {"steps_sampled": sampled, "every": every, "records": len(records),
                           "launches_recorded": sum(r[4] for r in records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),
-        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "sweep": sw,
-        "fused_epilogue": fe, "variants": va,
+        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "cpu_parallel": cpu_par, "sweep": sw,
+        "fused_epilogue": fe, "variants": va, "ll_sweep": lls, "n16_sweep": n16,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -664,6 +781,68 @@ def cpu_baseline(seconds: float = 10.0, scale_div: int = 32) -> dict:
     dt = time.perf_counter() - t0
     return {"value": round(reps * b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{desc}, {reps} passes in {dt:.1f} s, single-threaded C"}
+
+
+def cpu_parallel(seconds: float = 10.0, scale_div: int = 32) -> dict:
+    """The same oracle sample split by element range over every host core
+    (threads; the oracle's C routines run without the GIL): each thread does
+    one-shot, two-shot (the reduce-scatter sums then the all-gather copies),
+    the ring (its per-element order statement, which the literal step
+    simulation is pinned to) and the LL / LL128 pack -> reduce -> unpack of
+    its range.  A second CPU figure beside the single-threaded oracle."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    import workloads
+    n = 8
+    N = (64 * MiB // 2) // scale_div
+    c = ((1 * MiB) // 4) // scale_div
+    xs = workloads.rank_inputs(n, N, "bf16", "normal", 1003)
+    ps = workloads.payload_f32(n, c, 1004)
+    C = oracle.chunk_elems(n, N, "bf16")
+    chunk = (np.arange(N) // C).astype(np.int32)
+    b = sum(step_bytes(n, N, 2, c).values())
+    cores = os.cpu_count() or 1
+    # element ranges: multiples of 30 words keep LL128 lines whole
+    def ranges(total, align):
+        per = -(-total // cores)
+        per = -(-per // align) * align
+        return [(lo, min(total, lo + per)) for lo in range(0, total, per)]
+    xr, pr = ranges(N, 8), ranges(c, 30)
+
+    def work(t, step_id):
+        if t < len(xr):
+            lo, hi = xr[t]
+            cols = [x[lo:hi] for x in xs]
+            oracle.all_reduce(cols, "bf16")
+            oracle.all_reduce(cols, "bf16")            # two-shot: the same sums, then copies
+            oracle.ring_order_sum(cols, chunk[lo:hi], "bf16")
+        if t < len(pr):
+            lo, hi = pr[t]
+            sub = [p[lo:hi] for p in ps]
+            red, _ = oracle.ll_reduce([oracle.ll_pack(p, step_id) for p in sub], hi - lo, step_id)
+            for r in red:
+                oracle.ll_unpack(r, hi - lo, step_id)
+            red, _ = oracle.ll128_reduce([oracle.ll128_pack(p, step_id) for p in sub], hi - lo, step_id)
+            for r in red:
+                oracle.ll128_unpack(r, hi - lo, step_id)
+
+    threads = max(len(xr), len(pr))
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        list(pool.map(lambda t: work(t, 1), range(threads)))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            list(pool.map(lambda t: work(t, 2 + reps), range(threads)))
+            reps += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+    return {"value": round(reps * b / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle routines, element-range parallel",
+            "sample": f"the cpu_baseline sample (1/{scale_div} of the step) over {threads} threads, "
+                      f"{reps} passes in {dt:.1f} s"}
 
 
 def run_reference(args):
