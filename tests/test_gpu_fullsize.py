@@ -111,3 +111,38 @@ def test_ll_largest_payload_in_the_bench_configuration():
                     np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), want.view(np.uint32))
     finally:
         assert ar.ar_destroy(h) == ar.AR_OK
+
+
+def test_other_calls_at_the_prefill_size():
+    # n = 8 bf16, 64 MiB per rank, in the configuration the bench's variants
+    # leg times: push and copy-in == one-shot and the persistent ring == the
+    # step ring, all bit for bit over whole buffers; the hop-rounded ring and
+    # the tree against the oracle over whole buffers
+    n, dtype, S = 8, "bf16", 64 * MiB
+    N = S // 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(3) + 77)
+    outs = {k: [torch.empty_like(t) for t in ins] for k in
+            ("one_shot", "push", "copyin", "ring", "persistent", "rounded", "tree")}
+    h = ar.ar_create(n, S)
+    try:
+        for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
+            assert ar.ar_set_option(h, opt, 1) == ar.AR_OK
+        for key, call in (("one_shot", ar.ar_one_shot), ("push", ar.ar_one_shot_push),
+                          ("copyin", ar.ar_one_shot_copyin), ("ring", ar.ar_ring),
+                          ("persistent", ar.ar_ring_persistent), ("rounded", ar.ar_ring_rounded),
+                          ("tree", ar.ar_tree)):
+            _run(call, h, ins, outs[key], N, dtype)
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+    for r in range(n):
+        assert torch.equal(outs["push"][r], outs["one_shot"][r])
+        assert torch.equal(outs["copyin"][r], outs["one_shot"][r])
+        assert torch.equal(outs["persistent"][r], outs["ring"][r])
+    host = [t.cpu().numpy().view(np.uint16) for t in ins]
+    want_rounded = oracle.ring_rounded(host, dtype)
+    want_tree = oracle.tree(host, dtype)
+    for r in (0, 3, 7):
+        np.testing.assert_array_equal(outs["rounded"][r].cpu().numpy().view(np.uint16), want_rounded[r])
+        np.testing.assert_array_equal(outs["tree"][r].cpu().numpy().view(np.uint16), want_tree[r])
