@@ -264,7 +264,7 @@ __device__ bool wait_ack(const Persist& P, uint64_t seq, const uint64_t* ack, ui
 // poll the next batch's flags (relaxed), then one fence that both releases
 // this batch's lines and acquires the next batch's, then the flags.
 template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM: 128 registers, no spills
 ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                        const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, uint64_t seq,
                        int64_t spin_ns, int absent, int prefetch, DevStatus* st)
@@ -328,11 +328,12 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
             fence_gpu();
             __syncwarp();
         }
-        while (b < nbatch) {
-            const size_t base = line_lo + b * kBatchLines;   // first line of the batch
-            // every load of the batch first: 8 lines and the rank's own elements
-            uint4 w[kI];
-            uint32_t xr[kI][kRawWords<DT>];
+        // a batch's loads: 8 lines and the rank's own elements, all issued
+        // before any is used
+        uint4 w[kI];
+        uint32_t xr[kI][kRawWords<DT>];
+        auto load_batch = [&](size_t bb) {
+            const size_t base = line_lo + bb * kBatchLines;
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
@@ -346,6 +347,10 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
                     load_raw<DT>(x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < slice_hi ? len : 0, xr[i]);
                 }
             }
+        };
+        if (b < nbatch) load_batch(b);
+        while (b < nbatch) {
+            const size_t base = line_lo + b * kBatchLines;   // first line of the batch
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
@@ -379,27 +384,29 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
                         st8_plain(tx + 8 * l + j, __float_as_uint(v[0]), __float_as_uint(v[1]));
                 }
             }
-            // the next batch's flags, polled before the fence so that one
-            // fence releases this batch and acquires the next
+            // the next batch: acquire its flags and issue its loads before
+            // this batch's release, so that they are in flight while this
+            // batch's stores drain
             const size_t nb = b + kPWarps;
-            const bool need_fl = t >= 1 && nb < nbatch;
-            const bool nready = __all_sync(kFull, !need_fl || !flag_live(nb) || ld_relaxed(flag_ptr(nb)) == f_in);
-            __syncwarp();
-            fence_gpu();
+            if (t >= 1 && nb < nbatch) {
+                const bool ok = __all_sync(kFull, !flag_live(nb) || ld_acquire(flag_ptr(nb)) == f_in);
+                if (!ok && !wait_lines(P, seq, flag_ptr(nb), flag_live(nb), f_in, spin_ns, st, r,
+                                       line_lo + nb * kBatchLines + lane))
+                    return;
+                __syncwarp();
+            }
+            if (nb < nbatch) load_batch(nb);
             if (sends) {
+                __syncwarp();
+                fence_gpu();
                 const size_t fl = base + lane;
                 if (fl * kLineWords < slice_hi) st_relaxed(flag_of(tx, fl), f_out);
             }
-            if (need_fl && !nready) {
-                if (!wait_lines(P, seq, flag_ptr(nb), flag_live(nb), f_in, spin_ns, st, r,
-                                line_lo + nb * kBatchLines + lane))
-                    return;
-            }
-            __syncwarp();
             b = nb;
         }
-        // message t-1 of this warp's batches is consumed (the last fence
-        // followed its loads): acknowledge it for the sender's slot reuse
+        // message t-1 of this warp's batches is consumed (its last batch's
+        // values were used before the last fence): acknowledge it for the
+        // sender's slot reuse
         if (t >= 1 && sends && lane == 0) {
             if (nbatch <= (size_t)warp) fence_gpu();
             st_relaxed(my_ack, f_in);
