@@ -10,7 +10,9 @@
  *   (reduce_impl)").  One-shot, two-shot and the LL/LL128 reduce add the
  *   ranks in rank order 0..n-1 starting from +0, so their outputs are
  *   bit-identical to each other and on every rank (same notes, §4, last
- *   paragraph).  The ring adds chunk c in the order c, c+1, ..., c+n-1.
+ *   paragraph).  The ring adds chunk c in the order c, c+1, ..., c+n-1
+ *   (fp32 partials; ar_ring_rounded rounds them at every hop); ar_tree adds
+ *   pairwise, level by level, rounding at every level.
  *
  * Conventions shared by every call:
  *   - Pointers named in/out/src/dst/lines are DEVICE pointers owned by the
@@ -30,7 +32,10 @@
  *     exercise 3).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream), never allocate and never synchronize, so they can be
- *     issued inside CUDA graph capture.  Host-side argument errors are
+ *     issued inside CUDA graph capture (tested for ar_one_shot, ar_two_shot
+ *     and ar_ring; the optional buffers of AR_OPT_PUSH_STAGING,
+ *     AR_OPT_REGISTERED and AR_OPT_PERSISTENT are allocated when the option
+ *     is set, never in a call).  Host-side argument errors are
  *     returned at once and nothing is launched.  Errors found by a kernel
  *     are sticky in the handle and are returned by ar_status().
  *   - A handle may be used from one host thread at a time.
