@@ -47,7 +47,6 @@ struct Handle {
     uint8_t* registered = nullptr;  // [n][stage_slot] (AR_OPT_REGISTERED)
     size_t stage_slot = 0;          // max_bytes rounded up to 256
     uint8_t* persist = nullptr;     // ar_ring_persistent's inboxes, acks, abort word (AR_OPT_PERSISTENT)
-    uint64_t persist_seq = 0;       // calls of ar_ring_persistent so far
     int persist_absent = -1;        // AR_OPT_ABSENT_RANK
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements

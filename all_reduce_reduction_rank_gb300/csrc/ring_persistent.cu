@@ -25,8 +25,10 @@
 //
 // Inbox of rank q: two slots (step parity) of `lps` lines.  Line l of a slot
 // holds elements 30 l .. 30 l + 29 of the chunk as fp32 words, and the flag
-// F(t) = 64 seq + t + 1 of the step t that wrote it (seq is new for every
-// call, so no line of an earlier call matches).
+// F(t) = 64 seq + t + 1 of the step t that wrote it.  seq is a call number
+// kept in device memory: every warp reads it at the start, and the call's
+// last warp to finish advances it, so each call -- also each replay of a
+// captured CUDA graph -- has its own, and no line of an earlier call matches.
 //
 // Ordering follows the PTX memory model and does not assume that a 128-byte
 // line is stored atomically: a warp writes the data of 32 lines, then
@@ -203,6 +205,8 @@ struct Persist {
     uint4* inbox;        // [n][2][lps] lines
     uint64_t* acks;      // [n][kcap][warps per CTA]
     uint64_t* abort_w;   // one word: == seq once a wait of this call gave up
+    uint64_t* epoch_w;   // the last finished call's seq
+    unsigned* done_w;    // warps of the current call that have finished
     size_t lps;
     int kcap;
 };
@@ -259,15 +263,14 @@ __device__ bool wait_ack(const Persist& P, uint64_t seq, const uint64_t* ack, ui
 // Work of one warp: batches b = warp, warp + 8, ... of its CTA's slice, the
 // same batches on every rank, so warp w of CTA k of rank r exchanges lines and
 // acknowledgements only with warp w of CTA k of ranks r-1 and r+1: the step
-// loop has no block-wide barrier.  Per batch, software-pipelined: load the
-// batch (lines + own elements), add and store (next rank's lines, outputs),
-// poll the next batch's flags (relaxed), then one fence that both releases
-// this batch's lines and acquires the next batch's, then the flags.
+// loop has no block-wide barrier.  Per batch, software-pipelined: add and
+// store the batch (next rank's lines, outputs), acquire the next batch's
+// flags and issue its loads, then release this batch (fence, flags) while
+// those loads are in flight.  A wait that gives up returns at once.
 template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM: 128 registers, no spills
-ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
-                       const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, uint64_t seq,
-                       int64_t spin_ns, int absent, int prefetch, DevStatus* st)
+__device__ __forceinline__ void persist_warp(const CPtrs<NR>& in, const MPtrs<NR>& out, const Persist& P, size_t C,
+                                             size_t count, size_t epc, uint64_t seq, int64_t spin_ns, int absent,
+                                             int prefetch, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
     constexpr int kI = kBatchLines / 4;   // lines per lane group per batch
@@ -414,6 +417,25 @@ ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
     }
 }
 
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM: 128 registers, no spills
+ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
+                       const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, int64_t spin_ns,
+                       int absent, int prefetch, DevStatus* st)
+{
+    // the same for every warp: only this call's last warp advances it
+    const uint64_t seq = ld_relaxed(P.epoch_w) + 1;
+    persist_warp<NR, DT>(in, out, P, C, count, epc, seq, spin_ns, absent, prefetch, st);
+    if ((threadIdx.x & 31) == 0) {
+        fence_gpu();
+        const unsigned total = gridDim.x * gridDim.y * (unsigned)kPWarps;
+        if (atomicAdd(P.done_w, 1u) == total - 1) {   // every other warp of the call is done
+            *P.done_w = 0u;
+            st_relaxed(P.epoch_w, seq);
+        }
+    }
+}
+
 }  // namespace
 
 // Calls up to this many bytes per rank prefetch each step's own elements
@@ -489,7 +511,8 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             P.kcap = persist_kcap(h.n, h.sm_count);
             P.acks = reinterpret_cast<uint64_t*>(h.persist + (size_t)h.n * 2 * lps * 128);
             P.abort_w = P.acks + (size_t)h.n * P.kcap * kPWarps;
-            const uint64_t seq = ++h.persist_seq;
+            P.epoch_w = P.abort_w + 1;
+            P.done_w = reinterpret_cast<unsigned*>(P.abort_w + 2);
 
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeCooperative;
@@ -506,7 +529,7 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             const uint64_t bytes = 2ull * ((uint64_t)NR * e * count + (uint64_t)(2 * NR - 2) * 128ull * L);
             rec_begin(h, s);
             const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_persistent_kernel<NR, DT>, ip, op, P, C, count,
-                                                       epc, seq, h.spin_ns, h.persist_absent,
+                                                       epc, h.spin_ns, h.persist_absent,
                                                        (int)(count * e <= kPersistPrefetchBytes), h.status);
             rec_end(h, s, AR_K_RING_PERSISTENT, bytes);
             *launches = 1;

@@ -32,8 +32,9 @@
  *     exercise 3).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream), never allocate and never synchronize, so they can be
- *     issued inside CUDA graph capture (tested for ar_one_shot, ar_two_shot
- *     and ar_ring; the optional buffers of AR_OPT_PUSH_STAGING,
+ *     issued inside CUDA graph capture (tested, with replays, for every
+ *     all-reduce call but ar_ring_noalloc and ar_allreduce_rmsnorm; the
+ *     optional buffers of AR_OPT_PUSH_STAGING,
  *     AR_OPT_REGISTERED and AR_OPT_PERSISTENT are allocated when the option
  *     is set, never in a call).  Host-side argument errors are
  *     returned at once and nothing is launched.  Errors found by a kernel

@@ -407,3 +407,30 @@ def test_tree_in_place_hand_worked_and_refusals():
         ins3, outs3 = empty_ranks(3, 64), empty_ranks(3, 64)
         assert ar.ar_tree(h, ptrs(ins3), ptrs(outs3), 16, "bf16") == ar.AR_ERR_INVALID
         assert ar.ar_tree(h, ptrs(ins3), ptrs(outs3), 0, "bf16") == ar.AR_ERR_INVALID
+
+
+@pytest.mark.parametrize("call,oracle_fn", [
+    ("ar_one_shot_push", "all_reduce"), ("ar_one_shot_copyin", "all_reduce"), ("ar_ring_rounded", "ring_rounded"),
+    ("ar_tree", "tree"), ("ar_ring_persistent", "ring")])
+def test_cuda_graph_capture_of_the_other_calls(call, oracle_fn):
+    # captured once, replayed on new contents of the same buffers
+    n, N = 8, 65536 + 3
+    xs = workloads.rank_inputs(n, N, "bf16", "normal_over_n", seed=14)
+    ys = workloads.rank_inputs(n, N, "bf16", "normal_over_n", seed=15)
+    ins = upload_ranks(xs)
+    outs = empty_ranks(n, xs[0].nbytes)
+    with Handle(n, N * 2, push_staging=1, registered=1, persistent=1) as h:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rc = getattr(ar, call)(h, ptrs(ins), ptrs(outs), N, "bf16", s)
+        assert rc == ar.AR_OK
+        for src in (xs, ys):
+            for b, a in zip(ins, src):
+                b.upload(a)
+            g.replay()
+            torch.cuda.synchronize()
+            want = getattr(oracle, oracle_fn)(src, "bf16")
+            for r in (0, 5):
+                np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
+        assert ar.ar_status(h) == ar.AR_OK
