@@ -711,10 +711,11 @@ def run_ours(args):
     lls = ll_sweep(wl, peak) if args.sweep else None
     e2e = e2e_leg(wl, max(3, min(args.steps, args.e2e_steps)), bytes_step) if args.e2e else None
     n16 = n16_sweep(dev, peak) if args.sweep else None
-    cpu = cpu_par = None
+    cpu = cpu_par = cpu_calls = None
     if world == 1 and rank == 0 and args.cpu_baseline:
         cpu = cpu_baseline(seconds=args.cpu_seconds)
         cpu_par = cpu_parallel(seconds=args.cpu_seconds)
+        cpu_calls = calls_cpu() if args.sweep else None
     wl.close()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -732,7 +733,7 @@ def run_ours(args):
         "launch_timing": {"steps_sampled": sampled, "every": every, "records": len(records),
                           "launches_recorded": sum(r[4] for r in records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),
-        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "cpu_parallel": cpu_par, "sweep": sw,
+        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "cpu_parallel": cpu_par, "cpu_calls": cpu_calls, "sweep": sw,
         "fused_epilogue": fe, "variants": va, "ll_sweep": lls, "n16_sweep": n16,
     }
     if rank == 0:
@@ -843,6 +844,53 @@ def cpu_parallel(seconds: float = 10.0, scale_div: int = 32) -> dict:
             "kind": "oracle routines, element-range parallel",
             "sample": f"the cpu_baseline sample (1/{scale_div} of the step) over {threads} threads, "
                       f"{reps} passes in {dt:.1f} s"}
+
+
+def calls_cpu(min_seconds: float = 0.5) -> dict:
+    """The oracle beside each all-reduce call of the variants leg and beside
+    the fused epilogue: n = 8 bf16 at 1 MiB per rank (the epilogue at
+    64 tokens x 8192), timed single-threaded on the host, GB/s of the same
+    algorithmic bytes the GPU figures use (ar_plan)."""
+    import numpy as np
+
+    import all_reduce_reduction_rank_gb300 as ar
+    import oracle
+    import workloads
+    n, N = 8, (1 * MiB) // 2
+    xs = workloads.rank_inputs(n, N, "bf16", "normal_over_n", 1003)
+    rows = {}
+
+    def timed(fn):
+        fn()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            reps += 1
+            if time.perf_counter() - t0 >= min_seconds:
+                return (time.perf_counter() - t0) / reps
+
+    for name, fn, op in (("one_shot", lambda: oracle.all_reduce(xs, "bf16"), ar.AR_OP_ONE_SHOT),
+                         ("one_shot_push", lambda: oracle.all_reduce(xs, "bf16"), ar.AR_OP_ONE_SHOT_PUSH),
+                         ("one_shot_copyin", lambda: oracle.all_reduce(xs, "bf16"), ar.AR_OP_ONE_SHOT_COPYIN),
+                         ("two_shot", lambda: oracle.all_gather(oracle.reduce_scatter(xs, "bf16"), "bf16"),
+                          ar.AR_OP_TWO_SHOT),
+                         ("ring", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING),
+                         ("ring_rounded", lambda: oracle.ring_rounded(xs, "bf16"), ar.AR_OP_RING_ROUNDED),
+                         ("ring_persistent", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_PERSISTENT),
+                         ("tree", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE)):
+        t = ar.ar_plan(op, n, N, "bf16")
+        sec = timed(fn)
+        rows[name] = {"bytes_per_rank": 2 * N, "ms": round(sec * 1e3, 3),
+                      "GB/s": round((t.hbm_read_bytes + t.hbm_write_bytes) / sec / 1e9, 3)}
+    T, H = 64, 8192
+    xr = workloads.rank_inputs(n, T * H, "bf16", "normal", 1005)
+    res = workloads.rank_inputs(1, T * H, "bf16", "normal", 1006)[0]
+    w = workloads.rank_inputs(1, H, "bf16", "uniform", 1007)[0]
+    sec = timed(lambda: oracle.allreduce_rmsnorm(xr, res, w, 1e-6, T, H, "bf16"))
+    S = T * H * 2
+    rows["allreduce_rmsnorm"] = {"tokens": T, "hidden": H, "ms": round(sec * 1e3, 3),
+                                 "GB/s": round(((2 * n + 2) * S + 2 * H) / sec / 1e9, 3)}
+    return {"kind": "oracle", "cores": 1, "sample": "n=8 bf16, 1 MiB per rank; epilogue 64 x 8192", **rows}
 
 
 def run_reference(args):
