@@ -1,0 +1,474 @@
+// Persistent ring all-reduce over a thread-block cluster: the ranks are the
+// CTAs of one cluster and a hop goes through distributed shared memory.
+//
+// The same protocol and sums as ring_persistent.cu (handbook "集合通信：NCCL
+// 的算法、协议与推理框架的定制 all-reduce", §协议: LL128 lines of 120 bytes of
+// data and an 8-byte flag, the receiver polling the flag; "多 GPU 与 NCCL",
+// §ring all-reduce: the steps and chunk rotation; fp32 partials, chunk c
+// summed from rank c, rounded once), so the result equals ar_ring's bit for
+// bit.  What differs is where the receiving inbox lives: in the receiving
+// CTA's shared memory, written by the sending CTA of the same cluster with
+// st.shared::cluster.  On this GPU a flag round trip through distributed
+// shared memory takes ~0.53 us against ~1.7 us through global memory, and
+// the lines never touch L2 or HBM: HBM sees only the ranks' own elements and
+// outputs, 2 n S per call, as one-shot does.
+//
+// Layout: cluster size n (one CTA per rank, cluster_ctarank = rank);
+// cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of 960
+// elements = 32 lines); clusters are independent, so the grid may run in any
+// number of waves and needs no cooperative launch.  Warp w of rank r handles
+// batches b = w, w+8, ... of the slice and exchanges lines only with warp w
+// of ranks r-1 and r+1.
+//
+// Shared memory of a CTA: per warp kSlots inbox slots of 32 lines (one batch
+// each), the per-warp count of batches its receiver has consumed, and an
+// abort word.  The sender writes batch q into slot q % kSlots once the
+// receiver has consumed batch q - kSlots; a line's flag is q + 1.  Shared
+// memory is zeroed at the start, behind a cluster barrier, so no flag of an
+// earlier launch survives; a cluster barrier at the end keeps every CTA
+// alive until no peer can still write into it.
+//
+// Ordering: data stores to the peer, __syncwarp, fence.acq_rel.cluster, flag
+// stores; the receiver polls its flags with ld.acquire.cluster, __syncwarp,
+// then reads the lines; the consumed count is published with
+// st.release.cluster.  Every wait is bounded by spin_ns and a poll count; a
+// wait that runs out records AR_ERR_FLAG_TIMEOUT (a line) or
+// AR_ERR_WAIT_TIMEOUT (a slot) and raises the abort word of every CTA of the
+// cluster, on which the other waits give up; all threads still reach the
+// final cluster barrier.
+#include "common.cuh"
+
+namespace argb {
+namespace {
+
+constexpr int kCWarps = kThreads / 32;
+constexpr int kCLineWords = 30;
+constexpr int kCBatchLines = 32;
+constexpr size_t kCBatchElems = (size_t)kCLineWords * kCBatchLines;   // 960
+constexpr int kSlots = 2;                                                 // inbox slots per warp
+constexpr unsigned kCFull = 0xffffffffu;
+constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kCBatchLines * 128;
+// inbox, then consumed[kCWarps] and the abort word, rounded to 16 bytes
+constexpr size_t kClusterSmem = kInboxBytes + ((kCWarps + 1) * sizeof(uint64_t) + 15) / 16 * 16;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t cta)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(cta));
+    return a;
+}
+
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acq_local(uint32_t a)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_rlx_local(uint32_t a)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld16_local(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st16_peer(uint32_t a, const uint4& v)
+{
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st8_peer(uint32_t a, uint32_t x, uint32_t y)
+{
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+
+__device__ __forceinline__ void st_rlx_peer(uint32_t a, uint64_t v)
+{
+    asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_rel_peer(uint32_t a, uint64_t v)
+{
+    asm volatile("st.release.cluster.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ uint2 ldg8(const void* p)
+{
+    uint2 v;
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg4(const void* p)
+{
+    uint32_t v;
+    asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Raw words of elements e .. e+nw-1 of a chunk of `len` elements (zero past
+// len): 4 fp32 words, or 2 words of two 16-bit elements.
+template <int DT> constexpr int kCRaw = DT == AR_F32 ? 4 : 2;
+
+template <int DT>
+__device__ __forceinline__ void load_raw(const void* chunk, size_t e, int nw, size_t len, uint32_t* w)
+{
+    using T = typename Payload<DT>::scalar_t;
+    const T* x = static_cast<const T*>(chunk);
+    if (e + (size_t)nw <= len) {
+        if constexpr (DT == AR_F32) {
+            const uint2 a = ldg8(x + e);
+            w[0] = a.x;
+            w[1] = a.y;
+            w[2] = w[3] = 0u;
+            if (nw == 4) {
+                const uint2 b = ldg8(x + e + 2);
+                w[2] = b.x;
+                w[3] = b.y;
+            }
+        } else {
+            w[0] = ldg4(x + e);
+            w[1] = nw == 4 ? ldg4(x + e + 2) : 0u;
+        }
+    } else {
+        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(chunk);
+        const uint32_t* x32 = reinterpret_cast<const uint32_t*>(chunk);
+#pragma unroll
+        for (int u = 0; u < kCRaw<DT>; ++u) w[u] = 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (u < nw && e + u < len) {
+                if constexpr (DT == AR_F32) w[u] = x32[e + u];
+                else w[u >> 1] |= (uint32_t)x16[e + u] << (16 * (u & 1));
+            }
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_raw(const uint32_t* w, float* f)
+{
+    if constexpr (DT == AR_F32) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(w[u]);
+    } else {
+        Payload<DT>::widen(w[0], f);
+        Payload<DT>::widen(w[1], f + 2);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void store_out(void* chunk, size_t e, int nw, size_t len, const float* f)
+{
+    using T = typename Payload<DT>::scalar_t;
+    T* y = static_cast<T*>(chunk);
+    if (e + (size_t)nw <= len) {
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+            if (u >= nw) break;
+            if constexpr (DT == AR_F32) {
+                asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(y + e + u), "r"(__float_as_uint(f[u])),
+                             "r"(__float_as_uint(f[u + 1]))
+                             : "memory");
+            } else {
+                const uint32_t w = Payload<DT>::narrow(f + u);
+                asm volatile("st.global.u32 [%0], %1;" ::"l"(y + e + u), "r"(w) : "memory");
+            }
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (u < nw && e + u < len) y[e + u] = Payload<DT>::narrow1(f[u]);
+    }
+}
+
+struct ClusterSmem {
+    uint32_t inbox;      // shared address of this CTA's inbox
+    uint32_t consumed;   // shared address of consumed[0]
+    uint32_t abort;      // shared address of the abort word
+};
+
+// Raise the abort word of every CTA of the cluster.
+template <int NR>
+__device__ void raise_abort(const ClusterSmem& S)
+{
+#pragma unroll
+    for (int q = 0; q < NR; ++q) st_rlx_peer(peer_addr(S.abort, (uint32_t)q), 1ull);
+}
+
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads, 2)
+ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t C,
+                    size_t count, size_t epc, int64_t spin_ns, int absent, int prefetch, DevStatus* st)
+{
+    using T = typename Payload<DT>::scalar_t;
+    constexpr int kI = kCBatchLines / 4;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint32_t crank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    const int r = (int)crank;
+    const size_t k = blockIdx.x / NR;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 3, j = lane & 7;
+    const int nw = j < 7 ? 4 : 2;
+    const int d = (r + 1) % NR, p = (r + NR - 1) % NR;   // next and previous rank
+    ClusterSmem S;
+    S.inbox = smem_addr(smem);
+    S.consumed = S.inbox + (uint32_t)kInboxBytes;
+    S.abort = S.consumed + kCWarps * 8;
+
+    // zero the inbox flags, consumed counts and abort word, then let every
+    // CTA of the cluster see that before any peer writes
+    for (uint32_t o = threadIdx.x * 16; o < (uint32_t)kClusterSmem; o += kThreads * 16)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(S.inbox + o), "r"(0u) : "memory");
+    cluster_barrier();
+
+    const size_t slice_lo = k * epc;
+    const size_t line_lo = slice_lo / kCLineWords;
+    const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kCBatchLines * 128);
+    const uint32_t peer_box = peer_addr(my_box, (uint32_t)d);                    // the next rank's inbox for this warp
+    const uint32_t my_consumed = S.consumed + 8 * warp;                            // written by the next rank
+    const uint32_t prev_consumed = peer_addr(S.consumed + 8 * warp, (uint32_t)p);  // the previous rank's copy
+    uint64_t q_recv = 0, q_send = 0;
+    bool dead = (r == absent);   // a rank that never joins (failure emulation)
+
+    for (int t = 0; t <= 2 * NR - 2 && !dead; ++t) {
+        const bool sends = t <= 2 * NR - 3;
+        const int c = t <= NR - 2 ? ((r - t) % NR + NR) % NR : ((r + NR - t) % NR + NR) % NR;
+        const size_t lo = (size_t)c * C;
+        const size_t len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
+        const size_t slice_hi = slice_lo + epc < len ? slice_lo + epc : len;
+        const size_t nlines = slice_hi > slice_lo ? (slice_hi - slice_lo + kCLineWords - 1) / kCLineWords : 0;
+        const size_t nbatch = (nlines + kCBatchLines - 1) / kCBatchLines;
+        const T* const x = static_cast<const T*>(in.p[r]) + lo;
+        T* const y = static_cast<T*>(out.p[r]) + lo;
+        if (prefetch && t <= NR - 1) {
+            for (size_t bb = warp; bb < nbatch; bb += kCWarps) {
+                const size_t e0 = (line_lo + bb * kCBatchLines) * kCLineWords + (size_t)lane * (128 / sizeof(T));
+                if (e0 < slice_hi) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + e0));
+            }
+        }
+        for (size_t b = warp; b < nbatch; b += kCWarps) {
+            const size_t base = line_lo + b * kCBatchLines;
+            // the rank's own elements first: they do not wait for any flag
+            uint32_t xr[kI][kCRaw<DT>];
+            if (t <= NR - 1) {
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    load_raw<DT>(x, l * kCLineWords + 4 * (size_t)j, nw, l * kCLineWords < slice_hi ? len : 0,
+                                 xr[i]);
+                }
+            }
+            uint4 w[kI];
+#pragma unroll
+            for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (t >= 1) {   // receive: wait for the 32 flags of this batch's slot
+                const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kCBatchLines * 128);
+                const bool live = (base + lane) * kCLineWords < slice_hi;
+                const uint32_t flag = slot + lane * 128 + 120;
+                bool ok = !live || ld_acq_local(flag) == q_recv + 1;
+                if (!__all_sync(kCFull, ok)) {
+                    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
+                    bool stop = false;
+                    for (uint64_t it = 0; it < cap && !stop; ++it) {
+                        if (it >= 1024) __nanosleep(32);
+                        if (!ok) ok = ld_acq_local(flag) == q_recv + 1;
+                        if (__all_sync(kCFull, ok)) break;
+                        if ((it & 31) == 31)
+                            stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
+                                                          ld_rlx_local(S.abort) != 0);
+                    }
+                    if (!__all_sync(kCFull, ok)) {
+                        if (ld_rlx_local(S.abort) == 0) {
+                            if (!ok) report_flag_timeout(st, r, base + lane);
+                            if (lane == 0) raise_abort<NR>(S);
+                        }
+                        dead = true;
+                        break;
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    if (l * kCLineWords < slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
+                }
+            }
+            float v[kI][4];
+#pragma unroll
+            for (int i = 0; i < kI; ++i) {
+                v[i][0] = __uint_as_float(w[i].x);
+                v[i][1] = __uint_as_float(w[i].y);
+                v[i][2] = __uint_as_float(w[i].z);
+                v[i][3] = __uint_as_float(w[i].w);
+                if (t <= NR - 1) {
+                    float xv[4];
+                    widen_raw<DT>(xr[i], xv);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[i][u] = t == 0 ? xv[u] : v[i][u] + xv[u];
+                }
+                if (t == NR - 1) {   // rounded once; the rounded value is passed on
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[i][u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[i][u]));
+                }
+            }
+            if (t >= 1) {   // this slot is free again: tell the previous rank
+                __syncwarp();
+                if (lane == 0) st_rel_peer(prev_consumed, q_recv + 1);
+                ++q_recv;
+            }
+            if (sends) {
+                // the next rank must have consumed the batch that last used this slot
+                if (q_send >= kSlots) {
+                    const uint64_t want = q_send - kSlots + 1;
+                    bool ok = ld_acq_local(my_consumed) >= want;
+                    if (!__all_sync(kCFull, ok)) {
+                        const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
+                        bool stop = false;
+                        for (uint64_t it = 0; it < cap && !stop; ++it) {
+                            if (it >= 1024) __nanosleep(32);
+                            ok = ld_acq_local(my_consumed) >= want;
+                            if (__all_sync(kCFull, ok)) break;
+                            if ((it & 31) == 31)
+                                stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
+                                                              ld_rlx_local(S.abort) != 0);
+                        }
+                        if (!__all_sync(kCFull, ok)) {
+                            if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                                report_wait_timeout(st);
+                                raise_abort<NR>(S);
+                            }
+                            dead = true;
+                            break;
+                        }
+                    }
+                }
+                const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kCBatchLines * 128);
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    if (l * kCLineWords >= slice_hi) continue;
+                    const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
+                    if (j < 7)
+                        st16_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                                __float_as_uint(v[i][2]), __float_as_uint(v[i][3])));
+                    else
+                        st8_peer(a, __float_as_uint(v[i][0]), __float_as_uint(v[i][1]));
+                }
+                __syncwarp();
+                fence_cluster();
+                if ((base + lane) * kCLineWords < slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
+                ++q_send;
+            }
+            // this rank's output last, after the hop is on its way
+            if (t >= NR - 1) {
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    if (l * kCLineWords < slice_hi) store_out<DT>(y, l * kCLineWords + 4 * (size_t)j, nw, len, v[i]);
+                }
+            }
+        }
+        if (!dead && ld_rlx_local(S.abort) != 0) dead = true;
+        dead = __any_sync(kCFull, dead);
+    }
+    // no CTA leaves while a peer may still write into its shared memory
+    cluster_barrier();
+}
+
+}  // namespace
+
+int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                        int* launches)
+{
+    return dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            CPtrs<NR> ip;
+            MPtrs<NR> op;
+            for (int q = 0; q < NR; ++q) {
+                ip.p[q] = in[q];
+                op.p[q] = out[q];
+            }
+            static const bool attr_ok =
+                cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kClusterSmem) == cudaSuccess &&
+                (NR <= 8 || cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>,
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess);
+            if (!attr_ok) {
+                cudaGetLastError();
+                return AR_ERR_CUDA;
+            }
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = NR;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cudaLaunchConfig_t cfg{};
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kClusterSmem;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            // clusters that fit at once: one wave of them
+            static int resident = -1;
+            if (resident < 0) {
+                cfg.gridDim = dim3((unsigned)(NR * 64));
+                if (cudaOccupancyMaxActiveClusters(&resident, ring_cluster_kernel<NR, DT>, &cfg) != cudaSuccess)
+                    resident = 0;
+                cudaGetLastError();
+            }
+            if (resident < 1) return AR_ERR_CUDA;
+            const size_t C = chunk_elems(NR, count, DT);
+            // slices of at least one batch per warp; one wave of clusters
+            // unless that would give a warp more batches per step than its
+            // receiver has inbox slots: at step 0 every rank sends without
+            // receiving, so a step's batches must fit in the receiver's slots
+            // (otherwise every rank waits on its successor: a cycle)
+            const size_t per_cta_min = kCBatchElems * kCWarps;
+            size_t K = (C + per_cta_min - 1) / per_cta_min;
+            if (K > (size_t)resident) K = (size_t)resident;
+            if (K < 1) K = 1;
+            size_t epc = (C + K - 1) / K;
+            epc = (epc + kCBatchElems - 1) / kCBatchElems * kCBatchElems;
+            if (epc > kCBatchElems * kCWarps * kSlots) epc = kCBatchElems * kCWarps * kSlots;
+            K = (C + epc - 1) / epc;
+            if (K < 1) K = 1;
+            cfg.gridDim = dim3((unsigned)(K * NR));
+            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            rec_begin(h, s);
+            const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_cluster_kernel<NR, DT>, ip, op, C, count, epc,
+                                                       h.spin_ns, h.persist_absent,
+                                                       (int)(S <= (32ull << 20)), h.status);
+            rec_end(h, s, AR_K_RING_CLUSTER, 2ull * NR * S);
+            *launches = 1;
+            if (err != cudaSuccess) {
+                cudaGetLastError();
+                return AR_ERR_CUDA;
+            }
+            return launch_status();
+        });
+    });
+}
+
+}  // namespace argb

@@ -86,7 +86,8 @@ typedef enum {
     AR_OP_ONE_SHOT_COPYIN = 12,
     AR_OP_RING_ROUNDED = 13,
     AR_OP_TREE = 14,
-    AR_OP_RING_PERSISTENT = 15
+    AR_OP_RING_PERSISTENT = 15,
+    AR_OP_RING_CLUSTER = 16
 } ar_op;
 
 /* Traffic of one call.
@@ -175,7 +176,8 @@ typedef enum {
     AR_K_RING_RS_STEP_ROUNDED = 15, /* ar_ring_rounded's reduce-scatter step */
     AR_K_TREE_LEVEL = 16,           /* one level of ar_tree */
     AR_K_RING_PERSISTENT = 17,      /* ar_ring_persistent (all steps) */
-    AR_K_COPYIN = 18                /* ar_one_shot_copyin's copy into the registered buffers */
+    AR_K_COPYIN = 18,               /* ar_one_shot_copyin's copy into the registered buffers */
+    AR_K_RING_CLUSTER = 19          /* ar_ring_cluster (all steps) */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -296,6 +298,17 @@ int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, 
  * ceil(chunk length / 30). */
 int ar_ring_persistent(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
+
+/* The persistent LL128 ring of ar_ring_persistent with the ranks mapped onto
+ * the CTAs of a thread-block cluster (cluster size n_ranks, up to 16): a hop
+ * writes the LL128 lines (and their flags) straight into the receiving CTA's
+ * shared memory, so the lines never reach L2 or HBM, and polling is local.
+ * Each cluster owns a slice of every chunk; clusters are independent.  Same
+ * bits as ar_ring.  Needs no optional buffers.  Waits are bounded as in
+ * ar_ring_persistent; AR_OPT_ABSENT_RANK applies.  AR_ERR_CUDA if the device
+ * cannot run a cluster of n_ranks CTAs.  HBM: reads n S, writes n S. */
+int ar_ring_cluster(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                    ar_stream_t stream);
 
 /* Ring all-reduce for callers that cannot allocate device memory (code that
  * runs where cudaMalloc is not allowed or not wanted: inside a framework that
@@ -453,7 +466,7 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
 /* Host only, no GPU needed: the code a call would return for these
  * arguments before launching anything.  op AR_OP_ONE_SHOT, AR_OP_TWO_SHOT,
  * AR_OP_RING, AR_OP_ONE_SHOT_PUSH, AR_OP_ONE_SHOT_COPYIN, AR_OP_RING_ROUNDED,
- * AR_OP_TREE (n_ranks a power of two), AR_OP_RING_PERSISTENT,
+ * AR_OP_TREE (n_ranks a power of two), AR_OP_RING_PERSISTENT, AR_OP_RING_CLUSTER,
  * AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls (n_ranks in
  * [2, 16]; the handle's optional buffers are not checked); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
  * AR_OP_LL128_UNPACK: the batched pack / unpack calls over n_ranks buffers

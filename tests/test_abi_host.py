@@ -102,7 +102,7 @@ def test_plan_batched_pack_scales_with_buffers(lib, nb):
 
 
 def test_plan_rejects_bad_arguments(lib):
-    bad = [(0, 8), (ar.AR_OP_RING_PERSISTENT + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
+    bad = [(0, 8), (ar.AR_OP_RING_CLUSTER + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
            (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]
     for op, n in bad:
         with pytest.raises(ar.ArError):
@@ -327,3 +327,12 @@ def test_plan_ring_persistent(lib, n, N):
     assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))
     ins, outs = _bufs(n), _bufs(n, off=64 << 20)
     assert _check(ar.AR_OP_RING_PERSISTENT, n, ins, outs, 1000) == ar.AR_OK
+
+
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+def test_plan_ring_cluster(lib, n):
+    N = 4099
+    t = ar.ar_plan(ar.AR_OP_RING_CLUSTER, n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (n * 2 * N, n * 2 * N)
+    assert t.steps == 2 * (n - 1) and t.launches == 1
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))

@@ -411,7 +411,7 @@ def test_tree_in_place_hand_worked_and_refusals():
 
 @pytest.mark.parametrize("call,oracle_fn", [
     ("ar_one_shot_push", "all_reduce"), ("ar_one_shot_copyin", "all_reduce"), ("ar_ring_rounded", "ring_rounded"),
-    ("ar_tree", "tree"), ("ar_ring_persistent", "ring")])
+    ("ar_tree", "tree"), ("ar_ring_persistent", "ring"), ("ar_ring_cluster", "ring")])
 def test_cuda_graph_capture_of_the_other_calls(call, oracle_fn):
     # captured once, replayed on new contents of the same buffers
     n, N = 8, 65536 + 3

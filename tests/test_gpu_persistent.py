@@ -141,3 +141,91 @@ def test_persistent_ring_absent_rank_times_out_and_the_handle_stays_usable(absen
     want = oracle.ring(xs, "f32")
     for r in range(n):
         np.testing.assert_array_equal(got[r], want[r])
+
+
+# --- the same ring over a thread-block cluster (ar_ring_cluster) -------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 1), (2, 9), (3, 1000), (5, 300_001), (8, 4099), (8, 7680 * 8 + 3),
+                                 (16, 65536 + 3), (16, 17), (8, 2_000_003)])
+def test_cluster_ring_matches_the_ring_oracle(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=13 * n + N)
+    want = oracle.ring(xs, dtype)
+    ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype])) as h:
+        rc = ar.ar_ring_cluster(h, ptrs(ins), ptrs(outs), N, dtype)
+        assert rc == ar.AR_OK, ar.ar_strerror(rc)
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+        t = ar.ar_traffic(h)
+        assert t.op == ar.AR_OP_RING_CLUSTER and t.launches == 1
+    for b in ins + outs:
+        assert b.guards_intact()
+    for r in range(n):
+        np.testing.assert_array_equal(bits(outs[r].download(payload_np_dtype(dtype))), bits(want[r]))
+
+
+def test_cluster_ring_in_place_repeated_and_equal_to_the_step_ring():
+    n = 8
+    with Handle(n, 2 * 3_000_017) as h:
+        for i, N in enumerate([3_000_017, 1000, 400_000, 8]):
+            xs = workloads.rank_inputs(n, N, "bf16", "normal_over_n", seed=200 + i)
+            ins = upload_ranks(xs)
+            outs = ins if i % 2 else empty_ranks(n, xs[0].nbytes)
+            assert ar.ar_ring_cluster(h, ptrs(ins), ptrs(outs), N, "bf16") == ar.AR_OK
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK
+            want = oracle.ring(xs, "bf16")
+            for r in range(n):
+                np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
+
+
+@pytest.mark.parametrize("absent", [0, 5])
+def test_cluster_ring_absent_rank_times_out_and_the_handle_stays_usable(absent):
+    n, N = 8, 200_000
+    xs = workloads.rank_inputs(n, N, "f32", "normal", seed=19)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 4)
+    with Handle(n, N * 4, spin_ns=200_000, absent_rank=absent) as h:
+        assert ar.ar_ring_cluster(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_OK
+        torch.cuda.synchronize()
+        rc, info = ar.ar_status_info(h)
+        assert rc in (ar.AR_ERR_FLAG_TIMEOUT, ar.AR_ERR_WAIT_TIMEOUT)
+        assert ar.ar_status(h) == ar.AR_OK
+        assert ar.ar_set_option(h, ar.AR_OPT_ABSENT_RANK, -1) == ar.AR_OK
+        assert ar.ar_ring_cluster(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_OK
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+    want = oracle.ring(xs, "f32")
+    for r in range(n):
+        np.testing.assert_array_equal(outs[r].download(np.float32), want[r])
+
+
+def test_cluster_ring_timing_record_and_plan():
+    n, N = 4, 100_000
+    xs = workloads.rank_inputs(n, N, "f32", "normal", seed=21)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 4)
+    with Handle(n, N * 4, timing=16) as h:
+        assert ar.ar_ring_cluster(h, ptrs(ins), ptrs(outs), N, "f32") == ar.AR_OK
+        recs = ar.ar_timing(h)
+    assert [r[0] for r in recs] == ["ring_cluster"]
+    t = ar.ar_plan(ar.AR_OP_RING_CLUSTER, n, N, "f32")
+    assert recs[0][3] == t.hbm_read_bytes + t.hbm_write_bytes == 2 * n * N * 4
+
+
+@pytest.mark.parametrize("n,N", [(2, 16 << 20), (8, 32 << 20)])
+def test_cluster_ring_large_slices(n, N):
+    # sizes where one wave of clusters would give a warp many batches per
+    # step: the slices are capped so that a step's batches fit the inbox
+    ins = workloads.rank_inputs_device(n, N, "bf16", "normal_over_n", 4321 + n)
+    a = [torch.empty_like(t) for t in ins]
+    c = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, 2 * N)
+    try:
+        assert ar.ar_ring(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in a], N, "bf16") == ar.AR_OK
+        assert ar.ar_ring_cluster(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in c], N, "bf16") == ar.AR_OK
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+    for r in range(n):
+        assert torch.equal(a[r], c[r])
