@@ -23,15 +23,19 @@
 // Shared memory of a CTA: per warp kSlots inbox slots of 32 lines (one batch
 // each), the per-warp count of batches its receiver has consumed, and an
 // abort word.  The sender writes batch q into slot q % kSlots once the
-// receiver has consumed batch q - kSlots; a line's flag is q + 1.  Shared
+// receiver has consumed batch q - kSlots; a line's flag is q + 1.  A warp
+// walks its (step, batch) pairs in one software-pipelined loop: it issues
+// the loads of the next pair's own elements before it sends the current
+// one, and publishes a consumed slot after its own send (one fence serves
+// both), which needs a step's batches to fit in kSlots - 1 slots.  Shared
 // memory is zeroed at the start, behind a cluster barrier, so no flag of an
 // earlier launch survives; a cluster barrier at the end keeps every CTA
 // alive until no peer can still write into it.
 //
 // Ordering: data stores to the peer, __syncwarp, fence.acq_rel.cluster, flag
 // stores; the receiver polls its flags with ld.acquire.cluster, __syncwarp,
-// then reads the lines; the consumed count is published with
-// st.release.cluster.  Every wait is bounded by spin_ns and a poll count; a
+// then reads the lines; the consumed count is a relaxed store after the
+// same fence.  Every wait is bounded by spin_ns and a poll count; a
 // wait that runs out records AR_ERR_FLAG_TIMEOUT (a line) or
 // AR_ERR_WAIT_TIMEOUT (a slot) and raises the abort word of every CTA of the
 // cluster, on which the other waits give up; all threads still reach the
@@ -45,7 +49,7 @@ constexpr int kCWarps = kThreads / 32;
 constexpr int kCLineWords = 30;
 constexpr int kCBatchLines = 32;
 constexpr size_t kCBatchElems = (size_t)kCLineWords * kCBatchLines;   // 960
-constexpr int kSlots = 2;                                                 // inbox slots per warp
+constexpr int kSlots = 3;                                                 // inbox slots per warp
 constexpr unsigned kCFull = 0xffffffffu;
 constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kCBatchLines * 128;
 // inbox, then consumed[kCWarps] and the abort word, rounded to 16 bytes
@@ -101,11 +105,6 @@ __device__ __forceinline__ void st8_peer(uint32_t a, uint32_t x, uint32_t y)
 __device__ __forceinline__ void st_rlx_peer(uint32_t a, uint64_t v)
 {
     asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_rel_peer(uint32_t a, uint64_t v)
-{
-    asm volatile("st.release.cluster.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
@@ -217,7 +216,7 @@ __device__ void raise_abort(const ClusterSmem& S)
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads, 2)
 ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t C,
-                    size_t count, size_t epc, int64_t spin_ns, int absent, int prefetch, DevStatus* st)
+                    size_t count, size_t epc, int64_t spin_ns, int absent, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
     constexpr int kI = kCBatchLines / 4;
@@ -250,146 +249,177 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     uint64_t q_recv = 0, q_send = 0;
     bool dead = (r == absent);   // a rank that never joins (failure emulation)
 
-    for (int t = 0; t <= 2 * NR - 2 && !dead; ++t) {
-        const bool sends = t <= 2 * NR - 3;
+    // the warp's (step, batch) pairs in order: step t moves chunk c(t); the
+    // warp's batches of it are b = warp, warp + 8, ... below nbatch(t)
+    struct Geom {
+        size_t len, slice_hi, nbatch;
+        const T* x;
+        T* y;
+    };
+    auto geom = [&](int t) -> Geom {
         const int c = t <= NR - 2 ? ((r - t) % NR + NR) % NR : ((r + NR - t) % NR + NR) % NR;
         const size_t lo = (size_t)c * C;
-        const size_t len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
-        const size_t slice_hi = slice_lo + epc < len ? slice_lo + epc : len;
-        const size_t nlines = slice_hi > slice_lo ? (slice_hi - slice_lo + kCLineWords - 1) / kCLineWords : 0;
-        const size_t nbatch = (nlines + kCBatchLines - 1) / kCBatchLines;
-        const T* const x = static_cast<const T*>(in.p[r]) + lo;
-        T* const y = static_cast<T*>(out.p[r]) + lo;
-        if (prefetch && t <= NR - 1) {
-            for (size_t bb = warp; bb < nbatch; bb += kCWarps) {
-                const size_t e0 = (line_lo + bb * kCBatchLines) * kCLineWords + (size_t)lane * (128 / sizeof(T));
-                if (e0 < slice_hi) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + e0));
-            }
+        Geom G;
+        G.len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
+        G.slice_hi = slice_lo + epc < G.len ? slice_lo + epc : G.len;
+        const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kCLineWords - 1) / kCLineWords : 0;
+        G.nbatch = (nlines + kCBatchLines - 1) / kCBatchLines;
+        G.x = static_cast<const T*>(in.p[r]) + lo;
+        G.y = static_cast<T*>(out.p[r]) + lo;
+        return G;
+    };
+    constexpr int kLast = 2 * NR - 2;   // t = 2n-2: only the last receive
+    auto next_pair = [&](int& t, size_t& b, Geom& G) {   // the warp's next (step, batch), or t > kLast
+        b += kCWarps;
+        while (t <= kLast && b >= G.nbatch) {
+            ++t;
+            b = (size_t)warp;
+            if (t <= kLast) G = geom(t);
         }
-        for (size_t b = warp; b < nbatch; b += kCWarps) {
-            const size_t base = line_lo + b * kCBatchLines;
-            // the rank's own elements first: they do not wait for any flag
-            uint32_t xr[kI][kCRaw<DT>];
-            if (t <= NR - 1) {
+    };
+    // the rank's own elements of a batch: issued early, used later
+    uint32_t xr[kI][kCRaw<DT>];
+    auto load_x = [&](int t, size_t b, const Geom& G) {
+        if (t > NR - 1) return;
+        const size_t base = line_lo + b * kCBatchLines;
 #pragma unroll
-                for (int i = 0; i < kI; ++i) {
-                    const size_t l = base + 4 * i + g;
-                    load_raw<DT>(x, l * kCLineWords + 4 * (size_t)j, nw, l * kCLineWords < slice_hi ? len : 0,
-                                 xr[i]);
+        for (int i = 0; i < kI; ++i) {
+            const size_t l = base + 4 * i + g;
+            load_raw<DT>(G.x, l * kCLineWords + 4 * (size_t)j, nw, l * kCLineWords < G.slice_hi ? G.len : 0, xr[i]);
+        }
+    };
+
+    int t = 0;
+    size_t b = (size_t)warp;
+    Geom G = geom(0);
+    if (b >= G.nbatch) {   // the warp's first pair
+        b -= kCWarps;
+        next_pair(t, b, G);
+    }
+    if (!dead && t <= kLast) load_x(t, b, G);
+    while (!dead && t <= kLast) {
+        const bool sends = t <= kLast - 1;
+        const size_t base = line_lo + b * kCBatchLines;
+        uint4 w[kI];
+#pragma unroll
+        for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (t >= 1) {   // receive: wait for the 32 flags of this batch's slot
+            const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kCBatchLines * 128);
+            const bool live = (base + lane) * kCLineWords < G.slice_hi;
+            const uint32_t flag = slot + lane * 128 + 120;
+            bool ok = !live || ld_acq_local(flag) == q_recv + 1;
+            if (!__all_sync(kCFull, ok)) {
+                const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
+                bool stop = false;
+                for (uint64_t it = 0; it < cap && !stop; ++it) {
+                    if (it >= 1024) __nanosleep(32);
+                    if (!ok) ok = ld_acq_local(flag) == q_recv + 1;
+                    if (__all_sync(kCFull, ok)) break;
+                    if ((it & 31) == 31)
+                        stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
+                                                      ld_rlx_local(S.abort) != 0);
+                }
+                if (!__all_sync(kCFull, ok)) {
+                    if (ld_rlx_local(S.abort) == 0) {
+                        if (!ok) report_flag_timeout(st, r, base + lane);
+                        if (lane == 0) raise_abort<NR>(S);
+                    }
+                    dead = true;
+                    break;
                 }
             }
-            uint4 w[kI];
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (t >= 1) {   // receive: wait for the 32 flags of this batch's slot
-                const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kCBatchLines * 128);
-                const bool live = (base + lane) * kCLineWords < slice_hi;
-                const uint32_t flag = slot + lane * 128 + 120;
-                bool ok = !live || ld_acq_local(flag) == q_recv + 1;
+            for (int i = 0; i < kI; ++i) {
+                const size_t l = base + 4 * i + g;
+                if (l * kCLineWords < G.slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
+            }
+        }
+        float v[kI][4];
+#pragma unroll
+        for (int i = 0; i < kI; ++i) {
+            v[i][0] = __uint_as_float(w[i].x);
+            v[i][1] = __uint_as_float(w[i].y);
+            v[i][2] = __uint_as_float(w[i].z);
+            v[i][3] = __uint_as_float(w[i].w);
+            if (t <= NR - 1) {
+                float xv[4];
+                widen_raw<DT>(xr[i], xv);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[i][u] = t == 0 ? xv[u] : v[i][u] + xv[u];
+            }
+            if (t == NR - 1) {   // rounded once; the rounded value is passed on
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[i][u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[i][u]));
+            }
+        }
+        // the next pair's own elements now: their loads fly during the send
+        int t2 = t;
+        size_t b2 = b;
+        Geom G2 = G;
+        next_pair(t2, b2, G2);
+        if (t2 <= kLast) load_x(t2, b2, G2);
+        if (sends) {
+            // the next rank must have consumed the batch that last used this slot
+            if (q_send >= kSlots) {
+                const uint64_t want = q_send - kSlots + 1;
+                bool ok = ld_acq_local(my_consumed) >= want;
                 if (!__all_sync(kCFull, ok)) {
                     const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
                     bool stop = false;
                     for (uint64_t it = 0; it < cap && !stop; ++it) {
                         if (it >= 1024) __nanosleep(32);
-                        if (!ok) ok = ld_acq_local(flag) == q_recv + 1;
+                        ok = ld_acq_local(my_consumed) >= want;
                         if (__all_sync(kCFull, ok)) break;
                         if ((it & 31) == 31)
                             stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
                                                           ld_rlx_local(S.abort) != 0);
                     }
                     if (!__all_sync(kCFull, ok)) {
-                        if (ld_rlx_local(S.abort) == 0) {
-                            if (!ok) report_flag_timeout(st, r, base + lane);
-                            if (lane == 0) raise_abort<NR>(S);
+                        if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                            report_wait_timeout(st);
+                            raise_abort<NR>(S);
                         }
                         dead = true;
                         break;
                     }
                 }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < kI; ++i) {
-                    const size_t l = base + 4 * i + g;
-                    if (l * kCLineWords < slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
-                }
             }
-            float v[kI][4];
+            const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kCBatchLines * 128);
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
-                v[i][0] = __uint_as_float(w[i].x);
-                v[i][1] = __uint_as_float(w[i].y);
-                v[i][2] = __uint_as_float(w[i].z);
-                v[i][3] = __uint_as_float(w[i].w);
-                if (t <= NR - 1) {
-                    float xv[4];
-                    widen_raw<DT>(xr[i], xv);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) v[i][u] = t == 0 ? xv[u] : v[i][u] + xv[u];
-                }
-                if (t == NR - 1) {   // rounded once; the rounded value is passed on
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) v[i][u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[i][u]));
-                }
+                const size_t l = base + 4 * i + g;
+                if (l * kCLineWords >= G.slice_hi) continue;
+                const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
+                if (j < 7)
+                    st16_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                            __float_as_uint(v[i][2]), __float_as_uint(v[i][3])));
+                else
+                    st8_peer(a, __float_as_uint(v[i][0]), __float_as_uint(v[i][1]));
             }
-            if (t >= 1) {   // this slot is free again: tell the previous rank
-                __syncwarp();
-                if (lane == 0) st_rel_peer(prev_consumed, q_recv + 1);
-                ++q_recv;
-            }
-            if (sends) {
-                // the next rank must have consumed the batch that last used this slot
-                if (q_send >= kSlots) {
-                    const uint64_t want = q_send - kSlots + 1;
-                    bool ok = ld_acq_local(my_consumed) >= want;
-                    if (!__all_sync(kCFull, ok)) {
-                        const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
-                        bool stop = false;
-                        for (uint64_t it = 0; it < cap && !stop; ++it) {
-                            if (it >= 1024) __nanosleep(32);
-                            ok = ld_acq_local(my_consumed) >= want;
-                            if (__all_sync(kCFull, ok)) break;
-                            if ((it & 31) == 31)
-                                stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
-                                                              ld_rlx_local(S.abort) != 0);
-                        }
-                        if (!__all_sync(kCFull, ok)) {
-                            if (lane == 0 && ld_rlx_local(S.abort) == 0) {
-                                report_wait_timeout(st);
-                                raise_abort<NR>(S);
-                            }
-                            dead = true;
-                            break;
-                        }
-                    }
-                }
-                const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kCBatchLines * 128);
+            __syncwarp();
+            fence_cluster();   // releases these lines; also orders this batch's inbox reads
+            if ((base + lane) * kCLineWords < G.slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
+            ++q_send;
+            // this batch's inbox slot is free again (its reads precede the
+            // fence): tell the previous rank.  Published after this rank's
+            // own send, so a step's batches must fit in kSlots - 1 slots.
+            if (t >= 1 && lane == 0) st_rlx_peer(prev_consumed, q_recv + 1);
+        }
+        if (t >= 1) ++q_recv;
+        // this rank's output last, after the hop is on its way
+        if (t >= NR - 1) {
 #pragma unroll
-                for (int i = 0; i < kI; ++i) {
-                    const size_t l = base + 4 * i + g;
-                    if (l * kCLineWords >= slice_hi) continue;
-                    const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
-                    if (j < 7)
-                        st16_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
-                                                __float_as_uint(v[i][2]), __float_as_uint(v[i][3])));
-                    else
-                        st8_peer(a, __float_as_uint(v[i][0]), __float_as_uint(v[i][1]));
-                }
-                __syncwarp();
-                fence_cluster();
-                if ((base + lane) * kCLineWords < slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
-                ++q_send;
-            }
-            // this rank's output last, after the hop is on its way
-            if (t >= NR - 1) {
-#pragma unroll
-                for (int i = 0; i < kI; ++i) {
-                    const size_t l = base + 4 * i + g;
-                    if (l * kCLineWords < slice_hi) store_out<DT>(y, l * kCLineWords + 4 * (size_t)j, nw, len, v[i]);
-                }
+            for (int i = 0; i < kI; ++i) {
+                const size_t l = base + 4 * i + g;
+                if (l * kCLineWords < G.slice_hi) store_out<DT>(G.y, l * kCLineWords + 4 * (size_t)j, nw, G.len, v[i]);
             }
         }
         if (!dead && ld_rlx_local(S.abort) != 0) dead = true;
         dead = __any_sync(kCFull, dead);
+        t = t2;
+        b = b2;
+        G = G2;
     }
     // no CTA leaves while a peer may still write into its shared memory
     cluster_barrier();
@@ -441,9 +471,10 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
             if (resident < 1) return AR_ERR_CUDA;
             const size_t C = chunk_elems(NR, count, DT);
             // slices of at least one batch per warp; one wave of clusters
-            // unless that would give a warp more batches per step than its
-            // receiver has inbox slots: at step 0 every rank sends without
-            // receiving, so a step's batches must fit in the receiver's slots
+            // unless that would give a warp more than kSlots - 1 batches per
+            // step: at step 0 every rank sends without receiving, and a
+            // receiver frees a slot only after its own send of the next
+            // batch, so a step's batches must fit in kSlots - 1 slots
             // (otherwise every rank waits on its successor: a cycle)
             const size_t per_cta_min = kCBatchElems * kCWarps;
             size_t K = (C + per_cta_min - 1) / per_cta_min;
@@ -451,15 +482,14 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
             if (K < 1) K = 1;
             size_t epc = (C + K - 1) / K;
             epc = (epc + kCBatchElems - 1) / kCBatchElems * kCBatchElems;
-            if (epc > kCBatchElems * kCWarps * kSlots) epc = kCBatchElems * kCWarps * kSlots;
+            if (epc > kCBatchElems * kCWarps * (kSlots - 1)) epc = kCBatchElems * kCWarps * (kSlots - 1);
             K = (C + epc - 1) / epc;
             if (K < 1) K = 1;
             cfg.gridDim = dim3((unsigned)(K * NR));
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
             rec_begin(h, s);
             const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_cluster_kernel<NR, DT>, ip, op, C, count, epc,
-                                                       h.spin_ns, h.persist_absent,
-                                                       (int)(S <= (32ull << 20)), h.status);
+                                                       h.spin_ns, h.persist_absent, h.status);
             rec_end(h, s, AR_K_RING_CLUSTER, 2ull * NR * S);
             *launches = 1;
             if (err != cudaSuccess) {
