@@ -147,8 +147,8 @@ enum {
     AR_OPT_PERSISTENT = 13,  /* 1: allocate the LL128 inboxes ar_ring_persistent needs
                                 (two slots per rank, about 4.3 x max_bytes in all);
                                 0 (default): free them */
-    AR_OPT_ABSENT_RANK = 14, /* failure emulation for ar_ring_persistent: rank r (0..n-1)
-                                never joins, so its neighbours' waits run out after
+    AR_OPT_ABSENT_RANK = 14, /* failure emulation for ar_ring_persistent and ar_ring_cluster:
+                                rank r (0..n-1) never joins, so its neighbours' waits run out after
                                 AR_OPT_SPIN_NS and the status reads AR_ERR_FLAG_TIMEOUT or
                                 AR_ERR_WAIT_TIMEOUT; -1 (default): every rank takes part */
     AR_OPT_PDL = 6           /* 1 (default): launch with programmatic stream
