@@ -460,14 +460,16 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
             cfg.stream = s;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            // clusters that fit at once: one wave of them
-            static int resident = -1;
-            if (resident < 0) {
-                cfg.gridDim = dim3((unsigned)(NR * 64));
-                if (cudaOccupancyMaxActiveClusters(&resident, ring_cluster_kernel<NR, DT>, &cfg) != cudaSuccess)
-                    resident = 0;
+            // clusters that fit at once: one wave of them (computed once,
+            // thread-safely, per kernel instantiation)
+            static const int resident = [&] {
+                cudaLaunchConfig_t q = cfg;
+                q.gridDim = dim3((unsigned)(NR * 64));
+                int nc = 0;
+                if (cudaOccupancyMaxActiveClusters(&nc, ring_cluster_kernel<NR, DT>, &q) != cudaSuccess) nc = 0;
                 cudaGetLastError();
-            }
+                return nc;
+            }();
             if (resident < 1) return AR_ERR_CUDA;
             const size_t C = chunk_elems(NR, count, DT);
             // slices of at least one batch per warp; one wave of clusters
