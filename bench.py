@@ -17,6 +17,12 @@ device time.  The 1.3 GiB per-step working set is 10x the 129 MB L2, so no
 flush is needed between steps.  Per-kernel times come from the library's
 own launch record (CUDA events on the launching stream, AR_OPT_TIMING).
 
+Beside the timed steps the JSON line carries: a decode/prefill sweep of
+one-shot and two-shot, the fused all-reduce + RMSNorm epilogue, every
+all-reduce call side by side (variants), the LL payload sweep, the n = 16
+doubling sweep, an end-to-end leg through host buffers (e2e), and the oracle
+timed on the host (cpu_baseline, cpu_parallel, cpu_calls).
+
 --impl reference times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload.  Multi-GPU runs (torchrun) are
 independent replicas: the path has no exchange between GPUs.
@@ -535,7 +541,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
     """Every all-reduce call of the library on the same n = 8 bf16 buffers, at
     64 KiB, 1 MiB, 8 MiB and 64 MiB per rank: one-shot, its push and copy-in
     forms, two-shot, the ring (one launch per step), the ring with hop
-    rounding, the persistent single-launch LL128 ring and the pairwise tree.
+    rounding, the persistent single-launch LL128 ring (global-memory inboxes,
+    and over a thread-block cluster) and the pairwise tree.
     Timing as in `sweep` (back-to-back calls on rotating slots, one event pair
     per batch, median of the batches); bytes are each call's algorithmic HBM
     bytes (ar_plan)."""
