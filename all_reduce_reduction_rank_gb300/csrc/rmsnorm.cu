@@ -13,8 +13,10 @@
 // Layout: one thread-block cluster of kClusterCtas CTAs per token row; CTA c
 // of the cluster owns a contiguous slice of the row.  Pass 1 reads the n rank
 // slices once, writes r, keeps r (fp32) in shared memory and accumulates its
-// squares; the CTAs' partial sums are combined in a fixed order through
-// distributed shared memory; pass 2 scales r and writes every rank's output.
+// squares; each CTA pushes its partial sum into every CTA's shared memory
+// (distributed shared memory), one cluster barrier, and every CTA adds the
+// partials in the same fixed order; pass 2 scales r and writes every rank's
+// output.
 // HBM: reads n S + S (+ the weight, H per launch), writes n S + S.
 #include "common.cuh"
 
@@ -38,16 +40,14 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// A float in CTA `cta`'s shared memory, at the offset of `local` in ours.
-__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t cta)
+// Write v to CTA `cta`'s shared memory, at the offset of `local` in ours.
+__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t cta, float v)
 {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                  : "=r"(remote)
                  : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(cta));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 template <int NR, int DT>
@@ -59,8 +59,11 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     constexpr int VE = kVecElems<DT>;
     extern __shared__ float r_slice[];                 // slice_vecs * VE floats
     __shared__ float warp_part[kNormThreads / 32];
-    __shared__ float cta_part;
+    __shared__ float parts[kClusterCtas];   // every CTA's sum of squares, pushed by that CTA
     __shared__ float row_inv;
+    // the first half of a cluster barrier: the wait before the partial sums
+    // are pushed makes sure every CTA of the cluster has started
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_acquire();
     const uint32_t c = cluster_ctarank();
     const size_t t = blockIdx.x / kClusterCtas;        // token row of this cluster
@@ -69,14 +72,18 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     const size_t v_hi = v_lo + slice_vecs < nvec_row ? v_lo + slice_vecs : nvec_row;
     const size_t row = t * nvec_row;                   // first 16-byte vector of the row
 
-    // pass 1: all-reduce, residual add, squares
+    // pass 1: all-reduce, residual add, squares.  Every load of a vector --
+    // the n ranks', the residual's and (for pass 2) the weight's -- is issued
+    // before any is used, so the pass waits on memory once.
     float ss = 0.0f;
+    uint4 w_first = make_uint4(0u, 0u, 0u, 0u);   // the weight of this thread's first vector
     for (size_t v = v_lo + threadIdx.x; v < v_hi; v += kNormThreads) {
         uint4 x[NR];
 #pragma unroll
         for (int q = 0; q < NR; ++q) x[q] = ld16(static_cast<const uint4*>(in.p[q]) + row + v);
-        const uint4 a = reduce_rank_order<DT, NR>(x);
         const uint4 res = ld16(static_cast<const uint4*>(residual) + row + v);
+        if (v == v_lo + threadIdx.x) w_first = ld16(static_cast<const uint4*>(weight) + v);
+        const uint4 a = reduce_rank_order<DT, NR>(x);
         float af[VE], rf[VE];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -102,25 +109,26 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     for (int o = 16; o > 0; o >>= 1) ss = ss + __shfl_down_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = ss;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (threadIdx.x == 0) {   // this CTA's partial, pushed into every CTA of the cluster
         float s = 0.0f;
         for (int w = 0; w < kNormThreads / 32; ++w) s = s + warp_part[w];
-        cta_part = s;
+        for (uint32_t k = 0; k < kClusterCtas; ++k) st_cluster_f32(&parts[c], k, s);
     }
-    // the row's: the cluster's CTAs in order, read from their shared memory
+    // one barrier: every push has landed, and none is left to land after it
     cluster_sync();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // the row's: the cluster's CTAs in order
         float s = 0.0f;
-        for (uint32_t k = 0; k < kClusterCtas; ++k) s = s + ld_cluster_f32(&cta_part, k);
+        for (uint32_t k = 0; k < kClusterCtas; ++k) s = s + parts[k];
         row_inv = 1.0f / sqrtf(s / (float)hidden + eps);
     }
-    cluster_sync();  // every CTA has read every partial before any CTA may exit
+    __syncthreads();
     pdl_release();
     const float inv = row_inv;
 
     // pass 2: scale, weight, round, write every rank's output
     for (size_t v = v_lo + threadIdx.x; v < v_hi; v += kNormThreads) {
-        const uint4 wv = ld16(static_cast<const uint4*>(weight) + v);
+        const uint4 wv = v == v_lo + threadIdx.x ? w_first : ld16(static_cast<const uint4*>(weight) + v);
         float wf[VE], y[VE];
 #pragma unroll
         for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(wv, j), wf + j * Payload<DT>::kPerWord);
