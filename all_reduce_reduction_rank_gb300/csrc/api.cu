@@ -384,7 +384,7 @@ const char* ar_strerror(int code)
     case AR_ERR_TOO_LARGE: return "count x element size exceeds max_bytes";
     case AR_ERR_CUDA: return "CUDA runtime error";
     case AR_ERR_FLAG_TIMEOUT: return "LL/LL128 flag not seen within the spin limit";
-    case AR_ERR_WAIT_TIMEOUT: return "a kernel's bounded wait for its bulk copies ran out";
+    case AR_ERR_WAIT_TIMEOUT: return "a kernel's bounded wait (its bulk copies, or a peer freeing a slot) ran out";
     default: return "unknown error code";
     }
 }
