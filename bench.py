@@ -535,6 +535,7 @@ def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
 
 
 VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
+E2E_SETS = 3   # device buffer sets the e2e leg rotates over
 
 
 def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
@@ -605,14 +606,14 @@ def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     copies its inputs from pinned host memory, runs, and reads its results
     (the n all-reduced buffers and the n LL and LL128 unpacked payloads) back.
 
-    Steps alternate between two device buffer sets, each with its own stream
+    Steps rotate over E2E_SETS device buffer sets, each with its own stream
     (copy in -> the step's calls -> copy out, in order on that stream), so
-    one step's copies overlap the other set's calls and copies in the other
+    one step's copies overlap the other sets' calls and copies in the other
     direction; every step still moves all of its own bytes in and out."""
     import torch
     n = wl.n
-    wl2 = Workload(n, wl.S, wl.ll_count, wl.dev, seed=1004)
-    sets = (wl, wl2)
+    extra = [Workload(n, wl.S, wl.ll_count, wl.dev, seed=1004 + i) for i in range(E2E_SETS - 1)]
+    sets = (wl, *extra)
     h_in = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.ins]
     h_pay = [torch.empty_like(t, device="cpu").pin_memory() for t in wl.pay]
     for h, d in zip(h_in + h_pay, wl.ins + wl.pay):
@@ -623,7 +624,7 @@ def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     d2h = sum(t.numel() * t.element_size() for t in h_outs[0])
 
     def one(i):
-        w, hout = sets[i % 2], h_outs[i % 2]
+        w, hout = sets[i % len(sets)], h_outs[i % len(sets)]
         with torch.cuda.stream(w.stream):
             for h, d in zip(h_in + h_pay, w.ins + w.pay):
                 d.copy_(h, non_blocking=True)
@@ -631,30 +632,33 @@ def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
             for h, d in zip(hout, w.outs + w.ll_dst + w.l128_dst):
                 h.copy_(d, non_blocking=True)
 
-    one(0)
-    one(1)
+    for i in range(len(sets)):
+        one(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     ev0.record(wl.stream)
-    wl2.stream.wait_event(ev0)
+    for w in extra:
+        w.stream.wait_event(ev0)
     for i in range(K):
         one(i)
-    done2 = torch.cuda.Event()
-    done2.record(wl2.stream)
-    wl.stream.wait_event(done2)
+    for w in extra:
+        done = torch.cuda.Event()
+        done.record(w.stream)
+        wl.stream.wait_event(done)
     ev1.record(wl.stream)
     torch.cuda.synchronize()
     import all_reduce_reduction_rank_gb300 as ar
     for w in sets:
         ar.check(ar.ar_status(w.h), "e2e status")
-    wl2.close()
+    for w in extra:
+        w.close()
     ms = reduce_scalar(ev0.elapsed_time(ev1), "max") / K
     world = dist_env()[1]
     return {"value": round(world * bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelining": "2 buffer sets on 2 streams: copy in, calls, copy out per step"}
+            "pipelining": f"{E2E_SETS} buffer sets on {E2E_SETS} streams: copy in, calls, copy out per step"}
 
 
 def run_ours(args):
