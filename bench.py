@@ -364,10 +364,14 @@ def sweep(wl, peak: float, batches: int = 7, min_calls: int = 64) -> dict:
             ms = statistics.median(per_call)
             gbs = b / (ms * 1e-3) / 1e9
             algbw = S / (ms * 1e-3) / 1e9
-            res[algo].append({"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
-                              "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
-                              "busbw_GB/s": round(algbw * 2 * (n - 1) / n, 1), "calls_per_batch": calls,
-                              "batches": batches})
+            row = {"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
+                   "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
+                   "busbw_GB/s": round(algbw * 2 * (n - 1) / n, 1), "calls_per_batch": calls, "batches": batches}
+            if S <= GRAPH_MAX_BYTES:
+                row["graph_us"] = round(_graph_us(wl.stream, lambda i: call(wl.h, pin[i % slots], pout[i % slots],
+                                                                            N, 1, wl.s)), 3)
+                ar.check(ar.ar_status(wl.h), algo)
+            res[algo].append(row)
     return res
 
 
@@ -415,6 +419,7 @@ def fused_epilogue(wl, peak: float, batches: int = 7, calls: int = 200) -> list:
                 b = (2 * n + 2) * S + H * 2 if name == "fused" else 2 * n * S
                 row[name + "_us"] = round(us, 3)
                 row[name + "_GB/s"] = round(b / (us * 1e-6) / 1e9, 1)
+                row[name + "_graph_us"] = round(_graph_us(wl.stream, lambda i: call(i % slots)), 3)
             ar.check(ar.ar_status(wl.h), "fused epilogue")
             out.append(row)
     return out
@@ -434,6 +439,36 @@ def _batched_us(stream, fn, calls: int, batches: int) -> float:
         e1.synchronize()
         per.append(e0.elapsed_time(e1) / calls)
     return statistics.median(per) * 1e3
+
+
+GRAPH_MAX_BYTES = 8 * MiB   # messages up to this size are also timed from a CUDA graph
+
+
+def _graph_us(stream, fn, in_graph: int = 20, replays: int = 10, batches: int = 5) -> float:
+    """Device time per call with the host out of the way: `in_graph` calls
+    fn(i) captured once into a CUDA graph on `stream`, replayed back to back;
+    median over batches, us.  Small calls issued one by one from Python are
+    bound by the host's issue rate (ctypes + launch, ~3 us a call on the
+    GPU machine's Grace CPU), which the replay removes."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(in_graph):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(batches):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(replays):
+                g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e3 / (in_graph * replays))
+    del g
+    return statistics.median(per)
 
 
 def ll_sweep(wl, peak: float, batches: int = 5) -> dict:
@@ -593,9 +628,14 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
             ms = statistics.median(per_call)
             gbs = b / (ms * 1e-3) / 1e9
             algbw = S / (ms * 1e-3) / 1e9
-            res[name].append({"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
-                              "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
-                              "launches": t.launches, "calls_per_batch": calls})
+            row = {"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
+                   "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
+                   "launches": t.launches, "calls_per_batch": calls}
+            if S <= GRAPH_MAX_BYTES:
+                row["graph_us"] = round(_graph_us(wl.stream, lambda i: call(h, pin[i % slots], pout[i % slots],
+                                                                            N, 1, wl.s)), 3)
+                ar.check(ar.ar_status(h), name)
+            res[name].append(row)
     for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
         ar.check(ar.ar_set_option(h, opt, 0), "variant buffers")
     return res
