@@ -63,7 +63,7 @@ int check_multi(int op, int n, size_t max_bytes, const void* const* in, void* co
     if (n < 2 || n > kMaxRanks) return AR_ERR_INVALID;
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
     if (is_ll_op(op) && dt != AR_F32) return AR_ERR_INVALID;
-    if (op == AR_OP_TREE && (n & (n - 1))) return AR_ERR_INVALID;
+    if ((op == AR_OP_TREE || op == AR_OP_TREE_FUSED) && (n & (n - 1))) return AR_ERR_INVALID;
     if (!in || !out) return AR_ERR_INVALID;
     for (int r = 0; r < n; ++r)
         if (!in[r] || !out[r]) return AR_ERR_INVALID;
@@ -209,6 +209,16 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         t->launches = count ? 1 : 0;
         t->hbm_read_bytes = nn * S + (2 * nn - 2) * 128 * lines;
         t->hbm_write_bytes = nn * S + (2 * nn - 2) * 128 * lines;
+        break;
+    }
+    case AR_OP_TREE_FUSED: {
+        int levels = 0;
+        while ((1 << levels) < n) ++levels;
+        t->link_bytes_per_rank = (double)levels * (double)S;
+        t->steps = levels;
+        t->launches = count ? 1 : 0;
+        t->hbm_read_bytes = nn * S;
+        t->hbm_write_bytes = nn * S;
         break;
     }
     case AR_OP_RING_CLUSTER:
@@ -395,11 +405,11 @@ size_t ar_ll128_bytes(size_t payload_bytes) { return 128u * ((payload_bytes + 11
 
 int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
 {
-    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_RING_CLUSTER) return AR_ERR_INVALID;
+    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_TREE_FUSED) return AR_ERR_INVALID;
     const bool multi =
         op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE || op >= AR_OP_ALLREDUCE_RMSNORM;
     if (multi && (n_ranks < 2 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;
-    if (op == AR_OP_TREE && (n_ranks & (n_ranks - 1))) return AR_ERR_INVALID;
+    if ((op == AR_OP_TREE || op == AR_OP_TREE_FUSED) && (n_ranks & (n_ranks - 1))) return AR_ERR_INVALID;
     if (!multi && (n_ranks < 1 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;  // buffers packed
     if (dt != AR_F32 && dt != AR_BF16 && dt != AR_F16) return AR_ERR_INVALID;
     plan(op, n_ranks, count, dt, t);
@@ -415,7 +425,7 @@ int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in, 
     }
     if (op != AR_OP_ONE_SHOT && op != AR_OP_TWO_SHOT && op != AR_OP_RING && op != AR_OP_ONE_SHOT_PUSH &&
         op != AR_OP_ONE_SHOT_COPYIN && op != AR_OP_RING_ROUNDED && op != AR_OP_TREE &&
-        op != AR_OP_RING_PERSISTENT && op != AR_OP_RING_CLUSTER && !is_ll_op(op))
+        op != AR_OP_RING_PERSISTENT && op != AR_OP_RING_CLUSTER && op != AR_OP_TREE_FUSED && !is_ll_op(op))
         return AR_ERR_INVALID;
     return check_multi(op, n_ranks, max_bytes, in, out, count, dt);
 }
@@ -574,6 +584,11 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
 int ar_one_shot(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
 {
     return all_reduce_call(AR_OP_ONE_SHOT, launch_one_shot, h, in, out, count, dt, s);
+}
+
+int ar_tree_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
+{
+    return all_reduce_call(AR_OP_TREE_FUSED, launch_tree_fused, h, in, out, count, dt, s);
 }
 
 int ar_ring_cluster(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)

@@ -145,6 +145,8 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
 int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                            cudaStream_t s, int* launches);
 size_t persist_bytes(int n, size_t max_bytes, int sm_count);
+int launch_tree_fused(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                      int* launches);
 int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
                         int* launches);
 uint64_t persist_lines_per_step(int n, size_t count, int dt);

@@ -95,3 +95,109 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
 }
 
 }  // namespace argb
+
+// ---------------------------------------------------------------------------
+// The same tree with every level done in registers, in one pass.
+//
+// The levels have no dependency across elements, so on one GPU a thread can
+// load the n ranks' values of its 16-byte vector once, run all log2(n)
+// pairwise levels on them (the same pairs, the same binary32 adds, the same
+// rounding to the payload type after every level), and store the n results:
+// HBM reads n S and writes n S, as one-shot does, instead of log2(n) times
+// that.  Same bits as the level-by-level tree.
+namespace argb {
+namespace {
+
+template <int NR, int DT>
+__global__ void __launch_bounds__(kThreads)
+tree_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
+                  size_t count)
+{
+    pdl_acquire();
+    using T = typename Payload<DT>::scalar_t;
+    constexpr int P = Payload<DT>::kPerWord;   // elements per 32-bit word
+    constexpr int VE = kVecElems<DT>;
+    // all levels over one value per rank, rounded after each level
+    auto levels = [](float (&f)[NR]) {
+#pragma unroll
+        for (int d = 1; d < NR; d <<= 1) {
+            float g[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) g[r] = Payload<DT>::widen1(Payload<DT>::narrow1(f[r] + f[r ^ d]));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) f[r] = g[r];
+        }
+    };
+    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+        uint4 x[NR];
+#pragma unroll
+        for (int q = 0; q < NR; ++q) x[q] = ld16(static_cast<const uint4*>(in.p[q]) + v);
+        uint32_t y[NR][4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            float e[NR][P];
+#pragma unroll
+            for (int q = 0; q < NR; ++q) Payload<DT>::widen(word(x[q], w), e[q]);
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                float f[NR];
+#pragma unroll
+                for (int q = 0; q < NR; ++q) f[q] = e[q][k];
+                levels(f);
+#pragma unroll
+                for (int q = 0; q < NR; ++q) e[q][k] = f[q];
+            }
+#pragma unroll
+            for (int q = 0; q < NR; ++q) y[q][w] = Payload<DT>::narrow(e[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < NR; ++q)
+            st16(static_cast<uint4*>(out.p[q]) + v, make_uint4(y[q][0], y[q][1], y[q][2], y[q][3]));
+    }
+    pdl_release();
+    if (blockIdx.x == gridDim.x - 1) {   // the ragged tail (< VE elements)
+        const size_t i = nvec * VE + threadIdx.x;
+        if (i < count) {
+            float f[NR];
+#pragma unroll
+            for (int q = 0; q < NR; ++q) f[q] = Payload<DT>::widen1(static_cast<const T*>(in.p[q])[i]);
+            levels(f);
+#pragma unroll
+            for (int q = 0; q < NR; ++q) static_cast<T*>(out.p[q])[i] = Payload<DT>::narrow1(f[q]);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_tree_fused(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                      int* launches)
+{
+    if (h.n & (h.n - 1)) return AR_ERR_INVALID;
+    return dispatch_dtype(dt, [&](auto dtc) -> int {
+        constexpr int DT = decltype(dtc)::value;
+        return dispatch_ranks(h.n, [&](auto nrc) -> int {
+            constexpr int NR = decltype(nrc)::value;
+            if constexpr ((NR & (NR - 1)) != 0) {
+                return AR_ERR_INVALID;
+            } else {
+                CPtrs<NR> ip;
+                MPtrs<NR> op;
+                for (int q = 0; q < NR; ++q) {
+                    ip.p[q] = in[q];
+                    op.p[q] = out[q];
+                }
+                const size_t nvec = count / kVecElems<DT>;
+                const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+                rec_begin(h, s);
+                launch_kernel(h, tree_fused_kernel<NR, DT>, dim3(grid_for(h, nvec)), kThreads, 0, s, ip, op, nvec,
+                              count);
+                rec_end(h, s, AR_K_TREE_FUSED, 2ull * NR * S);
+                *launches = 1;
+                return launch_status();
+            }
+        });
+    });
+}
+
+}  // namespace argb

@@ -122,7 +122,7 @@ KERNEL_SOURCES = {
     "ll128_pack": ["ll.cu"], "ll128_unpack": ["ll.cu"], "ll128_reduce": ["ll.cu"],
     "allreduce_rmsnorm": ["rmsnorm.cu"], "push": ["one_shot_modes.cu"], "push_reduce": ["one_shot_modes.cu"],
     "copyin": ["one_shot_modes.cu"], "ring_rs_step_rounded": ["ring.cu"], "tree_level": ["tree.cu"],
-    "ring_persistent": ["ring_persistent.cu"], "ring_cluster": ["ring_cluster.cu"],
+    "ring_persistent": ["ring_persistent.cu"], "ring_cluster": ["ring_cluster.cu"], "tree_fused": ["tree.cu"],
 }
 
 
@@ -599,7 +599,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
              ("ring_rounded", L.ar_ring_rounded, ar.AR_OP_RING_ROUNDED),
              ("ring_persistent", L.ar_ring_persistent, ar.AR_OP_RING_PERSISTENT),
              ("ring_cluster", L.ar_ring_cluster, ar.AR_OP_RING_CLUSTER),
-             ("tree", L.ar_tree, ar.AR_OP_TREE))
+             ("tree", L.ar_tree, ar.AR_OP_TREE),
+             ("tree_fused", L.ar_tree_fused, ar.AR_OP_TREE_FUSED))
     res = {a[0]: [] for a in algos}
     for S in VARIANT_SIZES:
         if S > wl.S:
@@ -930,7 +931,8 @@ def calls_cpu(min_seconds: float = 0.5) -> dict:
                          ("ring_rounded", lambda: oracle.ring_rounded(xs, "bf16"), ar.AR_OP_RING_ROUNDED),
                          ("ring_persistent", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_PERSISTENT),
                          ("ring_cluster", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_CLUSTER),
-                         ("tree", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE)):
+                         ("tree", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE),
+                         ("tree_fused", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE_FUSED)):
         t = ar.ar_plan(op, n, N, "bf16")
         sec = timed(fn)
         rows[name] = {"bytes_per_rank": 2 * N, "ms": round(sec * 1e3, 3),

@@ -87,7 +87,8 @@ typedef enum {
     AR_OP_RING_ROUNDED = 13,
     AR_OP_TREE = 14,
     AR_OP_RING_PERSISTENT = 15,
-    AR_OP_RING_CLUSTER = 16
+    AR_OP_RING_CLUSTER = 16,
+    AR_OP_TREE_FUSED = 17
 } ar_op;
 
 /* Traffic of one call.
@@ -177,7 +178,8 @@ typedef enum {
     AR_K_TREE_LEVEL = 16,           /* one level of ar_tree */
     AR_K_RING_PERSISTENT = 17,      /* ar_ring_persistent (all steps) */
     AR_K_COPYIN = 18,               /* ar_one_shot_copyin's copy into the registered buffers */
-    AR_K_RING_CLUSTER = 19          /* ar_ring_cluster (all steps) */
+    AR_K_RING_CLUSTER = 19,         /* ar_ring_cluster (all steps) */
+    AR_K_TREE_FUSED = 20            /* ar_tree_fused (all levels) */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -281,6 +283,14 @@ int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t
  * may differ from one-shot's by the levels' roundings, for fp32 by the order
  * of the adds.  log2(n) launches; HBM per level: n S read, n S written. */
 int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t stream);
+
+/* The pairwise tree of ar_tree with all log2(n) levels done in registers in
+ * one pass: each thread loads the n ranks' values of a 16-byte vector once,
+ * applies every level (the same pairs, adds and roundings) and stores the n
+ * results.  Same bits as ar_tree; one launch; HBM reads n S, writes n S (the
+ * level-by-level form moves log2(n) times that). */
+int ar_tree_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                  ar_stream_t stream);
 
 /* The ring of ar_ring in a single (cooperative) launch, each hop carried as
  * LL128 lines: 120 bytes of fp32 words and an 8-byte step flag per 128 bytes
@@ -466,7 +476,7 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
 /* Host only, no GPU needed: the code a call would return for these
  * arguments before launching anything.  op AR_OP_ONE_SHOT, AR_OP_TWO_SHOT,
  * AR_OP_RING, AR_OP_ONE_SHOT_PUSH, AR_OP_ONE_SHOT_COPYIN, AR_OP_RING_ROUNDED,
- * AR_OP_TREE (n_ranks a power of two), AR_OP_RING_PERSISTENT, AR_OP_RING_CLUSTER,
+ * AR_OP_TREE and AR_OP_TREE_FUSED (n_ranks a power of two), AR_OP_RING_PERSISTENT, AR_OP_RING_CLUSTER,
  * AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls (n_ranks in
  * [2, 16]; the handle's optional buffers are not checked); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
  * AR_OP_LL128_UNPACK: the batched pack / unpack calls over n_ranks buffers

@@ -102,7 +102,7 @@ def test_plan_batched_pack_scales_with_buffers(lib, nb):
 
 
 def test_plan_rejects_bad_arguments(lib):
-    bad = [(0, 8), (ar.AR_OP_RING_CLUSTER + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
+    bad = [(0, 8), (ar.AR_OP_TREE_FUSED + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
            (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]
     for op, n in bad:
         with pytest.raises(ar.ArError):
@@ -336,3 +336,13 @@ def test_plan_ring_cluster(lib, n):
     assert (t.hbm_read_bytes, t.hbm_write_bytes) == (n * 2 * N, n * 2 * N)
     assert t.steps == 2 * (n - 1) and t.launches == 1
     assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16])
+def test_plan_tree_fused(lib, n):
+    N = 4099
+    t = ar.ar_plan(ar.AR_OP_TREE_FUSED, n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (n * 2 * N, n * 2 * N)
+    assert t.steps == n.bit_length() - 1 and t.launches == 1
+    with pytest.raises(ar.ArError):
+        ar.ar_plan(ar.AR_OP_TREE_FUSED, 6, N, "bf16")

@@ -411,7 +411,7 @@ def test_tree_in_place_hand_worked_and_refusals():
 
 @pytest.mark.parametrize("call,oracle_fn", [
     ("ar_one_shot_push", "all_reduce"), ("ar_one_shot_copyin", "all_reduce"), ("ar_ring_rounded", "ring_rounded"),
-    ("ar_tree", "tree"), ("ar_ring_persistent", "ring"), ("ar_ring_cluster", "ring")])
+    ("ar_tree", "tree"), ("ar_tree_fused", "tree"), ("ar_ring_persistent", "ring"), ("ar_ring_cluster", "ring")])
 def test_cuda_graph_capture_of_the_other_calls(call, oracle_fn):
     # captured once, replayed on new contents of the same buffers
     n, N = 8, 65536 + 3
@@ -434,3 +434,39 @@ def test_cuda_graph_capture_of_the_other_calls(call, oracle_fn):
             for r in (0, 5):
                 np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
         assert ar.ar_status(h) == ar.AR_OK
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 9), (4, 1000), (8, 4099), (8, 300_001), (16, 65536 + 3), (16, 7)])
+def test_tree_fused_matches_the_tree(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=9 * n + N)
+    want = oracle.tree(xs, dtype)
+    ins = upload_ranks(xs)
+    a, b = empty_ranks(n, xs[0].nbytes), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype])) as h:
+        assert ar.ar_tree_fused(h, ptrs(ins), ptrs(a), N, dtype) == ar.AR_OK
+        t = ar.ar_traffic(h)
+        assert t.op == ar.AR_OP_TREE_FUSED and t.launches == 1
+        assert ar.ar_tree(h, ptrs(ins), ptrs(b), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for r in range(n):
+        got = a[r].download(payload_np_dtype(dtype))
+        np.testing.assert_array_equal(bits(got), bits(want[r]))
+        np.testing.assert_array_equal(bits(got), bits(b[r].download(payload_np_dtype(dtype))))
+    for buf in ins + a + b:
+        assert buf.guards_intact()
+
+
+def test_tree_fused_in_place_and_refusal():
+    b = lambda v: oracle.f32_to_bf16(np.full(40, v, np.float32))
+    ins = upload_ranks([b(256.0), b(1.0), b(1.0), b(0.0)])
+    with Handle(4, 80) as h:
+        assert ar.ar_tree_fused(h, ptrs(ins), ptrs(ins), 40, "bf16") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for x in ins:
+        np.testing.assert_array_equal(oracle.bf16_to_f32(x.download(np.uint16)), np.full(40, 256.0, np.float32))
+    with Handle(6, 64) as h:
+        i6, o6 = empty_ranks(6, 64), empty_ranks(6, 64)
+        assert ar.ar_tree_fused(h, ptrs(i6), ptrs(o6), 16, "bf16") == ar.AR_ERR_INVALID

@@ -24,6 +24,7 @@ CALLS = {
     "copyin": (ar.ar_one_shot_copyin, oracle.all_reduce),
     "ring_rounded": (ar.ar_ring_rounded, oracle.ring_rounded),
     "tree": (ar.ar_tree, oracle.tree),
+    "tree_fused": (ar.ar_tree_fused, oracle.tree),
     "ring_persistent": (ar.ar_ring_persistent, oracle.ring),
     "ring_cluster": (ar.ar_ring_cluster, oracle.ring),
 }
@@ -46,7 +47,7 @@ def test_every_call_on_a_random_case(i, n, N, dtype):
     ins = upload_ranks(xs)
     with Handle(n, max(16, N * E[dtype]), push_staging=1, registered=1, persistent=1) as h:
         for name, (call, ref) in CALLS.items():
-            if name == "tree" and n & (n - 1):
+            if name in ("tree", "tree_fused") and n & (n - 1):
                 assert call(h, ptrs(ins), ptrs(empty_ranks(n, xs[0].nbytes)), N, dtype) == ar.AR_ERR_INVALID
                 continue
             outs = empty_ranks(n, xs[0].nbytes)
