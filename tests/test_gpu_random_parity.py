@@ -63,3 +63,41 @@ def test_every_call_on_a_random_case(i, n, N, dtype):
                 assert b.guards_intact(), name
         for b in ins:
             assert b.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_every_call_with_signed_zeros_infinities_and_nans(dtype):
+    # special values at scattered positions: every finite or infinite output
+    # matches the oracle of that call bit for bit, every NaN output is NaN
+    # there too (NaN payloads are not compared: IEEE leaves them open)
+    n, N = 8, 20_011
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=4242)
+    f = [oracle.to_f32(x, dtype).copy() for x in xs]
+    f[0][::5] = -0.0
+    f[1][::5] = -0.0          # all ranks -0 at some positions: the rings keep -0, one-shot gives +0
+    for r in range(2, n):
+        f[r][::5] = -0.0
+    f[3][1::17] = np.inf
+    f[5][2::19] = -np.inf
+    f[6][3::23] = np.nan
+    if dtype == "bf16":
+        xs = [oracle.f32_to_bf16(a) for a in f]
+    elif dtype == "f16":
+        xs = [oracle.f32_to_f16(a) for a in f]
+    else:
+        xs = [a.astype(np.float32) for a in f]
+    ins = upload_ranks(xs)
+    with Handle(n, N * E[dtype], push_staging=1, registered=1, persistent=1) as h:
+        for name, (call, ref) in CALLS.items():
+            outs = empty_ranks(n, xs[0].nbytes)
+            rc = call(h, ptrs(ins), ptrs(outs), N, dtype)
+            assert rc == ar.AR_OK, (name, ar.ar_strerror(rc))
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK, name
+            want = ref(xs, dtype)
+            for r in (0, 7):
+                got = outs[r].download(payload_np_dtype(dtype))
+                gf, wf = oracle.to_f32(got, dtype), oracle.to_f32(want[r], dtype)
+                assert np.array_equal(np.isnan(gf), np.isnan(wf)), name
+                keep = ~np.isnan(wf)
+                np.testing.assert_array_equal(bits(got)[keep], bits(want[r])[keep], err_msg=f"{name} rank {r}")
