@@ -40,18 +40,17 @@
 // AR_ERR_WAIT_TIMEOUT (a slot) and raises the abort word of every CTA of the
 // cluster, on which the other waits give up; all threads still reach the
 // final cluster barrier.
-#include "common.cuh"
+#include "lines.cuh"
 
 namespace argb {
 namespace {
 
+using namespace lines;
+
 constexpr int kCWarps = kThreads / 32;
-constexpr int kCLineWords = 30;
-constexpr int kCBatchLines = 32;
-constexpr size_t kCBatchElems = (size_t)kCLineWords * kCBatchLines;   // 960
 constexpr int kSlots = 3;                                                 // inbox slots per warp
 constexpr unsigned kCFull = 0xffffffffu;
-constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kCBatchLines * 128;
+constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kBatchLines * 128;
 // inbox, then consumed[kCWarps] and the abort word, rounded to 16 bytes
 constexpr size_t kClusterSmem = kInboxBytes + ((kCWarps + 1) * sizeof(uint64_t) + 15) / 16 * 16;
 
@@ -109,96 +108,6 @@ __device__ __forceinline__ void st_rlx_peer(uint32_t a, uint64_t v)
 
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
-__device__ __forceinline__ uint2 ldg8(const void* p)
-{
-    uint2 v;
-    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ldg4(const void* p)
-{
-    uint32_t v;
-    asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// Raw words of elements e .. e+nw-1 of a chunk of `len` elements (zero past
-// len): 4 fp32 words, or 2 words of two 16-bit elements.
-template <int DT> constexpr int kCRaw = DT == AR_F32 ? 4 : 2;
-
-template <int DT>
-__device__ __forceinline__ void load_raw(const void* chunk, size_t e, int nw, size_t len, uint32_t* w)
-{
-    using T = typename Payload<DT>::scalar_t;
-    const T* x = static_cast<const T*>(chunk);
-    if (e + (size_t)nw <= len) {
-        if constexpr (DT == AR_F32) {
-            const uint2 a = ldg8(x + e);
-            w[0] = a.x;
-            w[1] = a.y;
-            w[2] = w[3] = 0u;
-            if (nw == 4) {
-                const uint2 b = ldg8(x + e + 2);
-                w[2] = b.x;
-                w[3] = b.y;
-            }
-        } else {
-            w[0] = ldg4(x + e);
-            w[1] = nw == 4 ? ldg4(x + e + 2) : 0u;
-        }
-    } else {
-        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(chunk);
-        const uint32_t* x32 = reinterpret_cast<const uint32_t*>(chunk);
-#pragma unroll
-        for (int u = 0; u < kCRaw<DT>; ++u) w[u] = 0u;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (u < nw && e + u < len) {
-                if constexpr (DT == AR_F32) w[u] = x32[e + u];
-                else w[u >> 1] |= (uint32_t)x16[e + u] << (16 * (u & 1));
-            }
-        }
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ void widen_raw(const uint32_t* w, float* f)
-{
-    if constexpr (DT == AR_F32) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) f[u] = __uint_as_float(w[u]);
-    } else {
-        Payload<DT>::widen(w[0], f);
-        Payload<DT>::widen(w[1], f + 2);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ void store_out(void* chunk, size_t e, int nw, size_t len, const float* f)
-{
-    using T = typename Payload<DT>::scalar_t;
-    T* y = static_cast<T*>(chunk);
-    if (e + (size_t)nw <= len) {
-#pragma unroll
-        for (int u = 0; u < 4; u += 2) {
-            if (u >= nw) break;
-            if constexpr (DT == AR_F32) {
-                asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(y + e + u), "r"(__float_as_uint(f[u])),
-                             "r"(__float_as_uint(f[u + 1]))
-                             : "memory");
-            } else {
-                const uint32_t w = Payload<DT>::narrow(f + u);
-                asm volatile("st.global.u32 [%0], %1;" ::"l"(y + e + u), "r"(w) : "memory");
-            }
-        }
-    } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (u < nw && e + u < len) y[e + u] = Payload<DT>::narrow1(f[u]);
-    }
-}
-
 struct ClusterSmem {
     uint32_t inbox;      // shared address of this CTA's inbox
     uint32_t consumed;   // shared address of consumed[0]
@@ -219,7 +128,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                     size_t count, size_t epc, int64_t spin_ns, int absent, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
-    constexpr int kI = kCBatchLines / 4;
+    constexpr int kI = kBatchLines / 4;
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t crank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
@@ -241,8 +150,8 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     cluster_barrier();
 
     const size_t slice_lo = k * epc;
-    const size_t line_lo = slice_lo / kCLineWords;
-    const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kCBatchLines * 128);
+    const size_t line_lo = slice_lo / kLineWords;
+    const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kBatchLines * 128);
     const uint32_t peer_box = peer_addr(my_box, (uint32_t)d);                    // the next rank's inbox for this warp
     const uint32_t my_consumed = S.consumed + 8 * warp;                            // written by the next rank
     const uint32_t prev_consumed = peer_addr(S.consumed + 8 * warp, (uint32_t)p);  // the previous rank's copy
@@ -262,8 +171,8 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         Geom G;
         G.len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
         G.slice_hi = slice_lo + epc < G.len ? slice_lo + epc : G.len;
-        const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kCLineWords - 1) / kCLineWords : 0;
-        G.nbatch = (nlines + kCBatchLines - 1) / kCBatchLines;
+        const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
+        G.nbatch = (nlines + kBatchLines - 1) / kBatchLines;
         G.x = static_cast<const T*>(in.p[r]) + lo;
         G.y = static_cast<T*>(out.p[r]) + lo;
         return G;
@@ -278,14 +187,14 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         }
     };
     // the rank's own elements of a batch: issued early, used later
-    uint32_t xr[kI][kCRaw<DT>];
+    uint32_t xr[kI][kRawWords<DT>];
     auto load_x = [&](int t, size_t b, const Geom& G) {
         if (t > NR - 1) return;
-        const size_t base = line_lo + b * kCBatchLines;
+        const size_t base = line_lo + b * kBatchLines;
 #pragma unroll
         for (int i = 0; i < kI; ++i) {
             const size_t l = base + 4 * i + g;
-            load_raw<DT>(G.x, l * kCLineWords + 4 * (size_t)j, nw, l * kCLineWords < G.slice_hi ? G.len : 0, xr[i]);
+            load_raw<DT>(G.x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < G.slice_hi ? G.len : 0, xr[i]);
         }
     };
 
@@ -299,13 +208,13 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     if (!dead && t <= kLast) load_x(t, b, G);
     while (!dead && t <= kLast) {
         const bool sends = t <= kLast - 1;
-        const size_t base = line_lo + b * kCBatchLines;
+        const size_t base = line_lo + b * kBatchLines;
         uint4 w[kI];
 #pragma unroll
         for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
         if (t >= 1) {   // receive: wait for the 32 flags of this batch's slot
-            const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kCBatchLines * 128);
-            const bool live = (base + lane) * kCLineWords < G.slice_hi;
+            const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kBatchLines * 128);
+            const bool live = (base + lane) * kLineWords < G.slice_hi;
             const uint32_t flag = slot + lane * 128 + 120;
             bool ok = !live || ld_acq_local(flag) == q_recv + 1;
             if (!__all_sync(kCFull, ok)) {
@@ -332,7 +241,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
-                if (l * kCLineWords < G.slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
+                if (l * kLineWords < G.slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
             }
         }
         float v[kI][4];
@@ -385,11 +294,11 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                     }
                 }
             }
-            const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kCBatchLines * 128);
+            const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kBatchLines * 128);
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
-                if (l * kCLineWords >= G.slice_hi) continue;
+                if (l * kLineWords >= G.slice_hi) continue;
                 const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
                 if (j < 7)
                     st16_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
@@ -399,7 +308,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             }
             __syncwarp();
             fence_cluster();   // releases these lines; also orders this batch's inbox reads
-            if ((base + lane) * kCLineWords < G.slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
+            if ((base + lane) * kLineWords < G.slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
             ++q_send;
             // this batch's inbox slot is free again (its reads precede the
             // fence): tell the previous rank.  Published after this rank's
@@ -412,7 +321,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
-                if (l * kCLineWords < G.slice_hi) store_out<DT>(G.y, l * kCLineWords + 4 * (size_t)j, nw, G.len, v[i]);
+                if (l * kLineWords < G.slice_hi) store_elems<DT>(G.y, l * kLineWords + 4 * (size_t)j, nw, G.len, v[i]);
             }
         }
         if (!dead && ld_rlx_local(S.abort) != 0) dead = true;
@@ -478,13 +387,13 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
             // receiver frees a slot only after its own send of the next
             // batch, so a step's batches must fit in kSlots - 1 slots
             // (otherwise every rank waits on its successor: a cycle)
-            const size_t per_cta_min = kCBatchElems * kCWarps;
+            const size_t per_cta_min = kBatchElems * kCWarps;
             size_t K = (C + per_cta_min - 1) / per_cta_min;
             if (K > (size_t)resident) K = (size_t)resident;
             if (K < 1) K = 1;
             size_t epc = (C + K - 1) / K;
-            epc = (epc + kCBatchElems - 1) / kCBatchElems * kCBatchElems;
-            if (epc > kCBatchElems * kCWarps * (kSlots - 1)) epc = kCBatchElems * kCWarps * (kSlots - 1);
+            epc = (epc + kBatchElems - 1) / kBatchElems * kBatchElems;
+            if (epc > kBatchElems * kCWarps * (kSlots - 1)) epc = kBatchElems * kCWarps * (kSlots - 1);
             K = (C + epc - 1) / epc;
             if (K < 1) K = 1;
             cfg.gridDim = dim3((unsigned)(K * NR));
