@@ -28,7 +28,7 @@ AR_OK, AR_ERR_INVALID, AR_ERR_ALIGN, AR_ERR_TOO_LARGE, AR_ERR_CUDA, AR_ERR_FLAG_
 (AR_OP_NONE, AR_OP_ONE_SHOT, AR_OP_TWO_SHOT, AR_OP_RING, AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL_REDUCE,
  AR_OP_LL128_PACK, AR_OP_LL128_UNPACK, AR_OP_LL128_REDUCE, AR_OP_ALLREDUCE_RMSNORM, AR_OP_ONE_SHOT_PUSH,
  AR_OP_ONE_SHOT_COPYIN, AR_OP_RING_ROUNDED, AR_OP_TREE, AR_OP_RING_PERSISTENT, AR_OP_RING_CLUSTER,
- AR_OP_TREE_FUSED) = range(18)
+ AR_OP_TREE_FUSED, AR_OP_RING_FUSED, AR_OP_RING_ROUNDED_FUSED) = range(20)
 AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING, AR_OPT_TIMING_PAUSE, AR_OPT_PDL = 1, 2, 3, 4, 5, 6
 AR_OPT_AUTO_POLICY, AR_OPT_AUTO_ALPHA_NS, AR_OPT_AUTO_BETA_MBS, AR_OPT_AUTO_HANDOFF = 7, 8, 9, 10
 AR_OPT_PUSH_STAGING, AR_OPT_REGISTERED, AR_OPT_PERSISTENT, AR_OPT_ABSENT_RANK = 11, 12, 13, 14
@@ -37,7 +37,7 @@ KERNELS = {1: "one_shot", 2: "reduce_scatter", 3: "all_gather", 4: "ring_rs_step
            6: "ll_pack", 7: "ll_unpack", 8: "ll_reduce", 9: "ll128_pack", 10: "ll128_unpack",
            11: "ll128_reduce", 12: "allreduce_rmsnorm", 13: "push", 14: "push_reduce",
            15: "ring_rs_step_rounded", 16: "tree_level", 17: "ring_persistent",
-           18: "copyin", 19: "ring_cluster", 20: "tree_fused"}
+           18: "copyin", 19: "ring_cluster", 20: "tree_fused", 21: "ring_fused", 22: "ring_rounded_fused"}
 
 # C symbols the header declares (checked by the CPU tests against include/ar.h)
 EXPORTS = (
@@ -47,7 +47,7 @@ EXPORTS = (
     "ar_check_args", "ar_strerror", "ar_timing", "ar_ll_pack_n", "ar_ll_unpack_n", "ar_ll128_pack_n",
     "ar_ll128_unpack_n", "ar_ring_noalloc", "ar_select", "ar_auto", "ar_allreduce_rmsnorm",
     "ar_one_shot_push", "ar_one_shot_copyin", "ar_ring_rounded", "ar_tree", "ar_ring_persistent",
-    "ar_ring_cluster", "ar_tree_fused",
+    "ar_ring_cluster", "ar_tree_fused", "ar_ring_fused", "ar_ring_rounded_fused",
 )
 
 
@@ -110,6 +110,8 @@ def lib() -> ctypes.CDLL:
                 "ar_ring_persistent": ([vp, pp, pp, sz, i32, vp], i32),
                 "ar_ring_cluster": ([vp, pp, pp, sz, i32, vp], i32),
                 "ar_tree_fused": ([vp, pp, pp, sz, i32, vp], i32),
+                "ar_ring_fused": ([vp, pp, pp, sz, i32, vp], i32),
+                "ar_ring_rounded_fused": ([vp, pp, pp, sz, i32, vp], i32),
                 "ar_ll_bytes": ([sz], sz),
                 "ar_ll128_bytes": ([sz], sz),
                 "ar_ll_pack": ([vp, vp, vp, sz, u32, vp], i32),
@@ -221,6 +223,15 @@ def ar_ring_cluster(h, ins, outs, count: int, dtype, stream=None) -> int:
 
 def ar_tree_fused(h, ins, outs, count: int, dtype, stream=None) -> int:
     return lib().ar_tree_fused(h, _ptr_array(ins), _ptr_array(outs), count, _dtype(dtype), _stream(stream))
+
+
+def ar_ring_fused(h, ins, outs, count: int, dtype, stream=None) -> int:
+    return lib().ar_ring_fused(h, _ptr_array(ins), _ptr_array(outs), count, _dtype(dtype), _stream(stream))
+
+
+def ar_ring_rounded_fused(h, ins, outs, count: int, dtype, stream=None) -> int:
+    return lib().ar_ring_rounded_fused(h, _ptr_array(ins), _ptr_array(outs), count, _dtype(dtype),
+                                       _stream(stream))
 
 
 def ar_ring(h, ins, outs, count: int, dtype, stream=None) -> int:

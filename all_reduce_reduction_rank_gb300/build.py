@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 OUT_DIR = PKG / "_build"
 LIB = PKG / "libar_gb300.so"
 SOURCES = ["api.cu", "one_shot.cu", "two_shot.cu", "ring.cu", "ll.cu", "ring_noalloc.cu", "rmsnorm.cu",
-           "one_shot_modes.cu", "tree.cu", "ring_persistent.cu", "ring_cluster.cu"]
+           "one_shot_modes.cu", "tree.cu", "ring_persistent.cu", "ring_cluster.cu", "ring_fused.cu"]
 HEADERS = ["common.cuh", "internal.h", "bulk.cuh", "lines.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -222,6 +222,8 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         break;
     }
     case AR_OP_RING_CLUSTER:
+    case AR_OP_RING_FUSED:
+    case AR_OP_RING_ROUNDED_FUSED:
         t->link_bytes_per_rank = 2.0 * (double)(nn - 1) * (double)S / (double)nn;
         t->steps = 2 * (n - 1);
         t->launches = count ? 1 : 0;
@@ -405,7 +407,7 @@ size_t ar_ll128_bytes(size_t payload_bytes) { return 128u * ((payload_bytes + 11
 
 int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t)
 {
-    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_TREE_FUSED) return AR_ERR_INVALID;
+    if (!t || op < AR_OP_ONE_SHOT || op > AR_OP_RING_ROUNDED_FUSED) return AR_ERR_INVALID;
     const bool multi =
         op <= AR_OP_RING || op == AR_OP_LL_REDUCE || op == AR_OP_LL128_REDUCE || op >= AR_OP_ALLREDUCE_RMSNORM;
     if (multi && (n_ranks < 2 || n_ranks > kMaxRanks)) return AR_ERR_INVALID;
@@ -425,7 +427,8 @@ int ar_check_args(int op, int n_ranks, size_t max_bytes, const void* const* in, 
     }
     if (op != AR_OP_ONE_SHOT && op != AR_OP_TWO_SHOT && op != AR_OP_RING && op != AR_OP_ONE_SHOT_PUSH &&
         op != AR_OP_ONE_SHOT_COPYIN && op != AR_OP_RING_ROUNDED && op != AR_OP_TREE &&
-        op != AR_OP_RING_PERSISTENT && op != AR_OP_RING_CLUSTER && op != AR_OP_TREE_FUSED && !is_ll_op(op))
+        op != AR_OP_RING_PERSISTENT && op != AR_OP_RING_CLUSTER && op != AR_OP_TREE_FUSED &&
+        op != AR_OP_RING_FUSED && op != AR_OP_RING_ROUNDED_FUSED && !is_ll_op(op))
         return AR_ERR_INVALID;
     return check_multi(op, n_ranks, max_bytes, in, out, count, dt);
 }
@@ -594,6 +597,17 @@ int ar_tree_fused(ar_handle h, const void* const* in, void* const* out, size_t c
 int ar_ring_cluster(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
 {
     return all_reduce_call(AR_OP_RING_CLUSTER, launch_ring_cluster, h, in, out, count, dt, s);
+}
+
+int ar_ring_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t s)
+{
+    return all_reduce_call(AR_OP_RING_FUSED, launch_ring_fused, h, in, out, count, dt, s);
+}
+
+int ar_ring_rounded_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                          ar_stream_t s)
+{
+    return all_reduce_call(AR_OP_RING_ROUNDED_FUSED, launch_ring_rounded_fused, h, in, out, count, dt, s);
 }
 
 int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,

@@ -149,6 +149,10 @@ int launch_tree_fused(Handle& h, const void* const* in, void* const* out, size_t
                       int* launches);
 int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
                         int* launches);
+int launch_ring_fused(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
+                      int* launches);
+int launch_ring_rounded_fused(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
+                              cudaStream_t s, int* launches);
 uint64_t persist_lines_per_step(int n, size_t count, int dt);
 int launch_ll_pack(Handle& h, int nb, const float* const* src, void* const* lines, size_t count, uint32_t step,
                    cudaStream_t s);

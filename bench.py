@@ -123,6 +123,7 @@ KERNEL_SOURCES = {
     "allreduce_rmsnorm": ["rmsnorm.cu"], "push": ["one_shot_modes.cu"], "push_reduce": ["one_shot_modes.cu"],
     "copyin": ["one_shot_modes.cu"], "ring_rs_step_rounded": ["ring.cu"], "tree_level": ["tree.cu"],
     "ring_persistent": ["ring_persistent.cu"], "ring_cluster": ["ring_cluster.cu"], "tree_fused": ["tree.cu"],
+    "ring_fused": ["ring_fused.cu"], "ring_rounded_fused": ["ring_fused.cu"],
 }
 
 
@@ -599,6 +600,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
              ("ring_rounded", L.ar_ring_rounded, ar.AR_OP_RING_ROUNDED),
              ("ring_persistent", L.ar_ring_persistent, ar.AR_OP_RING_PERSISTENT),
              ("ring_cluster", L.ar_ring_cluster, ar.AR_OP_RING_CLUSTER),
+             ("ring_fused", L.ar_ring_fused, ar.AR_OP_RING_FUSED),
+             ("ring_rounded_fused", L.ar_ring_rounded_fused, ar.AR_OP_RING_ROUNDED_FUSED),
              ("tree", L.ar_tree, ar.AR_OP_TREE),
              ("tree_fused", L.ar_tree_fused, ar.AR_OP_TREE_FUSED))
     res = {a[0]: [] for a in algos}
@@ -931,6 +934,9 @@ def calls_cpu(min_seconds: float = 0.5) -> dict:
                          ("ring_rounded", lambda: oracle.ring_rounded(xs, "bf16"), ar.AR_OP_RING_ROUNDED),
                          ("ring_persistent", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_PERSISTENT),
                          ("ring_cluster", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_CLUSTER),
+                         ("ring_fused", lambda: oracle.ring(xs, "bf16"), ar.AR_OP_RING_FUSED),
+                         ("ring_rounded_fused", lambda: oracle.ring_rounded(xs, "bf16"),
+                          ar.AR_OP_RING_ROUNDED_FUSED),
                          ("tree", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE),
                          ("tree_fused", lambda: oracle.tree(xs, "bf16"), ar.AR_OP_TREE_FUSED)):
         t = ar.ar_plan(op, n, N, "bf16")

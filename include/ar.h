@@ -88,7 +88,9 @@ typedef enum {
     AR_OP_TREE = 14,
     AR_OP_RING_PERSISTENT = 15,
     AR_OP_RING_CLUSTER = 16,
-    AR_OP_TREE_FUSED = 17
+    AR_OP_TREE_FUSED = 17,
+    AR_OP_RING_FUSED = 18,
+    AR_OP_RING_ROUNDED_FUSED = 19
 } ar_op;
 
 /* Traffic of one call.
@@ -179,7 +181,9 @@ typedef enum {
     AR_K_RING_PERSISTENT = 17,      /* ar_ring_persistent (all steps) */
     AR_K_COPYIN = 18,               /* ar_one_shot_copyin's copy into the registered buffers */
     AR_K_RING_CLUSTER = 19,         /* ar_ring_cluster (all steps) */
-    AR_K_TREE_FUSED = 20            /* ar_tree_fused (all levels) */
+    AR_K_TREE_FUSED = 20,           /* ar_tree_fused (all levels) */
+    AR_K_RING_FUSED = 21,           /* ar_ring_fused (all steps) */
+    AR_K_RING_ROUNDED_FUSED = 22    /* ar_ring_rounded_fused (all steps) */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -291,6 +295,23 @@ int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, 
  * level-by-level form moves log2(n) times that). */
 int ar_tree_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                   ar_stream_t stream);
+
+/* The ring of ar_ring with all 2(n-1) steps done in registers in one pass
+ * ("多 GPU 与 NCCL", §ring all-reduce): per element, chunk c's reduce-scatter
+ * is the chain x_c + x_{c+1} + ... + x_{c+n-1} (mod n) of binary32 adds, and
+ * the all-gather copies its rounded result unchanged, so each thread loads
+ * the n ranks' values of a 16-byte vector once, adds them in that order and
+ * stores the one rounded result to all n outputs.  Same chunks, order and
+ * bits as ar_ring; layout and in-place rules as ar_one_shot; needs no scratch.
+ * One launch; HBM reads n S, writes n S. */
+int ar_ring_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                  ar_stream_t stream);
+
+/* ar_ring_rounded in one pass, as ar_ring_fused: the partial is rounded to
+ * the payload type after every hop but the last.  Same bits as
+ * ar_ring_rounded.  One launch; HBM reads n S, writes n S. */
+int ar_ring_rounded_fused(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
+                          ar_stream_t stream);
 
 /* The ring of ar_ring in a single (cooperative) launch, each hop carried as
  * LL128 lines: 120 bytes of fp32 words and an 8-byte step flag per 128 bytes
@@ -477,6 +498,7 @@ int ar_plan(int op, int n_ranks, size_t count, ar_dtype dt, ar_traffic_t* t);
  * arguments before launching anything.  op AR_OP_ONE_SHOT, AR_OP_TWO_SHOT,
  * AR_OP_RING, AR_OP_ONE_SHOT_PUSH, AR_OP_ONE_SHOT_COPYIN, AR_OP_RING_ROUNDED,
  * AR_OP_TREE and AR_OP_TREE_FUSED (n_ranks a power of two), AR_OP_RING_PERSISTENT, AR_OP_RING_CLUSTER,
+ * AR_OP_RING_FUSED, AR_OP_RING_ROUNDED_FUSED,
  * AR_OP_LL_REDUCE, AR_OP_LL128_REDUCE: the multi-rank calls (n_ranks in
  * [2, 16]; the handle's optional buffers are not checked); AR_OP_LL_PACK, AR_OP_LL_UNPACK, AR_OP_LL128_PACK,
  * AR_OP_LL128_UNPACK: the batched pack / unpack calls over n_ranks buffers

@@ -102,7 +102,7 @@ def test_plan_batched_pack_scales_with_buffers(lib, nb):
 
 
 def test_plan_rejects_bad_arguments(lib):
-    bad = [(0, 8), (ar.AR_OP_TREE_FUSED + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
+    bad = [(0, 8), (ar.AR_OP_RING_ROUNDED_FUSED + 1, 8), (ar.AR_OP_ONE_SHOT, 1), (ar.AR_OP_RING, 17),
            (ar.AR_OP_ALLREDUCE_RMSNORM, 1)]
     for op, n in bad:
         with pytest.raises(ar.ArError):
@@ -346,3 +346,19 @@ def test_plan_tree_fused(lib, n):
     assert t.steps == n.bit_length() - 1 and t.launches == 1
     with pytest.raises(ar.ArError):
         ar.ar_plan(ar.AR_OP_TREE_FUSED, 6, N, "bf16")
+
+
+@pytest.mark.parametrize("op", ["AR_OP_RING_FUSED", "AR_OP_RING_ROUNDED_FUSED"])
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+def test_plan_ring_fused(lib, op, n):
+    N = 4099
+    t = ar.ar_plan(getattr(ar, op), n, N, "bf16")
+    assert (t.hbm_read_bytes, t.hbm_write_bytes) == (n * 2 * N, n * 2 * N)
+    assert t.steps == 2 * (n - 1) and t.launches == 1
+    assert t.link_bytes_per_rank == pytest.approx(model.link_bytes_ring(n, 2 * N))
+    assert ar.ar_plan(getattr(ar, op), n, 0, "bf16").launches == 0
+    ins, outs = _bufs(n), _bufs(n, off=64 << 20)
+    assert _check(getattr(ar, op), n, ins, outs, 1000) == ar.AR_OK
+    assert _check(getattr(ar, op), n, ins, ins, 1000) == ar.AR_OK   # in place
+    outs[1] = outs[0]
+    assert _check(getattr(ar, op), n, ins, outs, 1000) == ar.AR_ERR_INVALID

@@ -411,7 +411,8 @@ def test_tree_in_place_hand_worked_and_refusals():
 
 @pytest.mark.parametrize("call,oracle_fn", [
     ("ar_one_shot_push", "all_reduce"), ("ar_one_shot_copyin", "all_reduce"), ("ar_ring_rounded", "ring_rounded"),
-    ("ar_tree", "tree"), ("ar_tree_fused", "tree"), ("ar_ring_persistent", "ring"), ("ar_ring_cluster", "ring")])
+    ("ar_tree", "tree"), ("ar_tree_fused", "tree"), ("ar_ring_persistent", "ring"), ("ar_ring_cluster", "ring"),
+    ("ar_ring_fused", "ring"), ("ar_ring_rounded_fused", "ring_rounded")])
 def test_cuda_graph_capture_of_the_other_calls(call, oracle_fn):
     # captured once, replayed on new contents of the same buffers
     n, N = 8, 65536 + 3
@@ -470,3 +471,56 @@ def test_tree_fused_in_place_and_refusal():
     with Handle(6, 64) as h:
         i6, o6 = empty_ranks(6, 64), empty_ranks(6, 64)
         assert ar.ar_tree_fused(h, ptrs(i6), ptrs(o6), 16, "bf16") == ar.AR_ERR_INVALID
+
+
+# --- the ring's steps done in registers in one pass -----------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("n,N", [(2, 9), (3, 1000), (5, 4099), (8, 4099), (8, 300_001), (13, 50_001),
+                                 (16, 65536 + 3), (16, 7)])
+def test_ring_fused_matches_the_ring(dtype, n, N):
+    xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=11 * n + N)
+    ins = upload_ranks(xs)
+    a, b = empty_ranks(n, xs[0].nbytes), empty_ranks(n, xs[0].nbytes)
+    ra, rb = empty_ranks(n, xs[0].nbytes), empty_ranks(n, xs[0].nbytes)
+    with Handle(n, max(16, N * E[dtype])) as h:
+        assert ar.ar_ring_fused(h, ptrs(ins), ptrs(a), N, dtype) == ar.AR_OK
+        t = ar.ar_traffic(h)
+        assert t.op == ar.AR_OP_RING_FUSED and t.launches == 1 and t.steps == 2 * (n - 1)
+        assert ar.ar_ring(h, ptrs(ins), ptrs(b), N, dtype) == ar.AR_OK
+        assert ar.ar_ring_rounded_fused(h, ptrs(ins), ptrs(ra), N, dtype) == ar.AR_OK
+        assert ar.ar_traffic(h).op == ar.AR_OP_RING_ROUNDED_FUSED
+        assert ar.ar_ring_rounded(h, ptrs(ins), ptrs(rb), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    want, want_r = oracle.ring(xs, dtype), oracle.ring_rounded(xs, dtype)
+    for r in range(n):
+        got = a[r].download(payload_np_dtype(dtype))
+        np.testing.assert_array_equal(bits(got), bits(want[r]))
+        np.testing.assert_array_equal(bits(got), bits(b[r].download(payload_np_dtype(dtype))))
+        got_r = ra[r].download(payload_np_dtype(dtype))
+        np.testing.assert_array_equal(bits(got_r), bits(want_r[r]))
+        np.testing.assert_array_equal(bits(got_r), bits(rb[r].download(payload_np_dtype(dtype))))
+    for buf in ins + a + b + ra + rb:
+        assert buf.guards_intact()
+
+
+def test_ring_fused_in_place_hand_worked():
+    # bf16, n = 3, 8 elements per chunk: rank 0 holds 256, ranks 1 and 2 hold 1.
+    # Chunk 0 adds 256 + 1 + 1 = 258 in fp32 (exact in bf16); the hop-rounded
+    # form rounds 257 to 256 first and ends at 256.  Chunk 1 starts at rank 1:
+    # 1 + 1 + 256 = 258 both ways.  Chunk 2 starts at rank 2: 1 + 256 = 257,
+    # which the hop-rounded form rounds to 256 before adding the last 1.
+    b = lambda v: oracle.f32_to_bf16(np.full(24, v, np.float32))
+    x = [b(256.0), b(1.0), b(1.0)]
+    ins, ins_r = upload_ranks(x), upload_ranks(x)
+    with Handle(3, 48) as h:
+        assert ar.ar_ring_fused(h, ptrs(ins), ptrs(ins), 24, "bf16") == ar.AR_OK
+        assert ar.ar_ring_rounded_fused(h, ptrs(ins_r), ptrs(ins_r), 24, "bf16") == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    for y in ins:
+        np.testing.assert_array_equal(oracle.bf16_to_f32(y.download(np.uint16)), np.full(24, 258.0, np.float32))
+    want_r = np.array([256.0] * 8 + [258.0] * 8 + [256.0] * 8, np.float32)
+    for y in ins_r:
+        np.testing.assert_array_equal(oracle.bf16_to_f32(y.download(np.uint16)), want_r)

@@ -146,3 +146,29 @@ def test_other_calls_at_the_prefill_size():
     for r in (0, 3, 7):
         np.testing.assert_array_equal(outs["rounded"][r].cpu().numpy().view(np.uint16), want_rounded[r])
         np.testing.assert_array_equal(outs["tree"][r].cpu().numpy().view(np.uint16), want_tree[r])
+
+
+def test_fused_rings_at_the_prefill_size():
+    # n = 8 bf16, 64 MiB per rank: the one-pass rings against the oracle's
+    # ring orders over whole buffers, and equal to the step-by-step rings
+    n, dtype, S = 8, "bf16", 64 * MiB
+    N = S // 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(3) + 78)
+    outs = {k: [torch.empty_like(t) for t in ins] for k in ("fused", "ring", "rounded_fused", "rounded")}
+    h = ar.ar_create(n, S)
+    try:
+        for key, call in (("fused", ar.ar_ring_fused), ("ring", ar.ar_ring),
+                          ("rounded_fused", ar.ar_ring_rounded_fused), ("rounded", ar.ar_ring_rounded)):
+            _run(call, h, ins, outs[key], N, dtype)
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+    for r in range(n):
+        assert torch.equal(outs["fused"][r], outs["ring"][r])
+        assert torch.equal(outs["rounded_fused"][r], outs["rounded"][r])
+    host = [t.cpu().numpy().view(np.uint16) for t in ins]
+    want, want_rounded = oracle.ring(host, dtype), oracle.ring_rounded(host, dtype)
+    for r in (0, 4, 7):
+        np.testing.assert_array_equal(outs["fused"][r].cpu().numpy().view(np.uint16), want[r])
+        np.testing.assert_array_equal(outs["rounded_fused"][r].cpu().numpy().view(np.uint16), want_rounded[r])

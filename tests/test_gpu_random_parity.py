@@ -27,6 +27,8 @@ CALLS = {
     "tree_fused": (ar.ar_tree_fused, oracle.tree),
     "ring_persistent": (ar.ar_ring_persistent, oracle.ring),
     "ring_cluster": (ar.ar_ring_cluster, oracle.ring),
+    "ring_fused": (ar.ar_ring_fused, oracle.ring),
+    "ring_rounded_fused": (ar.ar_ring_rounded_fused, oracle.ring_rounded),
 }
 
 
