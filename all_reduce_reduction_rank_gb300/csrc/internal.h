@@ -127,6 +127,23 @@ inline unsigned grid_for_rows(const Handle& h, size_t work, int rows)
     return want ? (unsigned)want : 1u;
 }
 
+// Launch shape for a call too small to give every SM a full CTA: `work`
+// thread-iterations in each of `rows` rows (blockIdx.y), one per thread,
+// with the CTAs narrowed (down to one warp) until the grid covers the SMs or
+// cannot grow further.  Measured on GB300 (n = 8 bf16, 8 KiB - 1 MiB per
+// rank): a small call's time is set by how many SMs move its bytes, not by
+// how many threads each SM runs, so narrow CTAs on many SMs beat one wide CTA.
+struct Shape {
+    unsigned grid_x, block;
+};
+inline Shape narrow_shape(const Handle& h, size_t work, int rows = 1)
+{
+    unsigned block = kThreads;
+    while (block > 32 && ((work + block - 1) / block) * (size_t)rows < (size_t)h.sm_count) block >>= 1;
+    size_t want = (work + block - 1) / block;
+    return Shape{want ? (unsigned)want : 1u, block};
+}
+
 // Launchers: argument checks are done by the caller; these only launch.
 int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                     cudaStream_t s, int* launches);

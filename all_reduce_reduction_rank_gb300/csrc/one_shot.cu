@@ -20,18 +20,25 @@ namespace {
 // per thread without spilling at n = 16.
 template <int NR> __host__ __device__ constexpr int one_shot_unroll() { return NR <= 4 ? 4 : NR <= 8 ? 2 : 1; }
 
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+// U vectors per thread per iteration, in CTAs of up to kThreads threads.
+// Small: a call too small to give every SM a full CTA, run with U = 1 and
+// narrower CTAs, and compiled for three CTAs per SM (at most 80 registers;
+// a minimum of 0 leaves the full-size form to the compiler's own choice).
+// That bound matters for latency: measured on GB300 (n = 8 and 16 bf16,
+// CUDA-graph replay), the compiler's own register choice ran calls of 8 KiB -
+// 1 MiB per rank 0.2-1.9 us slower, while for full-size calls the bound
+// gains nothing and costs up to 5% at 2 MiB.
+template <int NR, int DT, int U, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 one_shot_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count)
 {
     pdl_acquire();
-    constexpr int U = one_shot_unroll<NR>();
-    const size_t span = (size_t)kThreads * U;
+    const size_t bs = U > 1 ? (size_t)kThreads : (size_t)blockDim.x, span = bs * U;  // U > 1: full CTAs only
     for (size_t base = (size_t)blockIdx.x * span; base < nvec; base += (size_t)gridDim.x * span) {
         uint4 x[U][NR];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < nvec) {
 #pragma unroll
                 for (int q = 0; q < NR; ++q) x[u][q] = ld16(static_cast<const uint4*>(in.p[q]) + v);
@@ -39,7 +46,7 @@ one_shot_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MP
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < nvec) {
                 const uint4 r = reduce_rank_order<DT, NR>(x[u]);
 #pragma unroll
@@ -217,7 +224,12 @@ int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t c
                 constexpr int U = one_shot_unroll<NR>();
                 const unsigned grid = grid_for(h, (nvec + U - 1) / U);
                 rec_begin(h, s);
-                launch_kernel(h, one_shot_kernel<NR, DT>, grid, kThreads, 0, s, ip, op, nvec, count);
+                if (grid < (unsigned)h.sm_count) {
+                    const Shape sh = narrow_shape(h, nvec);
+                    launch_kernel(h, one_shot_kernel<NR, DT, 1, true>, sh.grid_x, sh.block, 0, s, ip, op, nvec,
+                                  count);
+                } else
+                    launch_kernel(h, one_shot_kernel<NR, DT, U, false>, grid, kThreads, 0, s, ip, op, nvec, count);
                 rec_end(h, s, AR_K_ONE_SHOT, 2ull * NR * S);
             }
             *launches = 1;

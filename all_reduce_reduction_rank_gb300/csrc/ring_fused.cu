@@ -32,9 +32,11 @@ __device__ __forceinline__ void hop_round(float* a)
 }
 
 // Grid: blockIdx.y = chunk c (block-uniform ring order), blockIdx.x strides
-// over the chunk's 16-byte vectors.  HR: round the partial after every hop.  Three CTAs per SM
+// over the chunk's 16-byte vectors, U per thread per iteration in CTAs of up
+// to kThreads threads (U = 1 and narrower CTAs for calls too small to give
+// every SM a full CTA).  HR: round the partial after every hop.  Three CTAs per SM
 // at least: registers stay at or below 80, and no rank count spills.
-template <int NR, int DT, bool HR>
+template <int NR, int DT, bool HR, int U>
 __global__ void __launch_bounds__(kThreads, 3)
 ring_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t C,
                   size_t count)
@@ -42,7 +44,6 @@ ring_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ 
     pdl_acquire();
     using T = typename Payload<DT>::scalar_t;
     constexpr int VE = kVecElems<DT>;
-    constexpr int U = ring_fused_unroll<NR>();
     const int c = blockIdx.y;
     const size_t e_lo = (size_t)c * C;
     if (e_lo >= count) return;
@@ -50,12 +51,12 @@ ring_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ 
     const size_t nv = len / VE;
     // src(k): chunk c of the rank the chain reaches after k hops
     auto src = [&](int k) { return static_cast<const T*>(in.p[c + k < NR ? c + k : c + k - NR]) + e_lo; };
-    const size_t span = (size_t)kThreads * U;
+    const size_t bs = U > 1 ? (size_t)kThreads : (size_t)blockDim.x, span = bs * U;  // U > 1: full CTAs only
     for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
         uint4 x[U][NR];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < nv) {
 #pragma unroll
                 for (int k = 0; k < NR; ++k) x[u][k] = ld16(src(k) + v * VE);
@@ -63,7 +64,7 @@ ring_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ 
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < nv) {
                 float a[VE];
                 // the chain starts from rank c's value itself (no zero start)
@@ -118,7 +119,12 @@ int launch_ring_fused_impl(Handle& h, const void* const* in, void* const* out, s
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
             const dim3 grid(grid_for_rows(h, (cvec + U - 1) / U, NR), NR);
             rec_begin(h, s);
-            launch_kernel(h, ring_fused_kernel<NR, DT, HR>, grid, kThreads, 0, s, ip, op, C, count);
+            if (grid.x * grid.y < (unsigned)h.sm_count) {
+                const Shape sh = narrow_shape(h, cvec, NR);
+                launch_kernel(h, ring_fused_kernel<NR, DT, HR, 1>, dim3(sh.grid_x, NR), sh.block, 0, s, ip, op, C,
+                              count);
+            } else
+                launch_kernel(h, ring_fused_kernel<NR, DT, HR, U>, grid, kThreads, 0, s, ip, op, C, count);
             rec_end(h, s, HR ? AR_K_RING_ROUNDED_FUSED : AR_K_RING_FUSED, 2ull * NR * S);
             *launches = 1;
             return launch_status();

@@ -108,8 +108,10 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
 namespace argb {
 namespace {
 
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+// Small: a call too small to give every SM a full CTA, in narrower CTAs and
+// compiled for three CTAs per SM (for latency, as the one-shot kernel).
+template <int NR, int DT, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 tree_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
                   size_t count)
 {
@@ -128,7 +130,8 @@ tree_fused_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ 
             for (int r = 0; r < NR; ++r) f[r] = g[r];
         }
     };
-    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+    const size_t bs = Small ? (size_t)blockDim.x : (size_t)kThreads;   // the full-size form: kThreads-thread CTAs
+    for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs) {
         uint4 x[NR];
 #pragma unroll
         for (int q = 0; q < NR; ++q) x[q] = ld16(static_cast<const uint4*>(in.p[q]) + v);
@@ -189,9 +192,15 @@ int launch_tree_fused(Handle& h, const void* const* in, void* const* out, size_t
                 }
                 const size_t nvec = count / kVecElems<DT>;
                 const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+                // full CTAs, or narrower ones spread over more SMs for a small call
+                const unsigned grid = grid_for(h, nvec);
                 rec_begin(h, s);
-                launch_kernel(h, tree_fused_kernel<NR, DT>, dim3(grid_for(h, nvec)), kThreads, 0, s, ip, op, nvec,
-                              count);
+                if (grid < (unsigned)h.sm_count) {
+                    const Shape sh = narrow_shape(h, nvec);
+                    launch_kernel(h, tree_fused_kernel<NR, DT, true>, sh.grid_x, sh.block, 0, s, ip, op, nvec, count);
+                } else {
+                    launch_kernel(h, tree_fused_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, op, nvec, count);
+                }
                 rec_end(h, s, AR_K_TREE_FUSED, 2ull * NR * S);
                 *launches = 1;
                 return launch_status();

@@ -24,26 +24,28 @@ template <int NR> __host__ __device__ constexpr int rs_unroll() { return NR <= 4
 constexpr int kAgUnroll = 1;
 
 // Grid: blockIdx.y = chunk r (block-uniform output pointer, no per-vector
-// division), blockIdx.x strides over the chunk's 16-byte vectors.
+// division), blockIdx.x strides over the chunk's 16-byte vectors, in CTAs of
+// up to kThreads threads (narrower ones, and U = 1, for calls too small to
+// give every SM a full CTA; Small, compiled for three CTAs per SM as the
+// one-shot kernel's small form, for latency).
 
 // out[r][v] = rank-order sum of in[*][v] for v in chunk r.
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+template <int NR, int DT, int U, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t nvec,
                       size_t count, size_t cvec)
 {
     pdl_acquire();
-    constexpr int U = rs_unroll<NR>();
     const int r = blockIdx.y;
     const size_t lo = (size_t)r * cvec;
     const size_t hi = lo + cvec < nvec ? lo + cvec : nvec;
     uint4* const dst = static_cast<uint4*>(out.p[r]);
-    const size_t span = (size_t)kThreads * U;
+    const size_t bs = U > 1 ? (size_t)kThreads : (size_t)blockDim.x, span = bs * U;  // U > 1: full CTAs only
     for (size_t base = lo + (size_t)blockIdx.x * span; base < hi; base += (size_t)gridDim.x * span) {
         uint4 x[U][NR];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < hi) {
 #pragma unroll
                 for (int q = 0; q < NR; ++q) x[u][q] = ld16(static_cast<const uint4*>(in.p[q]) + v);
@@ -51,7 +53,7 @@ reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constan
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < hi) st16(dst + v, reduce_rank_order<DT, NR>(x[u]));
         }
     }
@@ -70,8 +72,8 @@ reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constan
 }
 
 // For v in chunk j: out[q][v] = out[j][v] for every q != j.
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+template <int NR, int DT, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 all_gather_kernel(const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t count, size_t cvec)
 {
     pdl_acquire();
@@ -80,17 +82,17 @@ all_gather_kernel(const __grid_constant__ MPtrs<NR> out, size_t nvec, size_t cou
     const size_t lo = (size_t)j * cvec;
     const size_t hi = lo + cvec < nvec ? lo + cvec : nvec;
     const uint4* const src = static_cast<const uint4*>(out.p[j]);
-    const size_t span = (size_t)kThreads * U;
+    const size_t bs = blockDim.x, span = bs * U;
     for (size_t base = lo + (size_t)blockIdx.x * span; base < hi; base += (size_t)gridDim.x * span) {
         uint4 x[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < hi) x[u] = ld16(src + v);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t v = base + (size_t)u * kThreads + threadIdx.x;
+            const size_t v = base + (size_t)u * bs + threadIdx.x;
             if (v < hi) {
 #pragma unroll
                 for (int q = 0; q < NR; ++q)
@@ -133,12 +135,24 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
             const dim3 g_rs(grid_for_rows(h, (cvec + U - 1) / U, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
+            // a call too small to give every SM a full CTA: narrower CTAs, one vector per thread
+            const bool narrow = g_rs.x * NR < (unsigned)h.sm_count;
+            const Shape sh = narrow_shape(h, cvec, NR);
             rec_begin(h, s);
-            launch_kernel(h, reduce_scatter_kernel<NR, DT>, g_rs, kThreads, 0, s, ip, op, nvec, count, cvec);
+            if (narrow)
+                launch_kernel(h, reduce_scatter_kernel<NR, DT, 1, true>, dim3(sh.grid_x, NR), sh.block, 0, s, ip, op,
+                              nvec, count, cvec);
+            else
+                launch_kernel(h, reduce_scatter_kernel<NR, DT, U, false>, g_rs, kThreads, 0, s, ip, op, nvec, count,
+                              cvec);
             rec_end(h, s, AR_K_REDUCE_SCATTER, (uint64_t)(NR + 1) * S);
             if (launch_status() != AR_OK) return AR_ERR_CUDA;
             rec_begin(h, s);
-            launch_kernel(h, all_gather_kernel<NR, DT>, g_ag, kThreads, 0, s, op, nvec, count, cvec);
+            if (narrow)
+                launch_kernel(h, all_gather_kernel<NR, DT, true>, dim3(sh.grid_x, NR), sh.block, 0, s, op, nvec, count,
+                              cvec);
+            else
+                launch_kernel(h, all_gather_kernel<NR, DT, false>, g_ag, kThreads, 0, s, op, nvec, count, cvec);
             rec_end(h, s, AR_K_ALL_GATHER, (uint64_t)NR * S);
             *launches = 2;
             return launch_status();
