@@ -477,7 +477,9 @@ def ll_sweep(wl, peak: float, batches: int = 5) -> dict:
     8 B .. 1 MiB per rank, doubling): one pass = batched pack of the n
     payloads, the flag-checked reduce, batched unpack, with a fresh step id
     per pass.  Reported per size: µs per pass, payload GB/s (n P / t), the
-    lines' wire efficiency and the algorithmic HBM GB/s of the three calls."""
+    lines' wire efficiency and the algorithmic HBM GB/s of the three calls
+    (all from back-to-back passes issued from Python), and the device time
+    per pass replayed from a CUDA graph."""
     import all_reduce_reduction_rank_gb300 as ar
     import workloads
 
@@ -512,7 +514,10 @@ def ll_sweep(wl, peak: float, batches: int = 5) -> dict:
             one(0)
             us = _batched_us(wl.stream, one, 200 if P <= 64 * 1024 else 50, batches)
             ar.check(ar.ar_status(h), kind + " sweep")
-            out[kind].append({"payload_bytes": P, "us_per_pass": round(us, 3),
+            # device time per pass: 20 passes (their step ids fixed at capture) replayed from a graph
+            gus = _graph_us(wl.stream, one)
+            ar.check(ar.ar_status(h), kind + " sweep, graph")
+            out[kind].append({"payload_bytes": P, "us_per_pass": round(us, 3), "graph_us_per_pass": round(gus, 3),
                               "payload_GB/s": round(n * P / (us * 1e-6) / 1e9, 2),
                               "wire_efficiency": round(wire, 4), "hbm_GB/s": round(b / (us * 1e-6) / 1e9, 1),
                               "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4)})
