@@ -528,7 +528,9 @@ def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
     """The n = 16 doubling sweep (bf16 and fp16, 1 KiB .. 256 MiB per rank):
     ring, one-shot and two-shot.  Inputs are 16 device buffers of 256 MiB;
     smaller messages rotate over slots of them so that back-to-back calls do
-    not find their data in L2.  µs per call and algorithmic HBM GB/s."""
+    not find their data in L2.  µs per call and algorithmic HBM GB/s of
+    back-to-back calls issued from Python, and (up to 8 MiB) the device time
+    per call replayed from a CUDA graph."""
     import ctypes
 
     import torch
@@ -567,12 +569,13 @@ def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
                     us = _batched_us(stream, one, calls, batches)
                     t = ar.ar_plan(op, n, count, dtype)
                     gbs = (t.hbm_read_bytes + t.hbm_write_bytes) / (us * 1e-6) / 1e9
-                    rows.append([S, round(us, 2), round(gbs, 1)])
+                    gus = round(_graph_us(stream, one), 3) if S <= GRAPH_MAX_BYTES else None
+                    rows.append([S, round(us, 2), round(gbs, 1), gus])
                 ar.check(ar.ar_status(h), name)
                 res[f"{dtype}/{name}"] = rows
     finally:
         ar.ar_destroy(h)
-    return {"columns": ["bytes_per_rank", "us", "hbm_GB/s"], "peak": peak, **res}
+    return {"columns": ["bytes_per_rank", "us", "hbm_GB/s", "graph_us"], "peak": peak, **res}
 
 
 VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
