@@ -10,8 +10,9 @@
 //   r = RN(a + residual)                          -> residual_out
 //   y = RN(r * 1/sqrt(mean(r^2) + eps) * weight)  -> norm_out[0..n-1]
 //
-// Layout: one thread-block cluster of kClusterCtas CTAs per token row; CTA c
-// of the cluster owns a contiguous slice of the row.  Pass 1 reads the n rank
+// Layout: one thread-block cluster of CL CTAs per token row (8; 16, a
+// non-portable cluster size, when the rows are too few to give every SM a
+// CTA with 8); CTA c of the cluster owns a contiguous slice of the row.  Pass 1 reads the n rank
 // slices once, writes r, keeps r (fp32) in shared memory and accumulates its
 // squares; each CTA pushes its partial sum into every CTA's shared memory
 // (distributed shared memory), one cluster barrier, and every CTA adds the
@@ -23,7 +24,7 @@
 namespace argb {
 namespace {
 
-constexpr int kClusterCtas = 8;
+constexpr int kClusterCtas = 8;   // the cluster size that sizes the shared-memory slice
 constexpr int kNormThreads = 128;
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -50,7 +51,7 @@ __device__ __forceinline__ void st_cluster_f32(float* local, uint32_t cta, float
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <int NR, int DT>
+template <int NR, int DT, int CL>
 __global__ void __launch_bounds__(kNormThreads)
 allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __restrict__ residual,
                          const void* __restrict__ weight, float eps, const __grid_constant__ MPtrs<NR> out,
@@ -59,14 +60,14 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     constexpr int VE = kVecElems<DT>;
     extern __shared__ float r_slice[];                 // slice_vecs * VE floats
     __shared__ float warp_part[kNormThreads / 32];
-    __shared__ float parts[kClusterCtas];   // every CTA's sum of squares, pushed by that CTA
+    __shared__ float parts[CL];   // every CTA's sum of squares, pushed by that CTA
     __shared__ float row_inv;
     // the first half of a cluster barrier: the wait before the partial sums
     // are pushed makes sure every CTA of the cluster has started
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_acquire();
     const uint32_t c = cluster_ctarank();
-    const size_t t = blockIdx.x / kClusterCtas;        // token row of this cluster
+    const size_t t = blockIdx.x / CL;                  // token row of this cluster
     const size_t nvec_row = hidden / VE;
     const size_t v_lo = (size_t)c * slice_vecs;
     const size_t v_hi = v_lo + slice_vecs < nvec_row ? v_lo + slice_vecs : nvec_row;
@@ -113,13 +114,13 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     if (threadIdx.x == 0) {   // this CTA's partial, pushed into every CTA of the cluster
         float s = 0.0f;
         for (int w = 0; w < kNormThreads / 32; ++w) s = s + warp_part[w];
-        for (uint32_t k = 0; k < kClusterCtas; ++k) st_cluster_f32(&parts[c], k, s);
+        for (uint32_t k = 0; k < CL; ++k) st_cluster_f32(&parts[c], k, s);
     }
     // one barrier: every push has landed, and none is left to land after it
     cluster_sync();
     if (threadIdx.x == 0) {   // the row's: the cluster's CTAs in order
         float s = 0.0f;
-        for (uint32_t k = 0; k < kClusterCtas; ++k) s = s + parts[k];
+        for (uint32_t k = 0; k < CL; ++k) s = s + parts[k];
         row_inv = 1.0f / sqrtf(s / (float)hidden + eps);
     }
     __syncthreads();
@@ -173,33 +174,45 @@ int launch_allreduce_rmsnorm(Handle& h, const void* const* in, const void* resid
                 ip.p[q] = in[q];
                 op.p[q] = out[q];
             }
-            const size_t slice = rmsnorm_slice_vecs(hidden, DT);
-            const size_t smem = slice * kVecElems<DT> * sizeof(float);
-            static const bool attr_ok =
-                cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kRmsnormMaxSliceBytes) == cudaSuccess;
-            if (!attr_ok) return AR_ERR_CUDA;
-            cudaLaunchAttribute attr[2];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = kClusterCtas;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[1].val.programmaticStreamSerializationAllowed = h.pdl ? 1 : 0;
-            cudaLaunchConfig_t cfg{};
-            cfg.gridDim = dim3((unsigned)(tokens * kClusterCtas));
-            cfg.blockDim = dim3(kNormThreads);
-            cfg.dynamicSmemBytes = smem;
-            cfg.stream = s;
-            cfg.attrs = attr;
-            cfg.numAttrs = 2;
             const uint64_t S = (uint64_t)tokens * hidden * sizeof(typename Payload<DT>::scalar_t);
             const uint64_t W = (uint64_t)hidden * sizeof(typename Payload<DT>::scalar_t);
-            rec_begin(h, s);
-            const cudaError_t e = cudaLaunchKernelEx(&cfg, allreduce_rmsnorm_kernel<NR, DT>, ip, residual, weight, eps,
-                                                     op, residual_out, hidden, slice);
-            rec_end(h, s, AR_K_ALLREDUCE_RMSNORM, 2ull * (NR + 1) * S + W);
-            return e == cudaSuccess ? launch_status() : AR_ERR_CUDA;
+            auto run = [&](auto clc) -> int {
+                constexpr int CL = decltype(clc)::value;
+                const size_t slice = (hidden / kVecElems<DT> + CL - 1) / CL;
+                const size_t smem = slice * kVecElems<DT> * sizeof(float);
+                static const bool attr_ok =
+                    cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kRmsnormMaxSliceBytes) == cudaSuccess &&
+                    (CL <= 8 || cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
+                                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess);
+                if (!attr_ok) {
+                    cudaGetLastError();
+                    return AR_ERR_CUDA;
+                }
+                cudaLaunchAttribute attr[2];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = CL;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[1].val.programmaticStreamSerializationAllowed = h.pdl ? 1 : 0;
+                cudaLaunchConfig_t cfg{};
+                cfg.gridDim = dim3((unsigned)(tokens * CL));
+                cfg.blockDim = dim3(kNormThreads);
+                cfg.dynamicSmemBytes = smem;
+                cfg.stream = s;
+                cfg.attrs = attr;
+                cfg.numAttrs = 2;
+                rec_begin(h, s);
+                const cudaError_t e = cudaLaunchKernelEx(&cfg, allreduce_rmsnorm_kernel<NR, DT, CL>, ip, residual,
+                                                         weight, eps, op, residual_out, hidden, slice);
+                rec_end(h, s, AR_K_ALLREDUCE_RMSNORM, 2ull * (NR + 1) * S + W);
+                return e == cudaSuccess ? launch_status() : AR_ERR_CUDA;
+            };
+            // few rows: clusters of 16 spread each row over twice the SMs
+            if (tokens * 16 <= (size_t)h.sm_count) return run(std::integral_constant<int, 16>{});
+            return run(std::integral_constant<int, kClusterCtas>{});
         });
     });
 }
