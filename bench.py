@@ -449,8 +449,8 @@ def _graph_us(stream, fn, in_graph: int = 20, replays: int = 10, batches: int = 
     """Device time per call with the host out of the way: `in_graph` calls
     fn(i) captured once into a CUDA graph on `stream`, replayed back to back;
     median over batches, us.  Small calls issued one by one from Python are
-    bound by the host's issue rate (ctypes + launch, ~3 us a call on the
-    GPU machine's Grace CPU), which the replay removes."""
+    bound by the host's issue rate (ctypes + launch, ~3 us a call on a
+    GB300 machine's Grace CPU), which the replay removes."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
