@@ -138,8 +138,12 @@ struct Shape {
 };
 inline Shape narrow_shape(const Handle& h, size_t work, int rows = 1)
 {
+    // never more CTAs than the launch cap (AR_OPT_CTAS_PER_SM) allows
+    const size_t cap = (size_t)h.sm_count * (size_t)(h.ctas_per_sm ? h.ctas_per_sm : kAutoCtasPerSm);
     unsigned block = kThreads;
-    while (block > 32 && ((work + block - 1) / block) * (size_t)rows < (size_t)h.sm_count) block >>= 1;
+    while (block > 32 && ((work + block - 1) / block) * (size_t)rows < (size_t)h.sm_count &&
+           ((work + block / 2 - 1) / (block / 2)) * (size_t)rows <= cap)
+        block >>= 1;
     size_t want = (work + block - 1) / block;
     return Shape{want ? (unsigned)want : 1u, block};
 }

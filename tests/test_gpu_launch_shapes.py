@@ -104,3 +104,25 @@ def test_ll_reduce_forms_at_the_switch(kind, which):
         np.testing.assert_array_equal(o.download(np.uint8), w)
     for b in lines_in + lines_out:
         assert b.guards_intact()
+
+
+@pytest.mark.parametrize("cap", [1, 2])
+@pytest.mark.parametrize("call", list(CALLS))
+def test_small_forms_under_a_cta_cap(call, cap):
+    # AR_OPT_CTAS_PER_SM bounds every launch, the narrowed small forms included: with one or two
+    # CTAs per SM allowed the small calls still cover every element, bit for bit
+    n, dtype = 8, "bf16"
+    for N in (7, 4099, _counts(call, n, dtype)[0]):
+        xs = workloads.rank_inputs(n, N, dtype, "normal_over_n", seed=53 * cap + N)
+        ins, outs = upload_ranks(xs), empty_ranks(n, xs[0].nbytes)
+        fn, ref = CALLS[call]
+        with Handle(n, max(16, N * E[dtype]), ctas_per_sm=cap) as h:
+            assert fn(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+            assert ar.ar_status(h) == ar.AR_OK
+        torch.cuda.synchronize()
+        want = ref(xs, dtype)
+        for r in (0, n - 1):
+            np.testing.assert_array_equal(bits(outs[r].download(np.uint16)), bits(want[r]),
+                                          err_msg=f"{call} cap={cap} N={N}")
+        for b in ins + outs:
+            assert b.guards_intact()
