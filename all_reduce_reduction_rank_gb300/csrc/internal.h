@@ -2,6 +2,7 @@
 // per-file launchers.  Not part of the C-ABI (that is include/ar.h).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <type_traits>
@@ -146,6 +147,24 @@ inline Shape narrow_shape(const Handle& h, size_t work, int rows = 1)
         block >>= 1;
     size_t want = (work + block - 1) / block;
     return Shape{want ? (unsigned)want : 1u, block};
+}
+
+// Kernel attributes (dynamic shared memory size, non-portable cluster size)
+// belong to the device they are set on: a launcher sets them through this,
+// once per device (a bit per device in `done`), with that device current.
+template <typename F>
+inline bool once_per_device(std::atomic<uint32_t>& done, F&& set)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 32) return false;
+    const uint32_t bit = 1u << dev;
+    if (done.load(std::memory_order_acquire) & bit) return true;
+    if (!set()) {
+        cudaGetLastError();
+        return false;
+    }
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
 }
 
 // Launchers: argument checks are done by the caller; these only launch.

@@ -182,15 +182,16 @@ one_shot_bulk_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant
     }
 }
 
-// Opts the kernel into its shared-memory size and returns its CTAs per SM.
+// Opts the kernel into its shared-memory size on the current device (once per
+// device).
 template <int NR, int DT>
-int bulk_blocks_per_sm()
+bool bulk_attributes()
 {
-    constexpr int smem = bulk_smem_bytes<NR>();
-    if (cudaFuncSetAttribute(one_shot_bulk_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        cudaGetLastError();
-    return blocks_per_sm(one_shot_bulk_kernel<NR, DT>, smem);
+    static std::atomic<uint32_t> done{0};
+    return once_per_device(done, [] {
+        return cudaFuncSetAttribute(one_shot_bulk_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bulk_smem_bytes<NR>()) == cudaSuccess;
+    });
 }
 
 }  // namespace
@@ -212,7 +213,8 @@ int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t c
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
             if (h.one_shot_impl == 2) {
                 constexpr int smem = bulk_smem_bytes<NR>();
-                static const int per_sm = bulk_blocks_per_sm<NR, DT>();
+                if (!bulk_attributes<NR, DT>()) return AR_ERR_CUDA;
+                static const int per_sm = blocks_per_sm(one_shot_bulk_kernel<NR, DT>, smem);
                 const size_t ntiles = (nvec * 16 + kBulkTile - 1) / kBulkTile;
                 size_t grid = (size_t)h.sm_count * (size_t)(h.ctas_per_sm ? h.ctas_per_sm : per_sm);
                 if (grid > ntiles) grid = ntiles;

@@ -349,15 +349,15 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
                 ip.p[q] = in[q];
                 op.p[q] = out[q];
             }
-            static const bool attr_ok =
-                cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kClusterSmem) == cudaSuccess &&
-                (NR <= 8 || cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>,
-                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess);
-            if (!attr_ok) {
-                cudaGetLastError();
-                return AR_ERR_CUDA;
-            }
+            static std::atomic<uint32_t> attr_done{0};
+            const bool attr_ok = once_per_device(attr_done, [&] {
+                return cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kClusterSmem) == cudaSuccess &&
+                       (NR <= 8 || cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>,
+                                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                                        1) == cudaSuccess);
+            });
+            if (!attr_ok) return AR_ERR_CUDA;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = NR;

@@ -180,16 +180,16 @@ int launch_allreduce_rmsnorm(Handle& h, const void* const* in, const void* resid
                 constexpr int CL = decltype(clc)::value;
                 const size_t slice = (hidden / kVecElems<DT> + CL - 1) / CL;
                 const size_t smem = slice * kVecElems<DT> * sizeof(float);
-                static const bool attr_ok =
-                    cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kRmsnormMaxSliceBytes) == cudaSuccess &&
-                    (CL <= 8 || cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
-                                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess);
-                if (!attr_ok) {
-                    cudaGetLastError();
-                    return AR_ERR_CUDA;
-                }
+                static std::atomic<uint32_t> attr_done{0};
+                const bool attr_ok = once_per_device(attr_done, [&] {
+                    return cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)kRmsnormMaxSliceBytes) == cudaSuccess &&
+                           (CL <= 8 || cudaFuncSetAttribute(allreduce_rmsnorm_kernel<NR, DT, CL>,
+                                                            cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                                            1) == cudaSuccess);
+                });
+                if (!attr_ok) return AR_ERR_CUDA;
                 cudaLaunchAttribute attr[2];
                 attr[0].id = cudaLaunchAttributeClusterDimension;
                 attr[0].val.clusterDim.x = CL;
