@@ -39,7 +39,12 @@
  *     is set, never in a call).  Host-side argument errors are
  *     returned at once and nothing is launched.  Errors found by a kernel
  *     are sticky in the handle and are returned by ar_status().
- *   - A handle may be used from one host thread at a time.
+ *   - A handle may be used from one host thread at a time.  Its calls share the
+ *     handle's device buffers (the ring's partials, the optional staging,
+ *     registered and inbox buffers, the status word), so calls of one handle
+ *     whose kernels could overlap on the GPU must be ordered: issue them on one
+ *     stream, or order the streams with events.  Calls of different handles are
+ *     independent.
  *
  * Return codes: AR_OK (0) or a negative AR_ERR_* value; ar_strerror() names it.
  */
