@@ -704,13 +704,63 @@ def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     import all_reduce_reduction_rank_gb300 as ar
     for w in sets:
         ar.check(ar.ar_status(w.h), "e2e status")
+    link = _host_link(wl, h_in + h_pay, h_outs[0], sets[1] if len(sets) > 1 else wl)
     for w in extra:
         w.close()
     ms = reduce_scalar(ev0.elapsed_time(ev1), "max") / K
     world = dist_env()[1]
     return {"value": round(world * bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelining": f"{E2E_SETS} buffer sets on {E2E_SETS} streams: copy in, calls, copy out per step"}
+            "pipelining": f"{E2E_SETS} buffer sets on {E2E_SETS} streams: copy in, calls, copy out per step",
+            "host_link_GB/s": link}
+
+
+def _host_link(wl, h_in, h_out, other) -> dict:
+    """This machine's pinned host<->device copy rates, measured on the e2e
+    leg's own buffers after its timed region: the step's inputs host->device,
+    its outputs device->host, and both at once on two streams (median of 3,
+    GB/s).  The e2e figure is bound by these, which vary from machine to
+    machine."""
+    import torch
+
+    d_in = wl.ins + wl.pay
+    d_out = wl.outs + wl.ll_dst + wl.l128_dst
+    b_in = sum(t.numel() * t.element_size() for t in h_in)
+    b_out = sum(t.numel() * t.element_size() for t in h_out)
+
+    def timed(fn):
+        per = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(wl.stream)
+            fn()
+            e1.record(wl.stream)
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(per)
+
+    def h2d(stream=None):
+        with torch.cuda.stream(stream or wl.stream):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+
+    def d2h(stream=None):
+        with torch.cuda.stream(stream or wl.stream):
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+
+    def both():
+        done = torch.cuda.Event()
+        other.stream.wait_stream(wl.stream)
+        h2d(wl.stream)
+        d2h(other.stream)
+        done.record(other.stream)
+        wl.stream.wait_event(done)
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    return {"h2d": round(b_in / t_in / 1e9, 1), "d2h": round(b_out / t_out / 1e9, 1),
+            "both": round((b_in + b_out) / t_both / 1e9, 1)}
 
 
 def run_ours(args):
