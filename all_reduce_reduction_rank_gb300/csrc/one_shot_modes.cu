@@ -20,14 +20,18 @@
 //
 // Both give the one-shot result bit for bit: fp32 sums in rank order from +0,
 // one rounding.
+//
+// Small: a call too small to give every SM a full CTA runs its kernels in
+// narrower CTAs compiled for three CTAs per SM, as the one-shot kernel's small
+// form (blockIdx.y = rank rows; one 16-byte vector per thread).
 #include "common.cuh"
 
 namespace argb {
 namespace {
 
 // stage[q][r] for r != q  <-  in[r].   Grid: blockIdx.y = sending rank r.
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+template <int NR, int DT, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 push_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ stage, size_t slot_bytes, size_t nvec,
             size_t count)
 {
@@ -35,7 +39,8 @@ push_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ stage, s
     using T = typename Payload<DT>::scalar_t;
     const int r = blockIdx.y;
     const uint4* const src = static_cast<const uint4*>(in.p[r]);
-    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+    const size_t bs = Small ? (size_t)blockDim.x : (size_t)kThreads;
+    for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs) {
         const uint4 x = ld16(src + v);
 #pragma unroll
         for (int q = 0; q < NR; ++q)
@@ -55,8 +60,8 @@ push_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ stage, s
 
 // out[q] = rank-order sum of stage[q][0..n-1], with in[q] as rank q's own term.
 // Grid: blockIdx.y = receiving rank q.
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+template <int NR, int DT, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                    const uint8_t* __restrict__ stage, size_t slot_bytes, size_t nvec, size_t count)
 {
@@ -67,7 +72,8 @@ push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__
         return r == q ? in.p[q] : static_cast<const void*>(stage + ((size_t)q * NR + r) * slot_bytes);
     };
     uint4* const dst = static_cast<uint4*>(out.p[q]);
-    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads) {
+    const size_t bs = Small ? (size_t)blockDim.x : (size_t)kThreads;
+    for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs) {
         uint4 x[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) x[r] = ld16(static_cast<const uint4*>(slot(r)) + v);
@@ -86,8 +92,8 @@ push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__
 }
 
 // reg[r] <- in[r] for every rank r.  Grid: blockIdx.y = rank.
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads)
+template <int NR, int DT, bool Small>
+__global__ void __launch_bounds__(kThreads, Small ? 3 : 0)
 copyin_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ reg, size_t slot_bytes, size_t nvec,
               size_t count)
 {
@@ -96,7 +102,8 @@ copyin_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ reg, s
     const int r = blockIdx.y;
     const uint4* const src = static_cast<const uint4*>(in.p[r]);
     uint4* const dst = reinterpret_cast<uint4*>(reg + (size_t)r * slot_bytes);
-    for (size_t v = (size_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (size_t)gridDim.x * kThreads)
+    const size_t bs = Small ? (size_t)blockDim.x : (size_t)kThreads;
+    for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs)
         st16(dst + v, ld16(src + v));
     pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
@@ -123,13 +130,25 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
             const size_t nvec = count / kVecElems<DT>;
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
             const dim3 grid(grid_for_rows(h, nvec, NR), NR);
+            const bool small = grid.x * NR < (unsigned)h.sm_count;   // narrower CTAs, as one-shot's small form
+            const Shape sh = narrow_shape(h, nvec, NR);
+            const dim3 g_small(sh.grid_x, NR);
             rec_begin(h, s);
-            launch_kernel(h, push_kernel<NR, DT>, grid, kThreads, 0, s, ip, h.push_stage, h.stage_slot, nvec, count);
+            if (small)
+                launch_kernel(h, push_kernel<NR, DT, true>, g_small, sh.block, 0, s, ip, h.push_stage, h.stage_slot,
+                              nvec, count);
+            else
+                launch_kernel(h, push_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, h.push_stage, h.stage_slot,
+                              nvec, count);
             rec_end(h, s, AR_K_PUSH, (uint64_t)NR * S + (uint64_t)NR * (NR - 1) * S);
             if (launch_status() != AR_OK) return AR_ERR_CUDA;
             rec_begin(h, s);
-            launch_kernel(h, push_reduce_kernel<NR, DT>, grid, kThreads, 0, s, ip, op,
-                          (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
+            if (small)
+                launch_kernel(h, push_reduce_kernel<NR, DT, true>, g_small, sh.block, 0, s, ip, op,
+                              (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
+            else
+                launch_kernel(h, push_reduce_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, op,
+                              (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
             rec_end(h, s, AR_K_PUSH_REDUCE, (uint64_t)NR * NR * S + (uint64_t)NR * S);
             *launches = 2;
             return launch_status();
@@ -148,9 +167,15 @@ int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, s
             for (int q = 0; q < NR; ++q) ip.p[q] = in[q];
             const size_t nvec = count / kVecElems<DT>;
             const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+            const dim3 grid(grid_for_rows(h, nvec, NR), NR);
+            const Shape sh = narrow_shape(h, nvec, NR);
             rec_begin(h, s);
-            launch_kernel(h, copyin_kernel<NR, DT>, dim3(grid_for_rows(h, nvec, NR), NR), kThreads, 0, s, ip,
-                          h.registered, h.stage_slot, nvec, count);
+            if (grid.x * NR < (unsigned)h.sm_count)   // narrower CTAs, as one-shot's small form
+                launch_kernel(h, copyin_kernel<NR, DT, true>, dim3(sh.grid_x, NR), sh.block, 0, s, ip, h.registered,
+                              h.stage_slot, nvec, count);
+            else
+                launch_kernel(h, copyin_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, h.registered, h.stage_slot,
+                              nvec, count);
             rec_end(h, s, AR_K_COPYIN, 2ull * NR * S);
             return launch_status();
         });
