@@ -103,3 +103,20 @@ def test_every_call_with_signed_zeros_infinities_and_nans(dtype):
                 assert np.array_equal(np.isnan(gf), np.isnan(wf)), name
                 keep = ~np.isnan(wf)
                 np.testing.assert_array_equal(bits(got)[keep], bits(want[r])[keep], err_msg=f"{name} rank {r}")
+
+
+def test_every_call_with_count_zero_is_a_no_op():
+    # count 0: AR_OK, no launch, no byte of any buffer touched, for every all-reduce call
+    n = 8
+    with Handle(n, 1 << 12, push_staging=1, registered=1, persistent=1) as h:
+        ins, outs = empty_ranks(n, 64, byte=0x11), empty_ranks(n, 64, byte=0x33)
+        for name, (call, _) in CALLS.items():
+            assert call(h, ptrs(ins), ptrs(outs), 0, "bf16") == ar.AR_OK, name
+            t = ar.ar_traffic(h)
+            assert t.launches == 0 and t.hbm_read_bytes == 0 and t.hbm_write_bytes == 0, name
+        assert ar.ar_status(h) == ar.AR_OK
+    torch.cuda.synchronize()
+    assert all(bool((b.body() == 0x11).all()) for b in ins)
+    assert all(bool((b.body() == 0x33).all()) for b in outs)
+    for b in ins + outs:
+        assert b.guards_intact()
