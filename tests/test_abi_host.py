@@ -362,3 +362,23 @@ def test_plan_ring_fused(lib, op, n):
     assert _check(getattr(ar, op), n, ins, ins, 1000) == ar.AR_OK   # in place
     outs[1] = outs[0]
     assert _check(getattr(ar, op), n, ins, outs, 1000) == ar.AR_ERR_INVALID
+
+
+def _header_constants():
+    text = open(os.path.join(ROOT, "include", "ar.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return {k: int(v) for k, v in re.findall(r"\b(AR_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    # every enum value of include/ar.h has the same value in the Python binding, and
+    # every kernel id its name in ar.KERNELS (what ar_timing reports)
+    consts = _header_constants()
+    assert len(consts) >= 60
+    kernels = {v: k[len("AR_K_"):].lower() for k, v in consts.items() if k.startswith("AR_K_")}
+    assert kernels == ar.KERNELS
+    for name, value in consts.items():
+        if name.startswith("AR_K_"):
+            continue
+        assert getattr(ar, name) == value, name
+    assert ar.DTYPES == {"f32": consts["AR_F32"], "bf16": consts["AR_BF16"], "f16": consts["AR_F16"]}
