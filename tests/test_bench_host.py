@@ -77,3 +77,24 @@ def test_warmup_below_three_is_refused():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_traffic_is_reported_only_for_the_captured_source(monkeypatch, tmp_path):
+    # the committed ncu summary is used while the kernel's sources hash to the captured value,
+    # scaled to the launch by algorithmic bytes; a changed source or a missing entry gives None
+    # (the sources' real hashes are not checked here: a kernel edited since its capture simply
+    # reports no traffic until it is captured again)
+    import json
+
+    import bench
+
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: rec[kernel]["source_sha256"])
+    for kernel, r in rec.items():
+        got = bench.ncu_traffic(kernel, r["algorithmic_bytes_per_launch"])
+        assert got == pytest.approx(r["dram_bytes_per_launch"])
+        assert bench.ncu_traffic(kernel, 2 * r["algorithmic_bytes_per_launch"]) == pytest.approx(
+            2 * r["dram_bytes_per_launch"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0" * 64)
+    assert all(bench.ncu_traffic(k, 1.0) is None for k in rec)
+    assert bench.ncu_traffic("no_such_kernel", 1.0) is None
