@@ -17,11 +17,17 @@ device time.  The 1.3 GiB per-step working set is 10x the 129 MB L2, so no
 flush is needed between steps.  Per-kernel times come from the library's
 own launch record (CUDA events on the launching stream, AR_OPT_TIMING).
 
-Beside the timed steps the JSON line carries: a decode/prefill sweep of
-one-shot and two-shot, the fused all-reduce + RMSNorm epilogue, every
-all-reduce call side by side (variants), the LL payload sweep, the n = 16
-doubling sweep, an end-to-end leg through host buffers (e2e), and the oracle
-timed on the host (cpu_baseline, cpu_parallel, cpu_calls).
+The run ends with ONE short JSON line (under 2 KB): the headline value, the
+roofline of the dominant kernel (algorithmic and DRAM rates), the oracle
+timed on the host (cpu_baseline), the end-to-end leg through host buffers
+(e2e) and the SM clocks seen during the timed region.  Everything else it
+measures goes to a details file (--details, default
+gpurun_out/bench_details.json): a decode/prefill sweep of one-shot and
+two-shot, the fused all-reduce + RMSNorm epilogue, every all-reduce call
+side by side (variants), the LL payload sweep, the n = 16 doubling sweep,
+the per-kernel table and the other CPU legs (cpu_parallel, cpu_calls).
+Rows whose algorithmic rate is above the measured copy peak are marked
+l2_assisted.
 
 --impl reference times the CPU oracle instead (the reference arm), on a
 bounded sample of the same workload.  Multi-GPU runs (torchrun) are
@@ -102,6 +108,19 @@ def step_bytes(n: int, N: int, e: int, ll_count: int) -> dict:
             t = ar.ar_plan(op, n, ll_count, "f32")
             b += t.hbm_read_bytes + t.hbm_write_bytes
         rows[kind] = b
+    return rows
+
+
+def step_bytes_model(n: int, N: int, e: int, ll_count: int) -> dict:
+    """The same per-row bytes from the oracle's closed forms (oracle/model.py),
+    for the legs that run the oracle and must not load the CUDA library."""
+    from oracle import model
+    rows = {"one_shot": sum(model.hbm_one_shot(n, N, e)), "two_shot": sum(model.hbm_two_shot(n, N, e)),
+            "ring": sum(model.hbm_ring(n, N, e))}
+    rows["ll"] = sum(model.hbm_ll_pack(ll_count)) * n + sum(model.hbm_ll_reduce(n, ll_count)) + \
+        sum(model.hbm_ll_unpack(ll_count)) * n
+    rows["ll128"] = sum(model.hbm_ll128_pack(ll_count)) * n + sum(model.hbm_ll128_reduce(n, ll_count)) + \
+        sum(model.hbm_ll128_unpack(ll_count)) * n
     return rows
 
 
@@ -372,7 +391,7 @@ def sweep(wl, peak: float, batches: int = 7, min_calls: int = 64) -> dict:
                 row["graph_us"] = round(_graph_us(wl.stream, lambda i: call(wl.h, pin[i % slots], pout[i % slots],
                                                                             N, 1, wl.s)), 3)
                 ar.check(ar.ar_status(wl.h), algo)
-            res[algo].append(row)
+            res[algo].append(mark_l2(row, peak))
     return res
 
 
@@ -517,10 +536,11 @@ def ll_sweep(wl, peak: float, batches: int = 5) -> dict:
             # device time per pass: 20 passes (their step ids fixed at capture) replayed from a graph
             gus = _graph_us(wl.stream, one)
             ar.check(ar.ar_status(h), kind + " sweep, graph")
-            out[kind].append({"payload_bytes": P, "us_per_pass": round(us, 3), "graph_us_per_pass": round(gus, 3),
-                              "payload_GB/s": round(n * P / (us * 1e-6) / 1e9, 2),
-                              "wire_efficiency": round(wire, 4), "hbm_GB/s": round(b / (us * 1e-6) / 1e9, 1),
-                              "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4)})
+            out[kind].append(mark_l2({"payload_bytes": P, "us_per_pass": round(us, 3),
+                                      "graph_us_per_pass": round(gus, 3),
+                                      "payload_GB/s": round(n * P / (us * 1e-6) / 1e9, 2),
+                                      "wire_efficiency": round(wire, 4), "hbm_GB/s": round(b / (us * 1e-6) / 1e9, 1),
+                                      "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4)}, peak))
     return out
 
 
@@ -570,12 +590,12 @@ def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
                     t = ar.ar_plan(op, n, count, dtype)
                     gbs = (t.hbm_read_bytes + t.hbm_write_bytes) / (us * 1e-6) / 1e9
                     gus = round(_graph_us(stream, one), 3) if S <= GRAPH_MAX_BYTES else None
-                    rows.append([S, round(us, 2), round(gbs, 1), gus])
+                    rows.append([S, round(us, 2), round(gbs, 1), gus, gbs > peak])
                 ar.check(ar.ar_status(h), name)
                 res[f"{dtype}/{name}"] = rows
     finally:
         ar.ar_destroy(h)
-    return {"columns": ["bytes_per_rank", "us", "hbm_GB/s", "graph_us"], "peak": peak, **res}
+    return {"columns": ["bytes_per_rank", "us", "hbm_GB/s", "graph_us", "l2_assisted"], "peak": peak, **res}
 
 
 VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
@@ -647,7 +667,7 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
                 row["graph_us"] = round(_graph_us(wl.stream, lambda i: call(h, pin[i % slots], pout[i % slots],
                                                                             N, 1, wl.s)), 3)
                 ar.check(ar.ar_status(h), name)
-            res[name].append(row)
+            res[name].append(mark_l2(row, peak))
     for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
         ar.check(ar.ar_set_option(h, opt, 0), "variant buffers")
     return res
@@ -817,7 +837,9 @@ def run_ours(args):
     traffic = ncu_traffic(dom, dk["bytes_per_launch"])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dk["GB/s"], 1), "peak": peak, "unit": "GB/s",
                 "frac": round(dk["GB/s"] / peak, 4), "traffic": traffic,
-                "bytes_per_launch": dk["bytes_per_launch"], "peak_source": peak_src}
+                "bytes_per_launch": dk["bytes_per_launch"], "us_per_launch": round(dk["us_per_launch"], 3),
+                "peak_source": peak_src}
+    roofline.update(dram_rate(traffic, dk["us_per_launch"], peak))
 
     sw = sweep(wl, peak) if args.sweep else None
     fe = fused_epilogue(wl, peak) if args.sweep else None
@@ -831,7 +853,7 @@ def run_ours(args):
         cpu_par = cpu_parallel(seconds=args.cpu_seconds)
         cpu_calls = calls_cpu() if args.sweep else None
     wl.close()
-    line = {
+    full = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -847,11 +869,91 @@ def run_ours(args):
         "launch_timing": {"steps_sampled": sampled, "every": every, "records": len(records),
                           "launches_recorded": sum(r[4] for r in records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),
-        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "cpu_parallel": cpu_par, "cpu_calls": cpu_calls, "sweep": sw,
-        "fused_epilogue": fe, "variants": va, "ll_sweep": lls, "n16_sweep": n16,
+        "clocks": clocks.summary(t_wall0, t_wall1), "e2e": e2e, "cpu_baseline": cpu, "cpu_parallel": cpu_par,
+        "cpu_calls": cpu_calls, "sweep": sw, "fused_epilogue": fe, "variants": va, "ll_sweep": lls,
+        "n16_sweep": n16,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        path = write_details(full, args.details)
+        print(json.dumps(headline(full, path)), flush=True)
+
+
+def dram_rate(traffic, us_per_launch: float, peak: float) -> dict:
+    """The dominant kernel's DRAM rate beside its algorithmic one: ncu's
+    DRAM bytes per launch over the same average launch time.  An algorithmic
+    rate above the copy peak with a DRAM rate below it means L2 served part
+    of the algorithmic bytes."""
+    if traffic is None or not us_per_launch:
+        return {"dram_achieved": None, "dram_frac": None}
+    a = traffic / (us_per_launch * 1e-6) / 1e9
+    return {"dram_achieved": round(a, 1), "dram_frac": round(a / peak, 4)}
+
+
+def mark_l2(row: dict, peak: float, key: str = "hbm_GB/s") -> dict:
+    """Flag a row whose algorithmic rate is above the measured copy peak:
+    such a rate is only reachable with part of its bytes served by L2."""
+    v = row.get(key)
+    if v is not None and v > peak:
+        row["l2_assisted"] = True
+    return row
+
+
+HEADLINE_MAX_BYTES = 2000
+
+
+def headline(full: dict, details_path: str | None) -> dict:
+    """The one JSON line the run ends with: the headline figures only (the
+    sweeps and per-kernel tables go to the details file).  Kept under
+    HEADLINE_MAX_BYTES so that a reader keeping the tail of stdout has it
+    whole."""
+    cfg = full["config"]
+    rf = full.get("roofline") or {}
+    keep_rf = ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic", "bytes_per_launch",
+               "us_per_launch", "dram_achieved", "dram_frac")
+    cpu = full.get("cpu_baseline")
+    e2e = full.get("e2e")
+    clk = full.get("clocks")
+    line = {k: full[k] for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data")}
+    line["config"] = {"workload": cfg["workload"], "n_ranks": cfg["n_ranks"], "bytes_per_rank": cfg["bytes_per_rank"],
+                      "ll_payload_bytes_per_rank": cfg["ll_payload_bytes_per_rank"],
+                      "bytes_per_step": cfg["bytes_per_step"], "l2": "no flush: 1.3 GiB per step > 129 MB L2",
+                      "parallelism": cfg["parallelism"]}
+    line["frac_of_peak"] = full.get("frac_of_peak")
+    line["frac_of_8tbs"] = full.get("frac_of_8tbs")
+    line["roofline"] = {k: rf.get(k) for k in keep_rf}
+    if rf.get("peak_source"):
+        line["roofline"]["peak_source"] = "measured" if rf["peak_source"].startswith("measured") else "fallback"
+    line["cpu_baseline"] = None if cpu is None else {
+        "value": cpu["value"], "unit": cpu["unit"], "cores": cpu["cores"], "kind": cpu["kind"],
+        "sample": cpu["sample"][:200]}
+    line["e2e"] = None if e2e is None else {
+        k: e2e[k] for k in ("value", "unit", "ms_per_step", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+    line["clocks"] = None if clk is None else {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    line["gpu_launches"] = full["gpu_launches"]
+    line["details"] = details_path
+    if len(json.dumps(line)) > HEADLINE_MAX_BYTES:      # never expected; keep the line whole regardless
+        line["cpu_baseline"] and line["cpu_baseline"].update(sample=line["cpu_baseline"]["sample"][:60])
+        line["details"] = os.path.basename(details_path) if details_path else None
+    return line
+
+
+def write_details(full: dict, path: str | None) -> str | None:
+    """Everything the run measured (sweeps, variants, per-kernel table, CPU
+    legs) as one JSON file; returns its path, or None if it cannot be
+    written (the headline line is printed regardless)."""
+    if not path:
+        return None
+    if not os.path.isabs(path):
+        path = os.path.join(ROOT, path)
+    try:
+        os.makedirs(os.path.dirname(path), exist_ok=True)
+        with open(path, "w") as f:
+            json.dump(full, f, indent=1)
+    except OSError as exc:
+        print(f"bench: details not written ({exc})", file=sys.stderr)
+        return None
+    return os.path.relpath(path, ROOT)
 
 
 # --------------------------------------------------------------------------
@@ -867,7 +969,7 @@ def oracle_sample(scale_div: int, seed: int = 1003):
     c = ((1 * MiB) // 4) // scale_div
     xs = workloads.rank_inputs(n, N, "bf16", "normal", seed)
     ps = workloads.payload_f32(n, c, seed + 1)
-    rows = step_bytes(n, N, 2, c)
+    rows = step_bytes_model(n, N, 2, c)
 
     def run(step_id: int):
         oracle.all_reduce(xs, "bf16")
@@ -918,7 +1020,7 @@ def cpu_parallel(seconds: float = 10.0, scale_div: int = 32) -> dict:
     ps = workloads.payload_f32(n, c, 1004)
     C = oracle.chunk_elems(n, N, "bf16")
     chunk = (np.arange(N) // C).astype(np.int32)
-    b = sum(step_bytes(n, N, 2, c).values())
+    b = sum(step_bytes_model(n, N, 2, c).values())
     cores = os.cpu_count() or 1
     # element ranges: multiples of 30 words keep LL128 lines whole
     def ranges(total, align):
@@ -1060,6 +1162,9 @@ def main(argv=None):
     p.add_argument("--ctas-per-sm", type=int, default=0, help="AR_OPT_CTAS_PER_SM (0 auto)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--details", default=os.path.join("gpurun_out", "bench_details.json"),
+                   help="JSON file for everything beyond the headline line (sweeps, variants, per-kernel "
+                        "table, CPU legs); '' for none")
     p.add_argument("--reference-budget", type=float, default=150.0,
                    help="seconds the reference arm's warm-up + timed steps should take in all")
     args = p.parse_args(argv)
