@@ -10,8 +10,11 @@
 // exits.  Host code never uses the array's name as an address: the first call
 // on a device, with that device current, asks the runtime for the array's
 // device address (cudaGetSymbolAddress) and the SM count, checks the result,
-// and keeps both for later calls on that device.  Make that first call before
-// any stream capture.
+// and keeps both for later calls on that device.  Only a successful lookup is
+// kept: a call whose lookup fails returns AR_ERR_CUDA and the next call on
+// that device tries again.  Make that first call before any stream capture
+// (the lookup may have to load the library's device code, which a capture
+// does not allow).
 //
 // All calls share the one array, which keeps whatever the last call left in
 // it.  Nothing in it has to start at zero: each call writes every partial
@@ -21,6 +24,7 @@
 // The kernels are variants of the ring step kernels of ring.cu (same chunks,
 // same rotation, same fp32 partials, same single rounding), reading and
 // writing their partials in the static array.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -34,36 +38,47 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) float g_ring_scratch[kNoAllocScratchBytes / sizeof(float)];
 
 struct DeviceSetup {
-    std::once_flag once;
-    int rc = AR_ERR_CUDA;
+    std::mutex mu;
+    std::atomic<bool> ready{false};
     float* scratch = nullptr;  // device address of g_ring_scratch on this device
     int sm_count = 0;
 };
 
 DeviceSetup g_setup[kMaxDevices];
 
-// Runs once per device, on the first call made with that device current.
+// The device address of the array and the SM count, looked up on the first
+// call made with that device current and kept once the lookup succeeds.  A
+// failed lookup keeps nothing, so a later call retries it; it clears the
+// runtime's last-error state only if no error was pending before it.
 int device_setup(int dev, DeviceSetup** out)
 {
     if (dev < 0 || dev >= kMaxDevices) return AR_ERR_CUDA;
     DeviceSetup& d = g_setup[dev];
-    std::call_once(d.once, [&] {
-        void* p = nullptr;
-        int sms = 0;
-        if (cudaGetSymbolAddress(&p, g_ring_scratch) != cudaSuccess || p == nullptr ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
-            cudaGetLastError();
-            d.rc = AR_ERR_CUDA;
-            return;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(d.mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            const bool pending = cudaPeekAtLastError() != cudaSuccess;
+            void* p = nullptr;
+            int sms = 0;
+            if (cudaGetSymbolAddress(&p, g_ring_scratch) != cudaSuccess || p == nullptr ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+                if (!pending) cudaGetLastError();
+                return AR_ERR_CUDA;
+            }
+            d.scratch = static_cast<float*>(p);
+            d.sm_count = sms;
+            d.ready.store(true, std::memory_order_release);
         }
-        d.scratch = static_cast<float*>(p);
-        d.sm_count = sms;
-        d.rc = AR_OK;
-    });
+    }
     *out = &d;
-    return d.rc;
+    return AR_OK;
 }
 
+// Grid cap: the library's default launch policy (at most 64 CTAs per SM per
+// launch, shared by the n rank rows, the CTAs grid-striding past that), the
+// same cap ar_ring's step launches use when no AR_OPT_CTAS_PER_SM is set.
+// Many short-lived CTAs let the block scheduler balance the SMs; measured on
+// GB300 they beat one resident wave of grid-striding CTAs by 5-14%.
 constexpr int kCtasPerSm = 64;
 
 // Reduce-scatter step s: rank r sends chunk (r - s) mod n to rank r + 1, which

@@ -599,6 +599,7 @@ def n16_sweep(dev, peak: float, batches: int = 3) -> dict:
 
 
 VARIANT_SIZES = (64 * 1024, 1 * MiB, 8 * MiB, 64 * MiB)
+NOALLOC_MAX_BYTES = 8 * MiB   # ar_ring_noalloc's static scratch holds n = 8 bf16 up to this per rank
 E2E_SETS = 3   # device buffer sets the e2e leg rotates over
 
 
@@ -607,7 +608,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
     64 KiB, 1 MiB, 8 MiB and 64 MiB per rank: one-shot, its push and copy-in
     forms, two-shot, the ring (one launch per step), the ring with hop
     rounding, the persistent single-launch LL128 ring (global-memory inboxes,
-    and over a thread-block cluster) and the pairwise tree.
+    and over a thread-block cluster), the pairwise tree, the one-pass forms,
+    and the handle-free ring (ar_ring_noalloc, up to its 8 MiB limit).
     Timing as in `sweep` (back-to-back calls on rotating slots, one event pair
     per batch, median of the batches); bytes are each call's algorithmic HBM
     bytes (ar_plan)."""
@@ -631,7 +633,10 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
              ("ring_fused", L.ar_ring_fused, ar.AR_OP_RING_FUSED),
              ("ring_rounded_fused", L.ar_ring_rounded_fused, ar.AR_OP_RING_ROUNDED_FUSED),
              ("tree", L.ar_tree, ar.AR_OP_TREE),
-             ("tree_fused", L.ar_tree_fused, ar.AR_OP_TREE_FUSED))
+             ("tree_fused", L.ar_tree_fused, ar.AR_OP_TREE_FUSED),
+             # the handle-free ring (static scratch, up to 8 MiB per rank at n = 8 bf16)
+             ("ring_noalloc", lambda _h, pi, po, cnt, dt, st: L.ar_ring_noalloc(n, pi, po, cnt, dt, st),
+              ar.AR_OP_RING))
     res = {a[0]: [] for a in algos}
     for S in VARIANT_SIZES:
         if S > wl.S:
@@ -643,6 +648,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
         pout = [P(wl.outs, k) for k in range(slots)]
         calls = max(min_calls, min(slots, 4096))
         for name, call, op in algos:
+            if name == "ring_noalloc" and S > NOALLOC_MAX_BYTES:
+                continue
             t = ar.ar_plan(op, n, N, "bf16")
             b = t.hbm_read_bytes + t.hbm_write_bytes
             for k in range(min(slots, 4)):

@@ -359,8 +359,10 @@ int ar_ring_cluster(ar_handle h, const void* const* in, void* const* out, size_t
  *     elements in all: 8 MiB of bf16 per rank at n = 8); larger calls
  *     return AR_ERR_TOO_LARGE.
  *   - The first call on a device, with that device current, looks up the
- *     array's device address and the SM count once; make that first call
- *     before any stream capture.
+ *     array's device address and the SM count and keeps them; make that
+ *     first call before any stream capture.  Only a successful lookup is
+ *     kept: a call whose lookup fails returns AR_ERR_CUDA, and the next call
+ *     on that device looks up again.
  *   - Every call shares the array and leaves its partials in it; nothing in
  *     it needs to start at zero.  Calls whose kernels overlap on the GPU
  *     race on it: issue them in order on one stream.
