@@ -32,12 +32,14 @@ AR_OK, AR_ERR_INVALID, AR_ERR_ALIGN, AR_ERR_TOO_LARGE, AR_ERR_CUDA, AR_ERR_FLAG_
 AR_OPT_CTAS_PER_SM, AR_OPT_SPIN_NS, AR_OPT_ONE_SHOT_IMPL, AR_OPT_TIMING, AR_OPT_TIMING_PAUSE, AR_OPT_PDL = 1, 2, 3, 4, 5, 6
 AR_OPT_AUTO_POLICY, AR_OPT_AUTO_ALPHA_NS, AR_OPT_AUTO_BETA_MBS, AR_OPT_AUTO_HANDOFF = 7, 8, 9, 10
 AR_OPT_PUSH_STAGING, AR_OPT_REGISTERED, AR_OPT_PERSISTENT, AR_OPT_ABSENT_RANK = 11, 12, 13, 14
+AR_OPT_TWO_SHOT_IMPL = 15
 AR_AUTO_MODEL, AR_AUTO_EMULATED = 0, 1
 KERNELS = {1: "one_shot", 2: "reduce_scatter", 3: "all_gather", 4: "ring_rs_step", 5: "ring_ag_step",
            6: "ll_pack", 7: "ll_unpack", 8: "ll_reduce", 9: "ll128_pack", 10: "ll128_unpack",
            11: "ll128_reduce", 12: "allreduce_rmsnorm", 13: "push", 14: "push_reduce",
            15: "ring_rs_step_rounded", 16: "tree_level", 17: "ring_persistent",
-           18: "copyin", 19: "ring_cluster", 20: "tree_fused", 21: "ring_fused", 22: "ring_rounded_fused"}
+           18: "copyin", 19: "ring_cluster", 20: "tree_fused", 21: "ring_fused", 22: "ring_rounded_fused",
+           23: "two_shot"}
 
 # C symbols the header declares (checked by the CPU tests against include/ar.h)
 EXPORTS = (

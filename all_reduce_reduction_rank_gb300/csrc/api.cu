@@ -142,7 +142,7 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         // summed over ranks that is 2 (n-1) S for any chunking.
         t->link_bytes_per_rank = 2.0 * (double)(nn - 1) * (double)S / (double)nn;
         t->steps = 2;
-        t->launches = count ? 2 : 0;
+        t->launches = count ? (two_shot_one_launch(0, S) ? 1 : 2) : 0;  // the default form's launches
         t->hbm_read_bytes = (nn + 1) * S;
         t->hbm_write_bytes = nn * S;
         break;
@@ -458,10 +458,17 @@ int ar_create(int n_ranks, size_t max_bytes, ar_handle* out)
         rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaMalloc(&h.status, sizeof(DevStatus)) != cudaSuccess) rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaMemset(h.status, 0, sizeof(DevStatus)) != cudaSuccess) rc = AR_ERR_CUDA;
+    // the one-launch two-shot's counters and tile flags: zero, so no flag matches a call's epoch (>= 1)
+    h.two_shot_sync_words = two_shot_sync_words(n_ranks, max_bytes);
+    if (rc == AR_OK && cudaMalloc(&h.two_shot_sync, h.two_shot_sync_words * sizeof(unsigned)) != cudaSuccess)
+        rc = AR_ERR_CUDA;
+    if (rc == AR_OK && cudaMemset(h.two_shot_sync, 0, h.two_shot_sync_words * sizeof(unsigned)) != cudaSuccess)
+        rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaDeviceSynchronize() != cudaSuccess) rc = AR_ERR_CUDA;
     if (rc != AR_OK) {
         if (h.ring_scratch) cudaFree(h.ring_scratch);
         if (h.status) cudaFree(h.status);
+        if (h.two_shot_sync) cudaFree(h.two_shot_sync);
         cudaGetLastError();
         c->magic = 0;
         delete c;
@@ -479,6 +486,7 @@ int ar_destroy(ar_handle hd)
         int r = cudaDeviceSynchronize() == cudaSuccess ? AR_OK : AR_ERR_CUDA;
         if (cudaFree(h->ring_scratch) != cudaSuccess) r = AR_ERR_CUDA;
         if (cudaFree(h->status) != cudaSuccess) r = AR_ERR_CUDA;
+        if (cudaFree(h->two_shot_sync) != cudaSuccess) r = AR_ERR_CUDA;
         if (h->push_stage && cudaFree(h->push_stage) != cudaSuccess) r = AR_ERR_CUDA;
         if (h->registered && cudaFree(h->registered) != cudaSuccess) r = AR_ERR_CUDA;
         if (h->persist && cudaFree(h->persist) != cudaSuccess) r = AR_ERR_CUDA;
@@ -506,6 +514,10 @@ int ar_set_option(ar_handle hd, int option, int64_t value)
     case AR_OPT_ONE_SHOT_IMPL:
         if (value < 0 || value > 2) return AR_ERR_INVALID;
         h->one_shot_impl = (int)value;
+        return AR_OK;
+    case AR_OPT_TWO_SHOT_IMPL:
+        if (value < 0 || value > 3) return AR_ERR_INVALID;
+        h->two_shot_impl = (int)value;
         return AR_OK;
     case AR_OPT_AUTO_POLICY:
         if (value != AR_AUTO_MODEL && value != AR_AUTO_EMULATED) return AR_ERR_INVALID;

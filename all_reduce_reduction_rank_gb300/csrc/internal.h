@@ -49,6 +49,9 @@ struct Handle {
     size_t stage_slot = 0;          // max_bytes rounded up to 256
     uint8_t* persist = nullptr;     // ar_ring_persistent's inboxes, acks, abort word (AR_OPT_PERSISTENT)
     int persist_absent = -1;        // AR_OPT_ABSENT_RANK
+    int two_shot_impl = 0;          // AR_OPT_TWO_SHOT_IMPL
+    unsigned* two_shot_sync = nullptr;  // the one-launch two-shot's counters and tile flags
+    size_t two_shot_sync_words = 0;
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements
     DevStatus* status = nullptr;    // device
@@ -84,6 +87,11 @@ inline size_t chunk_elems(int n, size_t N, int dt)
     size_t q = 16u / elem_bytes(dt);
     return (per + q - 1) / q * q;
 }
+
+// ar_two_shot's form: AR_OPT_TWO_SHOT_IMPL 1 = two launches, 2 = one launch
+// (per-tile CTA barrier), 3 = one launch (per-tile flags between CTAs);
+// 0 (auto) = form 2, measured fastest at every size on GB300.
+inline bool two_shot_one_launch(int impl, uint64_t /*bytes_per_rank*/) { return impl != 1; }
 
 // CTAs of `kernel` (kThreads threads, no dynamic shared memory) that fit on
 // one SM at once.  Callers cache it in a function-local static per kernel
@@ -172,6 +180,7 @@ int launch_one_shot(Handle& h, const void* const* in, void* const* out, size_t c
                     cudaStream_t s, int* launches);
 int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                     cudaStream_t s, int* launches);
+size_t two_shot_sync_words(int n, size_t max_bytes);
 int launch_ring(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                 cudaStream_t s, int* launches);
 int launch_ring_rounded(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,

@@ -1,17 +1,19 @@
 // Persistent ring all-reduce over a thread-block cluster: the ranks are the
 // CTAs of one cluster and a hop goes through distributed shared memory.
 //
-// The same protocol and sums as ring_persistent.cu (handbook "集合通信：NCCL
-// 的算法、协议与推理框架的定制 all-reduce", §协议: LL128 lines of 120 bytes of
-// data and an 8-byte flag, the receiver polling the flag; "多 GPU 与 NCCL",
-// §ring all-reduce: the steps and chunk rotation; fp32 partials, chunk c
-// summed from rank c, rounded once), so the result equals ar_ring's bit for
-// bit.  What differs is where the receiving inbox lives: in the receiving
-// CTA's shared memory, written by the sending CTA of the same cluster with
-// st.shared::cluster.  On this GPU a flag round trip through distributed
-// shared memory takes ~0.53 us against ~1.7 us through global memory, and
-// the lines never touch L2 or HBM: HBM sees only the ranks' own elements and
-// outputs, 2 n S per call, as one-shot does.
+// The same steps, lines and sums as ring_persistent.cu (handbook "集合通信：
+// NCCL 的算法、协议与推理框架的定制 all-reduce", §协议: LL128 lines of 120
+// bytes of data and an 8-byte flag; "多 GPU 与 NCCL", §ring all-reduce: the
+// steps and chunk rotation; fp32 partials, chunk c summed from rank c,
+// rounded once), so the result equals ar_ring's bit for bit.  What differs is
+// how a hop travels: the sending CTA writes the lines straight into the
+// receiving CTA's shared memory with asynchronous stores (st.async), each of
+// which counts its bytes on the receiving slot's mbarrier (complete_tx).
+// The receiver waits on that one barrier instead of polling 32 flags, and the
+// sender neither waits for its stores nor fences them: the barrier's
+// transaction count is what makes a batch visible.  The lines still carry
+// their LL128 flag (the batch number + 1), which the receiver checks.  HBM
+// sees only the ranks' own elements and outputs: 2 n S per call.
 //
 // Layout: cluster size n (one CTA per rank, cluster_ctarank = rank);
 // cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of 960
@@ -20,26 +22,24 @@
 // batches b = w, w+8, ... of the slice and exchanges lines only with warp w
 // of ranks r-1 and r+1.
 //
-// Shared memory of a CTA: per warp kSlots inbox slots of 32 lines (one batch
-// each), the per-warp count of batches its receiver has consumed, and an
-// abort word.  The sender writes batch q into slot q % kSlots once the
-// receiver has consumed batch q - kSlots; a line's flag is q + 1.  A warp
-// walks its (step, batch) pairs in one software-pipelined loop: it issues
-// the loads of the next pair's own elements before it sends the current
-// one, and publishes a consumed slot after its own send (one fence serves
-// both), which needs a step's batches to fit in kSlots - 1 slots.  Shared
-// memory is zeroed at the start, behind a cluster barrier, so no flag of an
-// earlier launch survives; a cluster barrier at the end keeps every CTA
-// alive until no peer can still write into it.
+// Shared memory of a CTA: per warp kSlots inbox slots of 32 lines; per slot a
+// "full" mbarrier (the receiver's: one arrival, the sender's expect_tx, plus
+// the slot's bytes) and an "empty" mbarrier (the sender's: one arrival by the
+// receiver once it has read the slot); an abort word.  Batch q of a warp goes
+// to slot q % kSlots; its use u = q / kSlots completes phase u of both
+// barriers.  The receiver frees a slot as soon as it has read it, before its
+// own send, so a step's batches may fill all kSlots slots: a warp's batches
+// per step are capped at kSlots, or at step 0 (every rank sending, none
+// receiving yet) every rank would wait on its successor.
 //
-// Ordering: data stores to the peer, __syncwarp, fence.acq_rel.cluster, flag
-// stores; the receiver polls its flags with ld.acquire.cluster, __syncwarp,
-// then reads the lines; the consumed count is a relaxed store after the
-// same fence.  Every wait is bounded by spin_ns and a poll count; a
-// wait that runs out records AR_ERR_FLAG_TIMEOUT (a line) or
-// AR_ERR_WAIT_TIMEOUT (a slot) and raises the abort word of every CTA of the
-// cluster, on which the other waits give up; all threads still reach the
-// final cluster barrier.
+// Every wait is bounded by spin_ns and a poll count.  A wait that runs out
+// records AR_ERR_FLAG_TIMEOUT (a batch that never came) or
+// AR_ERR_WAIT_TIMEOUT (a slot never freed) and raises the abort word of
+// every CTA of the cluster, on which the other waits give up.  Before any CTA
+// exits, a cluster barrier stops all sending; after an abort each CTA then
+// waits (bounded) for the bytes of any batch already announced into its
+// inbox, since an asynchronous store may still be landing; a second cluster
+// barrier ends the kernel.
 #include "lines.cuh"
 
 namespace argb {
@@ -50,9 +50,11 @@ using namespace lines;
 constexpr int kCWarps = kThreads / 32;
 constexpr int kSlots = 3;                                                 // inbox slots per warp
 constexpr unsigned kCFull = 0xffffffffu;
-constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kBatchLines * 128;
-// inbox, then consumed[kCWarps] and the abort word, rounded to 16 bytes
-constexpr size_t kClusterSmem = kInboxBytes + ((kCWarps + 1) * sizeof(uint64_t) + 15) / 16 * 16;
+constexpr size_t kSlotBytes = (size_t)kBatchLines * 128;
+constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kSlotBytes;
+// inbox, then full[kCWarps][kSlots] and empty[kCWarps][kSlots] mbarriers and the abort word
+constexpr size_t kBarOffset = kInboxBytes;
+constexpr size_t kClusterSmem = kInboxBytes + (2 * kCWarps * kSlots + 2) * sizeof(uint64_t);
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -66,13 +68,6 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t cta)
 __device__ __forceinline__ void cluster_barrier()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_acq_local(uint32_t a)
-{
-    uint64_t v;
-    asm volatile("ld.acquire.cluster.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ uint64_t ld_rlx_local(uint32_t a)
@@ -90,28 +85,59 @@ __device__ __forceinline__ uint4 ld16_local(uint32_t a)
     return v;
 }
 
-__device__ __forceinline__ void st16_peer(uint32_t a, const uint4& v)
-{
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st8_peer(uint32_t a, uint32_t x, uint32_t y)
-{
-    asm volatile("st.shared::cluster.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(x), "r"(y) : "memory");
-}
-
 __device__ __forceinline__ void st_rlx_peer(uint32_t a, uint64_t v)
 {
     asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// One try of waiting for phase `parity` of a barrier of this CTA, acquiring
+// at cluster scope what the phase's arrivals (and counted bytes) published.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Arrive on a barrier of another CTA of the cluster (relaxed: the caller has
+// already consumed what the arrival releases).
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on a barrier of another CTA, announcing `bytes` of asynchronous
+// stores that will complete on it.
+__device__ __forceinline__ void mbar_arrive_expect_tx_peer(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 16 bytes into another CTA's shared memory, counted on its barrier `bar`.
+__device__ __forceinline__ void st16_async_peer(uint32_t a, const uint4& v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(a),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+                 : "memory");
+}
 
 struct ClusterSmem {
-    uint32_t inbox;      // shared address of this CTA's inbox
-    uint32_t consumed;   // shared address of consumed[0]
-    uint32_t abort;      // shared address of the abort word
+    uint32_t inbox;   // shared address of this CTA's inbox
+    uint32_t full;    // full[0][0]
+    uint32_t empty;   // empty[0][0]
+    uint32_t abort;   // the abort word
 };
 
 // Raise the abort word of every CTA of the cluster.
@@ -120,6 +146,23 @@ __device__ void raise_abort(const ClusterSmem& S)
 {
 #pragma unroll
     for (int q = 0; q < NR; ++q) st_rlx_peer(peer_addr(S.abort, (uint32_t)q), 1ull);
+}
+
+// Bounded wait of a whole warp on phase `parity` of a local barrier.  Returns
+// false if spin_ns passed or the abort word was raised first.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t abort, int64_t spin_ns)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(kCFull, ok)) return true;
+    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
+    for (uint64_t it = 0; it < cap; ++it) {
+        if (!ok) ok = mbar_try_wait(bar, parity);
+        if (__all_sync(kCFull, ok)) return true;
+        if ((it & 15) == 15 &&
+            __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns || ld_rlx_local(abort) != 0))
+            return false;
+    }
+    return false;
 }
 
 template <int NR, int DT>
@@ -140,21 +183,27 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     const int d = (r + 1) % NR, p = (r + NR - 1) % NR;   // next and previous rank
     ClusterSmem S;
     S.inbox = smem_addr(smem);
-    S.consumed = S.inbox + (uint32_t)kInboxBytes;
-    S.abort = S.consumed + kCWarps * 8;
+    S.full = S.inbox + (uint32_t)kBarOffset;
+    S.empty = S.full + (uint32_t)(kCWarps * kSlots * 8);
+    S.abort = S.empty + (uint32_t)(kCWarps * kSlots * 8);
 
-    // zero the inbox flags, consumed counts and abort word, then let every
-    // CTA of the cluster see that before any peer writes
-    for (uint32_t o = threadIdx.x * 16; o < (uint32_t)kClusterSmem; o += kThreads * 16)
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(S.inbox + o), "r"(0u) : "memory");
+    // barriers and the abort word, initialised before any peer can use them
+    if (threadIdx.x < kCWarps * kSlots) {
+        mbar_init(S.full + 8 * threadIdx.x, 1);
+        mbar_init(S.empty + 8 * threadIdx.x, 1);
+    }
+    if (threadIdx.x == 0) asm volatile("st.shared.u64 [%0], %1;" ::"r"(S.abort), "l"(0ull) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     cluster_barrier();
 
     const size_t slice_lo = k * epc;
     const size_t line_lo = slice_lo / kLineWords;
-    const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kBatchLines * 128);
-    const uint32_t peer_box = peer_addr(my_box, (uint32_t)d);                    // the next rank's inbox for this warp
-    const uint32_t my_consumed = S.consumed + 8 * warp;                            // written by the next rank
-    const uint32_t prev_consumed = peer_addr(S.consumed + 8 * warp, (uint32_t)p);  // the previous rank's copy
+    const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kSlotBytes);
+    const uint32_t peer_box = peer_addr(my_box, (uint32_t)d);             // the next rank's inbox for this warp
+    const uint32_t my_full = S.full + (uint32_t)(warp * kSlots * 8);      // + 8 s: slot s of my inbox
+    const uint32_t peer_full = peer_addr(my_full, (uint32_t)d);           // the next rank's, for my sends
+    const uint32_t my_empty = S.empty + (uint32_t)(warp * kSlots * 8);    // my sends' slots at the next rank
+    const uint32_t prev_empty = peer_addr(my_empty, (uint32_t)p);         // the previous rank's, for my inbox
     uint64_t q_recv = 0, q_send = 0;
     bool dead = (r == absent);   // a rank that never joins (failure emulation)
 
@@ -176,6 +225,11 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         G.x = static_cast<const T*>(in.p[r]) + lo;
         G.y = static_cast<T*>(out.p[r]) + lo;
         return G;
+    };
+    // lines of batch b (from line_lo + 32 b) below the slice's end
+    auto live_lines = [&](size_t base, const Geom& G) -> uint32_t {
+        const size_t end = (G.slice_hi + kLineWords - 1) / kLineWords;
+        return base >= end ? 0u : (uint32_t)(end - base < (size_t)kBatchLines ? end - base : kBatchLines);
     };
     constexpr int kLast = 2 * NR - 2;   // t = 2n-2: only the last receive
     auto next_pair = [&](int& t, size_t& b, Geom& G) {   // the warp's next (step, batch), or t > kLast
@@ -209,39 +263,35 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     while (!dead && t <= kLast) {
         const bool sends = t <= kLast - 1;
         const size_t base = line_lo + b * kBatchLines;
+        const uint32_t nlive = live_lines(base, G);
         uint4 w[kI];
 #pragma unroll
         for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (t >= 1) {   // receive: wait for the 32 flags of this batch's slot
-            const uint32_t slot = my_box + (uint32_t)((q_recv % kSlots) * kBatchLines * 128);
-            const bool live = (base + lane) * kLineWords < G.slice_hi;
-            const uint32_t flag = slot + lane * 128 + 120;
-            bool ok = !live || ld_acq_local(flag) == q_recv + 1;
-            if (!__all_sync(kCFull, ok)) {
-                const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
-                bool stop = false;
-                for (uint64_t it = 0; it < cap && !stop; ++it) {
-                    if (it >= 1024) __nanosleep(32);
-                    if (!ok) ok = ld_acq_local(flag) == q_recv + 1;
-                    if (__all_sync(kCFull, ok)) break;
-                    if ((it & 31) == 31)
-                        stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
-                                                      ld_rlx_local(S.abort) != 0);
+        if (t >= 1) {   // receive: batch q_recv in slot q_recv % kSlots
+            const uint32_t s = (uint32_t)(q_recv % kSlots);
+            const uint32_t slot = my_box + s * (uint32_t)kSlotBytes;
+            if (!warp_wait(my_full + 8 * s, (uint32_t)((q_recv / kSlots) & 1), S.abort, spin_ns)) {
+                if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                    report_flag_timeout(st, r, base);
+                    raise_abort<NR>(S);
                 }
-                if (!__all_sync(kCFull, ok)) {
-                    if (ld_rlx_local(S.abort) == 0) {
-                        if (!ok) report_flag_timeout(st, r, base + lane);
-                        if (lane == 0) raise_abort<NR>(S);
-                    }
-                    dead = true;
-                    break;
-                }
+                dead = true;
+                break;
             }
-            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < kI; ++i) {
-                const size_t l = base + 4 * i + g;
-                if (l * kLineWords < G.slice_hi) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
+            for (int i = 0; i < kI; ++i)
+                if ((uint32_t)(4 * i + g) < nlive) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
+            // every line carries its flag: the batch number + 1
+            bool flags_ok = true;
+#pragma unroll
+            for (int i = 0; i < kI; ++i)
+                if (j == 7 && (uint32_t)(4 * i + g) < nlive)
+                    flags_ok = flags_ok && (((uint64_t)w[i].w << 32) | w[i].z) == q_recv + 1;
+            if (!__all_sync(kCFull, flags_ok)) {
+                if (!flags_ok) report_flag_timeout(st, r, base);
+                if (lane == 0) raise_abort<NR>(S);
+                dead = true;
+                break;
             }
         }
         float v[kI][4];
@@ -262,6 +312,12 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                 for (int u = 0; u < 4; ++u) v[i][u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[i][u]));
             }
         }
+        if (t >= 1) {
+            // the slot's lines are in registers and used: free it for the previous rank
+            __syncwarp();
+            if (lane == 0) mbar_arrive_peer(prev_empty + 8 * (uint32_t)(q_recv % kSlots));
+            ++q_recv;
+        }
         // the next pair's own elements now: their loads fly during the send
         int t2 = t;
         size_t b2 = b;
@@ -269,53 +325,33 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         next_pair(t2, b2, G2);
         if (t2 <= kLast) load_x(t2, b2, G2);
         if (sends) {
-            // the next rank must have consumed the batch that last used this slot
-            if (q_send >= kSlots) {
-                const uint64_t want = q_send - kSlots + 1;
-                bool ok = ld_acq_local(my_consumed) >= want;
-                if (!__all_sync(kCFull, ok)) {
-                    const uint64_t t0 = globaltimer_ns(), cap = (uint64_t)spin_ns / 16u + 4096u;
-                    bool stop = false;
-                    for (uint64_t it = 0; it < cap && !stop; ++it) {
-                        if (it >= 1024) __nanosleep(32);
-                        ok = ld_acq_local(my_consumed) >= want;
-                        if (__all_sync(kCFull, ok)) break;
-                        if ((it & 31) == 31)
-                            stop = __any_sync(kCFull, (int64_t)(globaltimer_ns() - t0) > spin_ns ||
-                                                          ld_rlx_local(S.abort) != 0);
-                    }
-                    if (!__all_sync(kCFull, ok)) {
-                        if (lane == 0 && ld_rlx_local(S.abort) == 0) {
-                            report_wait_timeout(st);
-                            raise_abort<NR>(S);
-                        }
-                        dead = true;
-                        break;
-                    }
+            const uint32_t s = (uint32_t)(q_send % kSlots);
+            // the next rank must have read the batch that last used this slot
+            if (q_send >= kSlots &&
+                !warp_wait(my_empty + 8 * s, (uint32_t)((q_send / kSlots - 1) & 1), S.abort, spin_ns)) {
+                if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                    report_wait_timeout(st);
+                    raise_abort<NR>(S);
                 }
+                dead = true;
+                break;
             }
-            const uint32_t slot = peer_box + (uint32_t)((q_send % kSlots) * kBatchLines * 128);
+            const uint32_t slot = peer_box + s * (uint32_t)kSlotBytes;
+            const uint32_t bar = peer_full + 8 * s;
+            if (lane == 0) mbar_arrive_expect_tx_peer(bar, nlive * 128u);
+            const uint64_t flag = q_send + 1;
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
-                const size_t l = base + 4 * i + g;
-                if (l * kLineWords >= G.slice_hi) continue;
+                if ((uint32_t)(4 * i + g) >= nlive) continue;
                 const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
-                if (j < 7)
-                    st16_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
-                                            __float_as_uint(v[i][2]), __float_as_uint(v[i][3])));
-                else
-                    st8_peer(a, __float_as_uint(v[i][0]), __float_as_uint(v[i][1]));
+                const uint4 val = j < 7 ? make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                                     __float_as_uint(v[i][2]), __float_as_uint(v[i][3]))
+                                        : make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                                     (uint32_t)flag, (uint32_t)(flag >> 32));
+                st16_async_peer(a, val, bar);
             }
-            __syncwarp();
-            fence_cluster();   // releases these lines; also orders this batch's inbox reads
-            if ((base + lane) * kLineWords < G.slice_hi) st_rlx_peer(slot + lane * 128 + 120, q_send + 1);
             ++q_send;
-            // this batch's inbox slot is free again (its reads precede the
-            // fence): tell the previous rank.  Published after this rank's
-            // own send, so a step's batches must fit in kSlots - 1 slots.
-            if (t >= 1 && lane == 0) st_rlx_peer(prev_consumed, q_recv + 1);
         }
-        if (t >= 1) ++q_recv;
         // this rank's output last, after the hop is on its way
         if (t >= NR - 1) {
 #pragma unroll
@@ -330,7 +366,24 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         b = b2;
         G = G2;
     }
-    // no CTA leaves while a peer may still write into its shared memory
+    // nothing is sent after this barrier
+    cluster_barrier();
+    if (ld_rlx_local(S.abort) != 0) {
+        // after an abort an announced batch may still be landing in this
+        // CTA's inbox: wait (bounded) for the next phase of every slot the
+        // previous rank may have filled since this warp last read it
+        const int64_t drain_ns = spin_ns < 100000 ? spin_ns : 100000;
+        for (uint32_t s = 0; s < (uint32_t)kSlots; ++s) {
+            const uint64_t used = q_recv > s ? (q_recv - s + kSlots - 1) / kSlots : 0;   // reads of slot s
+            const uint32_t bar = my_full + 8 * s;
+            const uint64_t t0 = globaltimer_ns();
+            for (uint64_t it = 0; it < 65536; ++it) {
+                if (mbar_try_wait(bar, (uint32_t)(used & 1))) break;
+                if ((int64_t)(globaltimer_ns() - t0) > drain_ns) break;
+            }
+        }
+    }
+    // no CTA leaves while a peer may still touch its shared memory
     cluster_barrier();
 }
 
@@ -382,18 +435,16 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
             if (resident < 1) return AR_ERR_CUDA;
             const size_t C = chunk_elems(NR, count, DT);
             // slices of at least one batch per warp; one wave of clusters
-            // unless that would give a warp more than kSlots - 1 batches per
-            // step: at step 0 every rank sends without receiving, and a
-            // receiver frees a slot only after its own send of the next
-            // batch, so a step's batches must fit in kSlots - 1 slots
-            // (otherwise every rank waits on its successor: a cycle)
+            // unless that would give a warp more than kSlots batches per step
+            // (at step 0 every rank sends without receiving, so a step's
+            // batches must fit the receiver's slots)
             const size_t per_cta_min = kBatchElems * kCWarps;
             size_t K = (C + per_cta_min - 1) / per_cta_min;
             if (K > (size_t)resident) K = (size_t)resident;
             if (K < 1) K = 1;
             size_t epc = (C + K - 1) / K;
             epc = (epc + kBatchElems - 1) / kBatchElems * kBatchElems;
-            if (epc > kBatchElems * kCWarps * (kSlots - 1)) epc = kBatchElems * kCWarps * (kSlots - 1);
+            if (epc > kBatchElems * kCWarps * kSlots) epc = kBatchElems * kCWarps * kSlots;
             K = (C + epc - 1) / epc;
             if (K < 1) K = 1;
             cfg.gridDim = dim3((unsigned)(K * NR));

@@ -142,7 +142,7 @@ KERNEL_SOURCES = {
     "allreduce_rmsnorm": ["rmsnorm.cu"], "push": ["one_shot_modes.cu"], "push_reduce": ["one_shot_modes.cu"],
     "copyin": ["one_shot_modes.cu"], "ring_rs_step_rounded": ["ring.cu"], "tree_level": ["tree.cu"],
     "ring_persistent": ["ring_persistent.cu"], "ring_cluster": ["ring_cluster.cu"], "tree_fused": ["tree.cu"],
-    "ring_fused": ["ring_fused.cu"], "ring_rounded_fused": ["ring_fused.cu"],
+    "ring_fused": ["ring_fused.cu"], "ring_rounded_fused": ["ring_fused.cu"], "two_shot": ["two_shot.cu"],
 }
 
 
@@ -278,7 +278,32 @@ class Workload:
         self.p_lld, self.p_l128d = P(self.ll_dst), P(self.l128_dst)
         self.L = ar.lib()
         self.step_id = 0
-        self.launches_per_step = 1 + 2 + 2 * (n - 1) + 2 * 3
+        self.launches_per_step = None   # counted by count_launches()
+
+    def calls(self, k: int):
+        """The step's C-ABI calls, in order, for step id k."""
+        L, h, s, N, c = self.L, self.h, self.s, self.N, self.ll_count
+        return (lambda: L.ar_one_shot(h, self.p_in, self.p_out, N, 1, s),
+                lambda: L.ar_two_shot(h, self.p_in, self.p_out, N, 1, s),
+                lambda: L.ar_ring(h, self.p_in, self.p_out, N, 1, s),
+                lambda: L.ar_ll_pack_n(h, self.p_pay, self.p_ll, c, k, s),
+                lambda: L.ar_ll_reduce(h, self.p_ll, self.p_llr, c, k, s),
+                lambda: L.ar_ll_unpack_n(h, self.p_llr, self.p_lld, c, k, s),
+                lambda: L.ar_ll128_pack_n(h, self.p_pay, self.p_l128, c, k, s),
+                lambda: L.ar_ll128_reduce(h, self.p_l128, self.p_l128r, c, k, s),
+                lambda: L.ar_ll128_unpack_n(h, self.p_l128r, self.p_l128d, c, k, s))
+
+    def count_launches(self) -> int:
+        """Run one (untimed) step and add up the kernels each call reports
+        (ar_traffic), so the count follows the forms the options select."""
+        import all_reduce_reduction_rank_gb300 as ar
+        self.step_id += 1
+        total = 0
+        for call in self.calls(self.step_id):
+            ar.check(call(), "step call")
+            total += ar.ar_traffic(self.h).launches
+        self.launches_per_step = total
+        return total
 
     def run(self):
         L, h, s, n, N, c = self.L, self.h, self.s, self.n, self.N, self.ll_count
@@ -626,6 +651,8 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
              ("one_shot_push", L.ar_one_shot_push, ar.AR_OP_ONE_SHOT_PUSH),
              ("one_shot_copyin", L.ar_one_shot_copyin, ar.AR_OP_ONE_SHOT_COPYIN),
              ("two_shot", L.ar_two_shot, ar.AR_OP_TWO_SHOT),
+             ("two_shot_two_launches", L.ar_two_shot, ar.AR_OP_TWO_SHOT),
+             ("two_shot_tile_flags", L.ar_two_shot, ar.AR_OP_TWO_SHOT),
              ("ring", L.ar_ring, ar.AR_OP_RING),
              ("ring_rounded", L.ar_ring_rounded, ar.AR_OP_RING_ROUNDED),
              ("ring_persistent", L.ar_ring_persistent, ar.AR_OP_RING_PERSISTENT),
@@ -650,6 +677,9 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
         for name, call, op in algos:
             if name == "ring_noalloc" and S > NOALLOC_MAX_BYTES:
                 continue
+            # two-shot as its default form, and forced to its other two forms
+            ar.check(ar.ar_set_option(h, ar.AR_OPT_TWO_SHOT_IMPL,
+                                      {"two_shot_two_launches": 1, "two_shot_tile_flags": 3}.get(name, 0)))
             t = ar.ar_plan(op, n, N, "bf16")
             b = t.hbm_read_bytes + t.hbm_write_bytes
             for k in range(min(slots, 4)):
@@ -669,12 +699,14 @@ def variants(wl, peak: float, batches: int = 5, min_calls: int = 32) -> dict:
             algbw = S / (ms * 1e-3) / 1e9
             row = {"bytes_per_rank": S, "us": round(ms * 1e3, 3), "hbm_GB/s": round(gbs, 1),
                    "frac_of_peak": round(gbs / peak, 4), "algbw_GB/s": round(algbw, 1),
-                   "launches": t.launches, "calls_per_batch": calls}
+                   "launches": t.launches if name == "ring_noalloc" else ar.ar_traffic(h).launches,
+                   "calls_per_batch": calls}
             if S <= GRAPH_MAX_BYTES:
                 row["graph_us"] = round(_graph_us(wl.stream, lambda i: call(h, pin[i % slots], pout[i % slots],
                                                                             N, 1, wl.s)), 3)
                 ar.check(ar.ar_status(h), name)
             res[name].append(mark_l2(row, peak))
+    ar.check(ar.ar_set_option(h, ar.AR_OPT_TWO_SHOT_IMPL, 0))
     for opt in (ar.AR_OPT_PUSH_STAGING, ar.AR_OPT_REGISTERED, ar.AR_OPT_PERSISTENT):
         ar.check(ar.ar_set_option(h, opt, 0), "variant buffers")
     return res
@@ -804,6 +836,8 @@ def run_ours(args):
     wl = Workload(n, S, ll_count, dev, seed=1003)
     ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_ONE_SHOT_IMPL, args.one_shot_impl))
     ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_CTAS_PER_SM, args.ctas_per_sm))
+    ar.check(ar.ar_set_option(wl.h, ar.AR_OPT_TWO_SHOT_IMPL, args.two_shot_impl))
+    wl.count_launches()
     peak, peak_src = measured_peak()
     rows = step_bytes(n, wl.N, 2, ll_count)
     bytes_step = sum(rows.values())
@@ -1167,6 +1201,9 @@ def main(argv=None):
                    help="record per-launch events on every k-th timed step")
     p.add_argument("--one-shot-impl", type=int, default=0, help="AR_OPT_ONE_SHOT_IMPL (0 auto, 1, 2)")
     p.add_argument("--ctas-per-sm", type=int, default=0, help="AR_OPT_CTAS_PER_SM (0 auto)")
+    p.add_argument("--two-shot-impl", type=int, default=0,
+                   help="AR_OPT_TWO_SHOT_IMPL (0 auto, 1 two launches, 2 one launch with a per-tile CTA "
+                        "barrier, 3 one launch with per-tile flags between CTAs)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--details", default=os.path.join("gpurun_out", "bench_details.json"),

@@ -108,7 +108,7 @@ typedef enum {
  *     LL/LL128 calls (whose reduce counts as 1 step).
  *   hbm_read_bytes / hbm_write_bytes: the bytes the call must move in this
  *     GPU's HBM (algorithmic, not measured).
- *   launches: kernels the call launched. */
+ *   launches: kernels the call launched (ar_plan: with the default options). */
 typedef struct {
     int op;                  /* ar_op */
     int n_ranks;             /* 1 for the per-buffer LL/LL128 pack/unpack */
@@ -159,6 +159,10 @@ enum {
                                 rank r (0..n-1) never joins, so its neighbours' waits run out after
                                 AR_OPT_SPIN_NS and the status reads AR_ERR_FLAG_TIMEOUT or
                                 AR_ERR_WAIT_TIMEOUT; -1 (default): every rank takes part */
+    AR_OPT_TWO_SHOT_IMPL = 15,/* ar_two_shot's form, same bits and bytes: 1 two launches (the
+                                kernel boundary separates the phases); 2 one launch, each CTA
+                                gathering the tile it reduced after a CTA barrier; 3 one launch,
+                                tiles handed between CTAs by ready flags; 0 (default): 2 */
     AR_OPT_PDL = 6           /* 1 (default): launch with programmatic stream
                                 serialization, so a kernel is scheduled while the one
                                 before it in the stream drains (each kernel waits for
@@ -188,7 +192,8 @@ typedef enum {
     AR_K_RING_CLUSTER = 19,         /* ar_ring_cluster (all steps) */
     AR_K_TREE_FUSED = 20,           /* ar_tree_fused (all levels) */
     AR_K_RING_FUSED = 21,           /* ar_ring_fused (all steps) */
-    AR_K_RING_ROUNDED_FUSED = 22    /* ar_ring_rounded_fused (all steps) */
+    AR_K_RING_ROUNDED_FUSED = 22,   /* ar_ring_rounded_fused (all steps) */
+    AR_K_TWO_SHOT = 23              /* ar_two_shot in one launch (both phases) */
 } ar_kernel;
 
 /* One timing record: `launches` consecutive launches of one kernel within
@@ -209,7 +214,8 @@ typedef struct {
 /* Create a handle for n_ranks in [2, 16] ranks of at most max_bytes each
  * (max_bytes >= 16), on the calling thread's current CUDA device.  It
  * allocates, once, the ring's fp32 partial-sum scratch (2 x n_ranks x chunk
- * x 4 B, about 4 x max_bytes) and a status word.  *out is set only on AR_OK.
+ * x 4 B, about 4 x max_bytes), the one-launch two-shot's tile flags (about
+ * max_bytes / 128 bytes) and a status word.  *out is set only on AR_OK.
  * The n-rank bound is the pages' kMaxNumGPU = 16 (custom all-reduce notes,
  * §调用). */
 int ar_create(int n_ranks, size_t max_bytes, ar_handle* out);
@@ -233,12 +239,20 @@ int ar_one_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
                 ar_dtype dt, ar_stream_t stream);
 
 /* Two-shot: reduce-scatter then all-gather (handbook "集合通信：NCCL 的
- * 算法、协议…", §算法, two-shot; "多 GPU 与 NCCL", §集合通信: all-reduce =
- * reduce-scatter + all-gather).  Chunk r = elements [rC, min((r+1)C, count))
- * with C = ceil(count/n) rounded up to a whole 16-byte vector.  Phase 1
- * writes chunk r's rank-order sum to out[r]; phase 2 copies chunk j of
- * out[j] to every other rank.  Bit-identical to ar_one_shot.  HBM: reads
- * (n+1) S, writes n S. */
+ * 算法、协议…", §算法, two-shot, with a synchronization between the phases;
+ * "多 GPU 与 NCCL", §集合通信: all-reduce = reduce-scatter + all-gather).
+ * Chunk r = elements [rC, min((r+1)C, count)) with C = ceil(count/n) rounded
+ * up to a whole 16-byte vector.  Phase 1 writes chunk r's rank-order sum to
+ * out[r]; phase 2 copies chunk j of out[j] to every other rank.  Three
+ * forms (AR_OPT_TWO_SHOT_IMPL): two launches, the kernel boundary separating
+ * the phases; one launch (the default), in which the CTA reducing a tile of a
+ * chunk gathers that tile itself after a CTA barrier; or one launch in which
+ * the CTA reducing a tile publishes a ready flag and another CTA gathers the
+ * tile once it sees the flag (bounded by AR_OPT_SPIN_NS; a wait that runs out
+ * leaves that tile's outputs on the other ranks untouched and ar_status
+ * reports AR_ERR_WAIT_TIMEOUT; its counters and flags live in the handle,
+ * about max_bytes / 128 bytes allocated by ar_create).  Bit-identical to
+ * ar_one_shot.  HBM: reads (n+1) S, writes n S. */
 int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t count,
                 ar_dtype dt, ar_stream_t stream);
 
