@@ -16,13 +16,13 @@
 // sees only the ranks' own elements and outputs: 2 n S per call.
 //
 // Layout: cluster size n (one CTA per rank, cluster_ctarank = rank);
-// cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of 960
-// elements = 32 lines); clusters are independent, so the grid may run in any
+// cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of one
+// batch, 30 L elements); clusters are independent, so the grid may run in any
 // number of waves and needs no cooperative launch.  Warp w of rank r handles
 // batches b = w, w+8, ... of the slice and exchanges lines only with warp w
 // of ranks r-1 and r+1.
 //
-// Shared memory of a CTA: per warp kSlots inbox slots of 32 lines; per slot a
+// Shared memory of a CTA: per warp kSlots inbox slots of L lines; per slot a
 // "full" mbarrier (the receiver's: one arrival, the sender's expect_tx, plus
 // the slot's bytes) and an "empty" mbarrier (the sender's: one arrival by the
 // receiver once it has read the slot); an abort word.  Batch q of a warp goes
@@ -48,13 +48,24 @@ namespace {
 using namespace lines;
 
 constexpr int kCWarps = kThreads / 32;
-constexpr int kSlots = 3;                                                 // inbox slots per warp
+// A warp's batch: L lines (L / 4 per lane group of 8 lanes), two forms.  A
+// hop's latency is set by the instructions one warp issues for its batch,
+// not by the transfer, so small calls use short batches (L = 8: a short
+// chain per hop, a step spread over more warps); large calls, which are
+// bound by instruction throughput, use long ones (L = 32: the per-batch work
+// amortised over 4x the data).  kSlots batches per warp fit the inbox, and
+// kMinBlocks CTAs fit on an SM.
+template <int L> struct Geo {
+    static constexpr int kLines = L;
+    static constexpr int kSlots = L == 8 ? 6 : 3;                     // inbox slots per warp
+    static constexpr int kMinBlocks = L == 8 ? 4 : 2;
+    static constexpr size_t kBatchElems = (size_t)kLineWords * L;
+    static constexpr size_t kSlotBytes = (size_t)L * 128;
+    static constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kSlotBytes;
+    // inbox, then full[kCWarps][kSlots] and empty[kCWarps][kSlots] mbarriers and the abort word
+    static constexpr size_t kSmem = kInboxBytes + (2 * kCWarps * kSlots + 2) * sizeof(uint64_t);
+};
 constexpr unsigned kCFull = 0xffffffffu;
-constexpr size_t kSlotBytes = (size_t)kBatchLines * 128;
-constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kSlotBytes;
-// inbox, then full[kCWarps][kSlots] and empty[kCWarps][kSlots] mbarriers and the abort word
-constexpr size_t kBarOffset = kInboxBytes;
-constexpr size_t kClusterSmem = kInboxBytes + (2 * kCWarps * kSlots + 2) * sizeof(uint64_t);
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -165,13 +176,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
-template <int NR, int DT>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int NR, int DT, int L>
+__global__ void __launch_bounds__(kThreads, Geo<L>::kMinBlocks)
 ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out, size_t C,
                     size_t count, size_t epc, int64_t spin_ns, int absent, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
-    constexpr int kI = kBatchLines / 4;
+    constexpr int kCLines = Geo<L>::kLines, kSlots = Geo<L>::kSlots;
+    constexpr size_t kSlotBytes = Geo<L>::kSlotBytes;
+    constexpr int kI = kCLines / 4;
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t crank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
@@ -183,7 +196,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     const int d = (r + 1) % NR, p = (r + NR - 1) % NR;   // next and previous rank
     ClusterSmem S;
     S.inbox = smem_addr(smem);
-    S.full = S.inbox + (uint32_t)kBarOffset;
+    S.full = S.inbox + (uint32_t)Geo<L>::kInboxBytes;
     S.empty = S.full + (uint32_t)(kCWarps * kSlots * 8);
     S.abort = S.empty + (uint32_t)(kCWarps * kSlots * 8);
 
@@ -221,7 +234,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         G.len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
         G.slice_hi = slice_lo + epc < G.len ? slice_lo + epc : G.len;
         const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
-        G.nbatch = (nlines + kBatchLines - 1) / kBatchLines;
+        G.nbatch = (nlines + kCLines - 1) / kCLines;
         G.x = static_cast<const T*>(in.p[r]) + lo;
         G.y = static_cast<T*>(out.p[r]) + lo;
         return G;
@@ -229,7 +242,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     // lines of batch b (from line_lo + 32 b) below the slice's end
     auto live_lines = [&](size_t base, const Geom& G) -> uint32_t {
         const size_t end = (G.slice_hi + kLineWords - 1) / kLineWords;
-        return base >= end ? 0u : (uint32_t)(end - base < (size_t)kBatchLines ? end - base : kBatchLines);
+        return base >= end ? 0u : (uint32_t)(end - base < (size_t)kCLines ? end - base : kCLines);
     };
     constexpr int kLast = 2 * NR - 2;   // t = 2n-2: only the last receive
     auto next_pair = [&](int& t, size_t& b, Geom& G) {   // the warp's next (step, batch), or t > kLast
@@ -244,7 +257,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     uint32_t xr[kI][kRawWords<DT>];
     auto load_x = [&](int t, size_t b, const Geom& G) {
         if (t > NR - 1) return;
-        const size_t base = line_lo + b * kBatchLines;
+        const size_t base = line_lo + b * kCLines;
 #pragma unroll
         for (int i = 0; i < kI; ++i) {
             const size_t l = base + 4 * i + g;
@@ -262,7 +275,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     if (!dead && t <= kLast) load_x(t, b, G);
     while (!dead && t <= kLast) {
         const bool sends = t <= kLast - 1;
-        const size_t base = line_lo + b * kBatchLines;
+        const size_t base = line_lo + b * kCLines;
         const uint32_t nlive = live_lines(base, G);
         uint4 w[kI];
 #pragma unroll
@@ -387,6 +400,40 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     cluster_barrier();
 }
 
+// The kernel's attributes, set once per device, and the clusters of it that
+// fit on the GPU at once (computed once per instantiation); 0 if the device
+// cannot run a cluster of NR such CTAs.
+template <int NR, int DT, int L>
+int cluster_setup()
+{
+    static std::atomic<uint32_t> attr_done{0};
+    const bool attr_ok = once_per_device(attr_done, [&] {
+        return cudaFuncSetAttribute(ring_cluster_kernel<NR, DT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Geo<L>::kSmem) == cudaSuccess &&
+               (NR <= 8 || cudaFuncSetAttribute(ring_cluster_kernel<NR, DT, L>,
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess);
+    });
+    if (!attr_ok) return 0;
+    static const int resident = [] {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = NR;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t q{};
+        q.gridDim = dim3((unsigned)(NR * 64));
+        q.blockDim = dim3(kThreads);
+        q.dynamicSmemBytes = Geo<L>::kSmem;
+        q.attrs = attr;
+        q.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, ring_cluster_kernel<NR, DT, L>, &q) != cudaSuccess) nc = 0;
+        cudaGetLastError();
+        return nc;
+    }();
+    return resident;
+}
+
 }  // namespace
 
 int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size_t count, int dt, cudaStream_t s,
@@ -402,63 +449,57 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
                 ip.p[q] = in[q];
                 op.p[q] = out[q];
             }
-            static std::atomic<uint32_t> attr_done{0};
-            const bool attr_ok = once_per_device(attr_done, [&] {
-                return cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kClusterSmem) == cudaSuccess &&
-                       (NR <= 8 || cudaFuncSetAttribute(ring_cluster_kernel<NR, DT>,
-                                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                                        1) == cudaSuccess);
-            });
-            if (!attr_ok) return AR_ERR_CUDA;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = NR;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cudaLaunchConfig_t cfg{};
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = kClusterSmem;
-            cfg.stream = s;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            // clusters that fit at once: one wave of them (computed once,
-            // thread-safely, per kernel instantiation)
-            static const int resident = [&] {
-                cudaLaunchConfig_t q = cfg;
-                q.gridDim = dim3((unsigned)(NR * 64));
-                int nc = 0;
-                if (cudaOccupancyMaxActiveClusters(&nc, ring_cluster_kernel<NR, DT>, &q) != cudaSuccess) nc = 0;
-                cudaGetLastError();
-                return nc;
-            }();
-            if (resident < 1) return AR_ERR_CUDA;
             const size_t C = chunk_elems(NR, count, DT);
-            // slices of at least one batch per warp; one wave of clusters
-            // unless that would give a warp more than kSlots batches per step
-            // (at step 0 every rank sends without receiving, so a step's
-            // batches must fit the receiver's slots)
-            const size_t per_cta_min = kBatchElems * kCWarps;
-            size_t K = (C + per_cta_min - 1) / per_cta_min;
-            if (K > (size_t)resident) K = (size_t)resident;
-            if (K < 1) K = 1;
-            size_t epc = (C + K - 1) / K;
-            epc = (epc + kBatchElems - 1) / kBatchElems * kBatchElems;
-            if (epc > kBatchElems * kCWarps * kSlots) epc = kBatchElems * kCWarps * kSlots;
-            K = (C + epc - 1) / epc;
-            if (K < 1) K = 1;
-            cfg.gridDim = dim3((unsigned)(K * NR));
-            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
-            rec_begin(h, s);
-            const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_cluster_kernel<NR, DT>, ip, op, C, count, epc,
-                                                       h.spin_ns, h.persist_absent, h.status);
-            rec_end(h, s, AR_K_RING_CLUSTER, 2ull * NR * S);
-            *launches = 1;
-            if (err != cudaSuccess) {
-                cudaGetLastError();
-                return AR_ERR_CUDA;
-            }
-            return launch_status();
+            auto run = [&](auto lc) -> int {
+                constexpr int L = decltype(lc)::value;
+                using G = Geo<L>;
+                const int resident = cluster_setup<NR, DT, L>();
+                if (resident < 1) return AR_ERR_CUDA;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = NR;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cudaLaunchConfig_t cfg{};
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = G::kSmem;
+                cfg.stream = s;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                // slices of at least one batch per warp; one wave of clusters
+                // unless that would give a warp more than kSlots batches per step
+                // (at step 0 every rank sends without receiving, so a step's
+                // batches must fit the receiver's slots)
+                const size_t per_cta_min = G::kBatchElems * kCWarps;
+                size_t K = (C + per_cta_min - 1) / per_cta_min;
+                if (K > (size_t)resident) K = (size_t)resident;
+                if (K < 1) K = 1;
+                size_t epc = (C + K - 1) / K;
+                epc = (epc + G::kBatchElems - 1) / G::kBatchElems * G::kBatchElems;
+                if (epc > G::kBatchElems * kCWarps * G::kSlots) epc = G::kBatchElems * kCWarps * G::kSlots;
+                K = (C + epc - 1) / epc;
+                if (K < 1) K = 1;
+                cfg.gridDim = dim3((unsigned)(K * NR));
+                const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
+                rec_begin(h, s);
+                const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_cluster_kernel<NR, DT, L>, ip, op, C, count,
+                                                           epc, h.spin_ns, h.persist_absent, h.status);
+                rec_end(h, s, AR_K_RING_CLUSTER, 2ull * NR * S);
+                *launches = 1;
+                if (err != cudaSuccess) {
+                    cudaGetLastError();
+                    return AR_ERR_CUDA;
+                }
+                return launch_status();
+            };
+            // short batches while one wave of clusters gives every warp at most two
+            // of them per step (measured on GB300, n = 8 bf16: 17.5 / 20.8 us at
+            // 64 KiB / 1 MiB per rank against 30.6 / 33.4 with long batches, and
+            // 110 against 80 us at 8 MiB, where long batches win)
+            const int res8 = cluster_setup<NR, DT, 8>();
+            if (res8 > 0 && C <= (size_t)res8 * kCWarps * Geo<8>::kBatchElems * 2)
+                return run(std::integral_constant<int, 8>{});
+            return run(std::integral_constant<int, 32>{});
         });
     });
 }

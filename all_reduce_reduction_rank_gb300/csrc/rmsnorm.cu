@@ -11,13 +11,15 @@
 //   y = RN(r * 1/sqrt(mean(r^2) + eps) * weight)  -> norm_out[0..n-1]
 //
 // Layout: one thread-block cluster of CL CTAs per token row (8; 16, a
-// non-portable cluster size, when the rows are too few to give every SM a
-// CTA with 8); CTA c of the cluster owns a contiguous slice of the row.  Pass 1 reads the n rank
-// slices once, writes r, keeps r (fp32) in shared memory and accumulates its
-// squares; each CTA pushes its partial sum into every CTA's shared memory
-// (distributed shared memory), one cluster barrier, and every CTA adds the
-// partials in the same fixed order; pass 2 scales r and writes every rank's
-// output.
+// non-portable cluster size, while the CTAs of 16-CTA clusters fit in one
+// wave); CTA c of the cluster owns a contiguous slice of the row.  Pass
+// 1 reads the n rank slices once, writes r, keeps r (fp32) in shared memory
+// and accumulates its squares; each CTA sends its partial sum into every
+// CTA's shared memory (distributed shared memory) with an asynchronous store
+// counted on the receiver's mbarrier, so each CTA waits only until the CL
+// partials have landed in its own shared memory (no second cluster barrier),
+// and adds them in the same fixed order; pass 2 scales r and writes every
+// rank's output.
 // HBM: reads n S + S (+ the weight, H per launch), writes n S + S.
 #include "common.cuh"
 
@@ -34,21 +36,22 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// Hardware barrier across the CTAs of a cluster (all of them are resident
-// together by construction), with release / acquire memory ordering.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Write v to CTA `cta`'s shared memory, at the offset of `local` in ours.
-__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t cta, float v)
+__device__ __forceinline__ uint32_t to_cluster(const void* local, uint32_t cta)
 {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                  : "=r"(remote)
                  : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(cta));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+    return remote;
+}
+
+// Write v to CTA `cta`'s shared memory, at the offset of `local` in ours, and
+// count its 4 bytes on that CTA's barrier at the offset of `bar` in ours.
+__device__ __forceinline__ void st_async_cluster_f32(float* local, const uint64_t* bar, uint32_t cta, float v)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(to_cluster(local, cta)),
+                 "r"(__float_as_uint(v)), "r"(to_cluster(bar, cta))
+                 : "memory");
 }
 
 // Compiled for at least four CTAs per SM: 72 registers at n = 8 where the
@@ -58,16 +61,25 @@ template <int NR, int DT, int CL>
 __global__ void __launch_bounds__(kNormThreads, 4)
 allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __restrict__ residual,
                          const void* __restrict__ weight, float eps, const __grid_constant__ MPtrs<NR> out,
-                         void* residual_out, size_t hidden, size_t slice_vecs)
+                         void* residual_out, size_t hidden, size_t slice_vecs, DevStatus* st)
 {
     constexpr int VE = kVecElems<DT>;
     extern __shared__ float r_slice[];                 // slice_vecs * VE floats
     __shared__ float warp_part[kNormThreads / 32];
-    __shared__ float parts[CL];   // every CTA's sum of squares, pushed by that CTA
+    __shared__ float parts[CL];   // every CTA's sum of squares, sent by that CTA
+    __shared__ __align__(8) uint64_t parts_bar;   // completes when the CL partials have landed
     __shared__ float row_inv;
-    // the first half of a cluster barrier: the wait before the partial sums
-    // are pushed makes sure every CTA of the cluster has started
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (threadIdx.x == 0) {
+        // one arrival (this one, expecting the CL partials' bytes), then the bytes
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&parts_bar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(4u * CL) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the first half of a cluster barrier: its wait, before the partial sums
+    // are sent, makes sure every CTA of the cluster has started and has set up
+    // its barrier
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     pdl_acquire();
     const uint32_t c = cluster_ctarank();
     const size_t t = blockIdx.x / CL;                  // token row of this cluster
@@ -113,18 +125,30 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     for (int o = 16; o > 0; o >>= 1) ss = ss + __shfl_down_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = ss;
     __syncthreads();
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (threadIdx.x == 0) {   // this CTA's partial, pushed into every CTA of the cluster
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (threadIdx.x == 0) {   // this CTA's partial, sent into every CTA of the cluster
         float s = 0.0f;
         for (int w = 0; w < kNormThreads / 32; ++w) s = s + warp_part[w];
-        for (uint32_t k = 0; k < CL; ++k) st_cluster_f32(&parts[c], k, s);
-    }
-    // one barrier: every push has landed, and none is left to land after it
-    cluster_sync();
-    if (threadIdx.x == 0) {   // the row's: the cluster's CTAs in order
-        float s = 0.0f;
-        for (uint32_t k = 0; k < CL; ++k) s = s + parts[k];
-        row_inv = 1.0f / sqrtf(s / (float)hidden + eps);
+        for (uint32_t k = 0; k < CL; ++k) st_async_cluster_f32(&parts[c], &parts_bar, k, s);
+        // wait (bounded) until all CL partials have landed here; a CTA leaves only
+        // after that, so nothing is still landing in its shared memory when it exits
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&parts_bar);
+        uint32_t done = 0;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 0; it < (1u << 22) && !done; ++it) {
+            asm volatile("{\n\t.reg .pred p;\n\t"
+                         "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(done)
+                         : "r"(bar)
+                         : "memory");
+            if (!done && (it & 255) == 255 && globaltimer_ns() - t0 > 100000000ull) break;   // 0.1 s
+        }
+        if (!done) report_wait_timeout(st);
+        // the row's: the cluster's CTAs in order
+        float t2 = 0.0f;
+        for (uint32_t k = 0; k < CL; ++k) t2 = t2 + parts[k];
+        row_inv = 1.0f / sqrtf(t2 / (float)hidden + eps);
     }
     __syncthreads();
     pdl_release();
@@ -209,12 +233,15 @@ int launch_allreduce_rmsnorm(Handle& h, const void* const* in, const void* resid
                 cfg.numAttrs = 2;
                 rec_begin(h, s);
                 const cudaError_t e = cudaLaunchKernelEx(&cfg, allreduce_rmsnorm_kernel<NR, DT, CL>, ip, residual,
-                                                         weight, eps, op, residual_out, hidden, slice);
+                                                         weight, eps, op, residual_out, hidden, slice, h.status);
                 rec_end(h, s, AR_K_ALLREDUCE_RMSNORM, 2ull * (NR + 1) * S + W);
                 return e == cudaSuccess ? launch_status() : AR_ERR_CUDA;
             };
-            // few rows: clusters of 16 spread each row over twice the SMs
-            if (tokens * 16 <= (size_t)h.sm_count) return run(std::integral_constant<int, 16>{});
+            // up to one wave of CTAs (four per SM), clusters of 16 spread each row over
+            // twice the SMs: measured on GB300 (n = 8 bf16, graph replay), 3.92 against
+            // 4.13 us at 32 x 8192; at 64 rows, where 16 would need more than a wave,
+            // clusters of 8 (5.3 us) beat 16, 4 and 2 (7.2, 6.7, 6.3 us)
+            if (tokens * 16 <= 4 * (size_t)h.sm_count) return run(std::integral_constant<int, 16>{});
             return run(std::integral_constant<int, kClusterCtas>{});
         });
     });

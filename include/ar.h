@@ -396,7 +396,8 @@ int ar_ring_noalloc(int n_ranks, const void* const* in, void* const* out, size_t
  * row-major payloads; residual, residual_out: [tokens][hidden] (one copy:
  * in tensor parallelism every rank holds the same residual; residual_out may
  * equal residual); weight: [hidden].  hidden must be a whole number of
- * 16-byte vectors and at most 327680 fp32 / 655360 bf16 or fp16 elements;
+ * 16-byte vectors and at most 327680 elements of any payload type (r is
+ * kept in fp32 in shared memory, at most 160 KiB per CTA of a cluster of 8);
  * eps >= 0.  In place (norm_out[r] == in[r]) is allowed; otherwise no output
  * may overlap an input or another output.  Each token row is handled by a
  * thread-block cluster of 8 CTAs, whose partial sums of squares are combined

@@ -105,3 +105,19 @@ def test_fused_epilogue_argument_errors():
         assert call(res=res.ptr + 8) == ar.AR_ERR_ALIGN
         assert call(T=0) == ar.AR_OK
         assert ar.ar_traffic(h).launches == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fused_epilogue_largest_hidden(dtype):
+    # the largest row the kernel keeps in shared memory (327680 elements: 160 KiB of fp32 per
+    # CTA of a cluster of 8), and the next whole vector past it refused
+    H = 327680
+    got_y, got_r, want_y, want_r, _ = _run(2, 1, H, dtype, seed=77)
+    np.testing.assert_array_equal(bits(got_r), bits(want_r))
+    assert _within_one_ulp(got_y[0], want_y, dtype).all()
+    H2 = H + 16 // E[dtype]
+    with Handle(2, H2 * E[dtype]) as h:
+        ins, outs = empty_ranks(2, H2 * E[dtype]), empty_ranks(2, H2 * E[dtype])
+        res, w, ro = Buf(H2 * E[dtype]), Buf(H2 * E[dtype]), Buf(H2 * E[dtype])
+        assert ar.ar_allreduce_rmsnorm(h, ptrs(ins), res.ptr, w.ptr, 1e-6, ptrs(outs), ro.ptr, 1, H2,
+                                       dtype) == ar.AR_ERR_INVALID
