@@ -1,23 +1,25 @@
 // Persistent ring all-reduce over a thread-block cluster: the ranks are the
 // CTAs of one cluster and a hop goes through distributed shared memory.
 //
-// The same steps, lines and sums as ring_persistent.cu (handbook "集合通信：
-// NCCL 的算法、协议与推理框架的定制 all-reduce", §协议: LL128 lines of 120
-// bytes of data and an 8-byte flag; "多 GPU 与 NCCL", §ring all-reduce: the
-// steps and chunk rotation; fp32 partials, chunk c summed from rank c,
-// rounded once), so the result equals ar_ring's bit for bit.  What differs is
-// how a hop travels: the sending CTA writes the lines straight into the
-// receiving CTA's shared memory with asynchronous stores (st.async), each of
-// which counts its bytes on the receiving slot's mbarrier (complete_tx).
-// The receiver waits on that one barrier instead of polling 32 flags, and the
-// sender neither waits for its stores nor fences them: the barrier's
-// transaction count is what makes a batch visible.  The lines still carry
-// their LL128 flag (the batch number + 1), which the receiver checks.  HBM
-// sees only the ranks' own elements and outputs: 2 n S per call.
+// The same steps and sums as ar_ring (handbook "多 GPU 与 NCCL", §ring
+// all-reduce: n-1 reduce-scatter steps then n-1 all-gather steps, chunk c
+// summed from rank c; fp32 partials, rounded once), so the result equals
+// ar_ring's bit for bit, in one launch.  A hop is a batch of 128-byte lines
+// of fp32 words that the sending CTA writes straight into the receiving
+// CTA's shared memory with asynchronous stores (st.async), each of which
+// counts its bytes on the receiving slot's mbarrier (complete_tx).  The
+// receiver waits on that one barrier; the sender neither waits for its
+// stores nor fences them.  This is the handbook's Simple protocol shape
+// ("集合通信：NCCL 的算法、协议与推理框架的定制 all-reduce", §协议: data, plus
+// a separate completion signal) rather than LL128's flag in every line:
+// inside a cluster the barrier's byte count gives what the per-line flag
+// gives over NVLink -- the data and its arrival in one operation -- without
+// spending 8 bytes of every line on it.  HBM sees only the ranks' own
+// elements and outputs: 2 n S per call.
 //
 // Layout: cluster size n (one CTA per rank, cluster_ctarank = rank);
 // cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of one
-// batch, 30 L elements); clusters are independent, so the grid may run in any
+// batch, 32 L elements); clusters are independent, so the grid may run in any
 // number of waves and needs no cooperative launch.  Warp w of rank r handles
 // batches b = w, w+8, ... of the slice and exchanges lines only with warp w
 // of ranks r-1 and r+1.
@@ -48,6 +50,44 @@ namespace {
 using namespace lines;
 
 constexpr int kCWarps = kThreads / 32;
+constexpr int kCWords = 32;   // fp32 words per 128-byte line: 4 per lane, 8 lanes per line
+
+// Four consecutive elements from e as raw words (zero past len).
+template <int DT>
+__device__ __forceinline__ void load4(const void* chunk, size_t e, size_t len, uint32_t* w)
+{
+    if (e + 4 <= len) {
+        if constexpr (DT == AR_F32) {
+            const uint4 v = ld16(static_cast<const float*>(chunk) + e);
+            w[0] = v.x;
+            w[1] = v.y;
+            w[2] = v.z;
+            w[3] = v.w;
+        } else {
+            const uint2 v = ld8_plain(static_cast<const uint16_t*>(chunk) + e);
+            w[0] = v.x;
+            w[1] = v.y;
+        }
+    } else {
+        load_raw<DT>(chunk, e, 4, len, w);
+    }
+}
+
+// Rounds f[0..4) to the payload type and stores the elements below len.
+template <int DT>
+__device__ __forceinline__ void store4(void* chunk, size_t e, size_t len, const float* f)
+{
+    if (e + 4 <= len) {
+        if constexpr (DT == AR_F32) {
+            st16(static_cast<float*>(chunk) + e, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                                            __float_as_uint(f[2]), __float_as_uint(f[3])));
+        } else {
+            st8_plain(static_cast<uint16_t*>(chunk) + e, Payload<DT>::narrow(f), Payload<DT>::narrow(f + 2));
+        }
+    } else {
+        store_elems<DT>(chunk, e, 4, len, f);
+    }
+}
 // A warp's batch: L lines (L / 4 per lane group of 8 lanes), two forms.  A
 // hop's latency is set by the instructions one warp issues for its batch,
 // not by the transfer, so small calls use short batches (L = 8: a short
@@ -59,7 +99,7 @@ template <int L> struct Geo {
     static constexpr int kLines = L;
     static constexpr int kSlots = L == 8 ? 6 : 3;                     // inbox slots per warp
     static constexpr int kMinBlocks = L == 8 ? 4 : 2;
-    static constexpr size_t kBatchElems = (size_t)kLineWords * L;
+    static constexpr size_t kBatchElems = (size_t)kCWords * L;
     static constexpr size_t kSlotBytes = (size_t)L * 128;
     static constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kSlotBytes;
     // inbox, then full[kCWarps][kSlots] and empty[kCWarps][kSlots] mbarriers and the abort word
@@ -192,7 +232,6 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     const size_t k = blockIdx.x / NR;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 3, j = lane & 7;
-    const int nw = j < 7 ? 4 : 2;
     const int d = (r + 1) % NR, p = (r + NR - 1) % NR;   // next and previous rank
     ClusterSmem S;
     S.inbox = smem_addr(smem);
@@ -210,7 +249,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     cluster_barrier();
 
     const size_t slice_lo = k * epc;
-    const size_t line_lo = slice_lo / kLineWords;
+    const size_t line_lo = slice_lo / kCWords;
     const uint32_t my_box = S.inbox + (uint32_t)(warp * kSlots * kSlotBytes);
     const uint32_t peer_box = peer_addr(my_box, (uint32_t)d);             // the next rank's inbox for this warp
     const uint32_t my_full = S.full + (uint32_t)(warp * kSlots * 8);      // + 8 s: slot s of my inbox
@@ -233,7 +272,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         Geom G;
         G.len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
         G.slice_hi = slice_lo + epc < G.len ? slice_lo + epc : G.len;
-        const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
+        const size_t nlines = G.slice_hi > slice_lo ? (G.slice_hi - slice_lo + kCWords - 1) / kCWords : 0;
         G.nbatch = (nlines + kCLines - 1) / kCLines;
         G.x = static_cast<const T*>(in.p[r]) + lo;
         G.y = static_cast<T*>(out.p[r]) + lo;
@@ -241,7 +280,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     };
     // lines of batch b (from line_lo + 32 b) below the slice's end
     auto live_lines = [&](size_t base, const Geom& G) -> uint32_t {
-        const size_t end = (G.slice_hi + kLineWords - 1) / kLineWords;
+        const size_t end = (G.slice_hi + kCWords - 1) / kCWords;
         return base >= end ? 0u : (uint32_t)(end - base < (size_t)kCLines ? end - base : kCLines);
     };
     constexpr int kLast = 2 * NR - 2;   // t = 2n-2: only the last receive
@@ -261,7 +300,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < kI; ++i) {
             const size_t l = base + 4 * i + g;
-            load_raw<DT>(G.x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < G.slice_hi ? G.len : 0, xr[i]);
+            load4<DT>(G.x, l * kCWords + 4 * (size_t)j, l * kCWords < G.slice_hi ? G.len : 0, xr[i]);
         }
     };
 
@@ -294,18 +333,6 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < kI; ++i)
                 if ((uint32_t)(4 * i + g) < nlive) w[i] = ld16_local(slot + (uint32_t)((4 * i + g) * 128 + 16 * j));
-            // every line carries its flag: the batch number + 1
-            bool flags_ok = true;
-#pragma unroll
-            for (int i = 0; i < kI; ++i)
-                if (j == 7 && (uint32_t)(4 * i + g) < nlive)
-                    flags_ok = flags_ok && (((uint64_t)w[i].w << 32) | w[i].z) == q_recv + 1;
-            if (!__all_sync(kCFull, flags_ok)) {
-                if (!flags_ok) report_flag_timeout(st, r, base);
-                if (lane == 0) raise_abort<NR>(S);
-                dead = true;
-                break;
-            }
         }
         float v[kI][4];
 #pragma unroll
@@ -352,16 +379,12 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             const uint32_t slot = peer_box + s * (uint32_t)kSlotBytes;
             const uint32_t bar = peer_full + 8 * s;
             if (lane == 0) mbar_arrive_expect_tx_peer(bar, nlive * 128u);
-            const uint64_t flag = q_send + 1;
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 if ((uint32_t)(4 * i + g) >= nlive) continue;
                 const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
-                const uint4 val = j < 7 ? make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
-                                                     __float_as_uint(v[i][2]), __float_as_uint(v[i][3]))
-                                        : make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
-                                                     (uint32_t)flag, (uint32_t)(flag >> 32));
-                st16_async_peer(a, val, bar);
+                st16_async_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                              __float_as_uint(v[i][2]), __float_as_uint(v[i][3])), bar);
             }
             ++q_send;
         }
@@ -370,7 +393,7 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
-                if (l * kLineWords < G.slice_hi) store_elems<DT>(G.y, l * kLineWords + 4 * (size_t)j, nw, G.len, v[i]);
+                if (l * kCWords < G.slice_hi) store4<DT>(G.y, l * kCWords + 4 * (size_t)j, G.len, v[i]);
             }
         }
         if (!dead && ld_rlx_local(S.abort) != 0) dead = true;

@@ -349,12 +349,16 @@ int ar_ring_rounded_fused(ar_handle h, const void* const* in, void* const* out, 
 int ar_ring_persistent(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
 
-/* The persistent LL128 ring of ar_ring_persistent with the ranks mapped onto
- * the CTAs of a thread-block cluster (cluster size n_ranks, up to 16): a hop
- * writes the LL128 lines (and their flags) straight into the receiving CTA's
- * shared memory, so the lines never reach L2 or HBM, and polling is local.
- * Each cluster owns a slice of every chunk; clusters are independent.  Same
- * bits as ar_ring.  Needs no optional buffers.  Waits are bounded as in
+/* The ring of ar_ring in one launch with the ranks mapped onto the CTAs of a
+ * thread-block cluster (cluster size n_ranks, up to 16): a hop is a batch of
+ * 128-byte lines of fp32 partials that the sending CTA writes straight into
+ * the receiving CTA's shared memory with asynchronous stores counted on the
+ * receiving slot's mbarrier (the handbook's Simple protocol shape: data plus
+ * a separate completion signal), so the lines never reach L2 or HBM and the
+ * receiver waits on one local barrier.  Each cluster owns a slice of every
+ * chunk; clusters are independent.  Short batches (8 lines per warp) for
+ * small calls, long ones (32 lines) for large.  Same bits as ar_ring.  Needs
+ * no optional buffers.  Waits are bounded by AR_OPT_SPIN_NS as in
  * ar_ring_persistent; AR_OPT_ABSENT_RANK applies.  AR_ERR_CUDA if the device
  * cannot run a cluster of n_ranks CTAs.  HBM: reads n S, writes n S. */
 int ar_ring_cluster(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
