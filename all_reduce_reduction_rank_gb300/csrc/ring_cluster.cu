@@ -94,11 +94,14 @@ __device__ __forceinline__ void store4(void* chunk, size_t e, size_t len, const 
 // chain per hop, a step spread over more warps); large calls, which are
 // bound by instruction throughput, use long ones (L = 32: the per-batch work
 // amortised over 4x the data).  kSlots batches per warp fit the inbox, and
-// kMinBlocks CTAs fit on an SM.
+// the kernel is compiled for kMinBlocks CTAs per SM.  Measured on GB300 (n = 8
+// bf16, graph replay): 13.7 / 16.1 us at 64 KiB / 1 MiB per rank with short
+// batches, 61.6 us at 8 MiB and 463 us at 64 MiB with long ones; 16- and
+// 24-line batches, and three CTAs per SM for long ones, were slower.
 template <int L> struct Geo {
     static constexpr int kLines = L;
-    static constexpr int kSlots = L == 8 ? 6 : 3;                     // inbox slots per warp
-    static constexpr int kMinBlocks = L == 8 ? 4 : 2;
+    static constexpr int kSlots = L == 8 ? 6 : 3;   // inbox slots per warp
+    static constexpr int kMinBlocks = 2;             // 4 for short batches measured 0.9-1.3 us slower
     static constexpr size_t kBatchElems = (size_t)kCWords * L;
     static constexpr size_t kSlotBytes = (size_t)L * 128;
     static constexpr size_t kInboxBytes = (size_t)kCWarps * kSlots * kSlotBytes;
@@ -516,9 +519,9 @@ int launch_ring_cluster(Handle& h, const void* const* in, void* const* out, size
                 return launch_status();
             };
             // short batches while one wave of clusters gives every warp at most two
-            // of them per step (measured on GB300, n = 8 bf16: 17.5 / 20.8 us at
-            // 64 KiB / 1 MiB per rank against 30.6 / 33.4 with long batches, and
-            // 110 against 80 us at 8 MiB, where long batches win)
+            // of them per step: small calls are latency-bound and gain from short
+            // batches (14.6 against 30.6 us at 64 KiB, n = 8 bf16), large ones are
+            // bound by instruction throughput and gain from long ones
             const int res8 = cluster_setup<NR, DT, 8>();
             if (res8 > 0 && C <= (size_t)res8 * kCWarps * Geo<8>::kBatchElems * 2)
                 return run(std::integral_constant<int, 8>{});

@@ -13,8 +13,9 @@
 // Layout: one thread-block cluster of CL CTAs per token row (8; 16, a
 // non-portable cluster size, while the CTAs of 16-CTA clusters fit in one
 // wave); CTA c of the cluster owns a contiguous slice of the row.  Pass
-// 1 reads the n rank slices once, writes r, keeps r (fp32) in shared memory
-// and accumulates its squares; each CTA sends its partial sum into every
+// 1 reads the n rank slices once, writes r, keeps r (fp32: a thread's first
+// vector in registers, any further ones in shared memory) and accumulates its
+// squares; each CTA sends its partial sum into every
 // CTA's shared memory (distributed shared memory) with an asynchronous store
 // counted on the receiver's mbarrier, so each CTA waits only until the CL
 // partials have landed in its own shared memory (no second cluster barrier),
@@ -54,9 +55,9 @@ __device__ __forceinline__ void st_async_cluster_f32(float* local, const uint64_
                  : "memory");
 }
 
-// Compiled for at least four CTAs per SM: 72 registers at n = 8 where the
-// compiler's own choice was 64, and 1-3% less time per call at 1-64 tokens
-// (graph-replay A/B on GB300, n = 8 bf16).
+// Compiled for at least four CTAs per SM (79 registers at n = 8, no spills at
+// any n); a bound of four measured 1-3% less time per call at 1-64 tokens
+// than the compiler's own choice (graph-replay A/B on GB300, n = 8 bf16).
 template <int NR, int DT, int CL>
 __global__ void __launch_bounds__(kNormThreads, 4)
 allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __restrict__ residual,
@@ -93,6 +94,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     // before any is used, so the pass waits on memory once.
     float ss = 0.0f;
     uint4 w_first = make_uint4(0u, 0u, 0u, 0u);   // the weight of this thread's first vector
+    float r_first[VE];                             // r of this thread's first vector (the rest in shared memory)
     for (size_t v = v_lo + threadIdx.x; v < v_hi; v += kNormThreads) {
         uint4 x[NR];
 #pragma unroll
@@ -113,12 +115,16 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
         float rq[VE];
 #pragma unroll
         for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(rr, j), rq + j * Payload<DT>::kPerWord);
-        float* dst = r_slice + (v - v_lo) * VE;
+        if (v == v_lo + threadIdx.x) {
 #pragma unroll
-        for (int k = 0; k < VE; ++k) {
-            dst[k] = rq[k];
-            ss = ss + rq[k] * rq[k];
+            for (int k = 0; k < VE; ++k) r_first[k] = rq[k];
+        } else {
+            float* dst = r_slice + (v - v_lo) * VE;
+#pragma unroll
+            for (int k = 0; k < VE; ++k) dst[k] = rq[k];
         }
+#pragma unroll
+        for (int k = 0; k < VE; ++k) ss = ss + rq[k] * rq[k];
     }
     // the CTA's sum of squares: warps, then the warps in order
 #pragma unroll
@@ -126,10 +132,12 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
     if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = ss;
     __syncthreads();
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (threadIdx.x == 0) {   // this CTA's partial, sent into every CTA of the cluster
+    if (threadIdx.x < CL) {   // this CTA's partial, sent into CTA k of the cluster by thread k
         float s = 0.0f;
         for (int w = 0; w < kNormThreads / 32; ++w) s = s + warp_part[w];
-        for (uint32_t k = 0; k < CL; ++k) st_async_cluster_f32(&parts[c], &parts_bar, k, s);
+        st_async_cluster_f32(&parts[c], &parts_bar, threadIdx.x, s);
+    }
+    if (threadIdx.x == 0) {
         // wait (bounded) until all CL partials have landed here; a CTA leaves only
         // after that, so nothing is still landing in its shared memory when it exits
         const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&parts_bar);
@@ -160,7 +168,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ CPtrs<NR> in, const void* __res
         float wf[VE], y[VE];
 #pragma unroll
         for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(wv, j), wf + j * Payload<DT>::kPerWord);
-        const float* src = r_slice + (v - v_lo) * VE;
+        const float* src = v == v_lo + threadIdx.x ? r_first : r_slice + (v - v_lo) * VE;
 #pragma unroll
         for (int k = 0; k < VE; ++k) y[k] = (src[k] * inv) * wf[k];
         const uint4 yo = round_vec<DT>(y);
