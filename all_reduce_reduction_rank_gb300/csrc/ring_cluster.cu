@@ -14,8 +14,10 @@
 // a separate completion signal) rather than LL128's flag in every line:
 // inside a cluster the barrier's byte count gives what the per-line flag
 // gives over NVLink -- the data and its arrival in one operation -- without
-// spending 8 bytes of every line on it.  HBM sees only the ranks' own
-// elements and outputs: 2 n S per call.
+// spending 8 bytes of every line on it.  For 16-bit payloads the all-gather
+// hops carry the completed (already rounded) values in the payload type,
+// half the bytes of fp32 lines.  HBM sees only the ranks' own elements and
+// outputs: 2 n S per call.
 //
 // Layout: cluster size n (one CTA per rank, cluster_ctarank = rank);
 // cluster k owns slice [k E, (k+1) E) of every chunk (E a multiple of one
@@ -73,6 +75,21 @@ __device__ __forceinline__ void load4(const void* chunk, size_t e, size_t len, u
     }
 }
 
+// Stores eight 16-bit elements (raw bits, one 16-byte vector) from e, those below len.
+template <int DT>
+__device__ __forceinline__ void store8_raw(void* chunk, size_t e, size_t len, const uint4& v)
+{
+    uint16_t* y = static_cast<uint16_t*>(chunk);
+    if (e + 8 <= len) {
+        st16(y + e, v);
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (e + u < len) y[e + u] = (uint16_t)(w[u >> 1] >> (16 * (u & 1)));
+    }
+}
+
 // Rounds f[0..4) to the payload type and stores the elements below len.
 template <int DT>
 __device__ __forceinline__ void store4(void* chunk, size_t e, size_t len, const float* f)
@@ -95,9 +112,10 @@ __device__ __forceinline__ void store4(void* chunk, size_t e, size_t len, const 
 // bound by instruction throughput, use long ones (L = 32: the per-batch work
 // amortised over 4x the data).  kSlots batches per warp fit the inbox, and
 // the kernel is compiled for kMinBlocks CTAs per SM.  Measured on GB300 (n = 8
-// bf16, graph replay): 13.7 / 16.1 us at 64 KiB / 1 MiB per rank with short
-// batches, 61.6 us at 8 MiB and 463 us at 64 MiB with long ones; 16- and
-// 24-line batches, and three CTAs per SM for long ones, were slower.
+// bf16, graph replay): 12.1 / 14.4 us at 64 KiB / 1 MiB per rank with short
+// batches, 49.2 us at 8 MiB and 365 us at 64 MiB with long ones (the step
+// ring: 19.0 / 23.2 / 58.6 / 435 us); 16- and 24-line batches, and three CTAs
+// per SM for long ones, were slower.
 template <int L> struct Geo {
     static constexpr int kLines = L;
     static constexpr int kSlots = L == 8 ? 6 : 3;   // inbox slots per warp
@@ -187,6 +205,14 @@ __device__ __forceinline__ void st16_async_peer(uint32_t a, const uint4& v, uint
                  : "memory");
 }
 
+// 8 bytes into another CTA's shared memory, counted on its barrier `bar`.
+__device__ __forceinline__ void st8_async_peer(uint32_t a, uint32_t x, uint32_t y, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1,%2}, [%3];" ::"r"(a),
+                 "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
 struct ClusterSmem {
     uint32_t inbox;   // shared address of this CTA's inbox
     uint32_t full;    // full[0][0]
@@ -228,6 +254,10 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     constexpr int kCLines = Geo<L>::kLines, kSlots = Geo<L>::kSlots;
     constexpr size_t kSlotBytes = Geo<L>::kSlotBytes;
     constexpr int kI = kCLines / 4;
+    // 16-bit payloads: the all-gather hops carry the completed values in the payload type (half the
+    // bytes of fp32 lines); fp32 payloads keep fp32 lines throughout
+    constexpr bool kNarrowGather = DT != AR_F32;
+    constexpr int kV = kCLines / 8 > 0 ? kCLines / 8 : 1;   // 16-byte payload vectors per lane of a batch
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t crank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
@@ -319,6 +349,69 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
         const bool sends = t <= kLast - 1;
         const size_t base = line_lo + b * kCLines;
         const uint32_t nlive = live_lines(base, G);
+        if (kNarrowGather && t >= NR) {
+            // an all-gather hop carries the completed values in the payload type: 16-byte
+            // vectors of 8 elements, vector u = lane + 32 i of the batch (4 per 32-element line)
+            const uint32_t nvec = 4 * nlive;
+            const uint32_t s = (uint32_t)(q_recv % kSlots);
+            const uint32_t slot = my_box + s * (uint32_t)kSlotBytes;
+            if (!warp_wait(my_full + 8 * s, (uint32_t)((q_recv / kSlots) & 1), S.abort, spin_ns)) {
+                if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                    report_flag_timeout(st, r, base);
+                    raise_abort<NR>(S);
+                }
+                dead = true;
+                break;
+            }
+            uint4 pv[kV];
+#pragma unroll
+            for (int i = 0; i < kV; ++i) {
+                const uint32_t u = (uint32_t)(lane + 32 * i);
+                pv[i] = u < nvec ? ld16_local(slot + 16u * u) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // this rank's output first: the stores use the loaded vectors, so every load of
+            // the slot has returned before the slot is freed below (elements past the slice's
+            // end are neither stored nor read by anyone)
+#pragma unroll
+            for (int i = 0; i < kV; ++i) {
+                const size_t e = base * kCWords + 8 * (size_t)(lane + 32 * i);
+                if (e < G.slice_hi) store8_raw<DT>(G.y, e, G.len, pv[i]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_peer(prev_empty + 8 * s);
+            ++q_recv;
+            int t2 = t;
+            size_t b2 = b;
+            Geom G2 = G;
+            next_pair(t2, b2, G2);
+            if (sends) {
+                const uint32_t so = (uint32_t)(q_send % kSlots);
+                if (q_send >= kSlots &&
+                    !warp_wait(my_empty + 8 * so, (uint32_t)((q_send / kSlots - 1) & 1), S.abort, spin_ns)) {
+                    if (lane == 0 && ld_rlx_local(S.abort) == 0) {
+                        report_wait_timeout(st);
+                        raise_abort<NR>(S);
+                    }
+                    dead = true;
+                    break;
+                }
+                const uint32_t oslot = peer_box + so * (uint32_t)kSlotBytes;
+                const uint32_t bar = peer_full + 8 * so;
+                if (lane == 0) mbar_arrive_expect_tx_peer(bar, nvec * 16u);
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    const uint32_t u = (uint32_t)(lane + 32 * i);
+                    if (u < nvec) st16_async_peer(oslot + 16u * u, pv[i], bar);
+                }
+                ++q_send;
+            }
+            if (!dead && ld_rlx_local(S.abort) != 0) dead = true;
+            dead = __any_sync(kCFull, dead);
+            t = t2;
+            b = b2;
+            G = G2;
+            continue;
+        }
         uint4 w[kI];
 #pragma unroll
         for (int i = 0; i < kI; ++i) w[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -355,6 +448,16 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
                 for (int u = 0; u < 4; ++u) v[i][u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[i][u]));
             }
         }
+        if (t >= NR) {
+            // an all-gather hop in fp32 lines: nothing above used the loaded lines, so this
+            // rank's output goes first -- its stores use them, so every load of the slot has
+            // returned before the slot is freed below
+#pragma unroll
+            for (int i = 0; i < kI; ++i) {
+                const size_t l = base + 4 * i + g;
+                if (l * kCWords < G.slice_hi) store4<DT>(G.y, l * kCWords + 4 * (size_t)j, G.len, v[i]);
+            }
+        }
         if (t >= 1) {
             // the slot's lines are in registers and used: free it for the previous rank
             __syncwarp();
@@ -381,18 +484,29 @@ ring_cluster_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
             }
             const uint32_t slot = peer_box + s * (uint32_t)kSlotBytes;
             const uint32_t bar = peer_full + 8 * s;
-            if (lane == 0) mbar_arrive_expect_tx_peer(bar, nlive * 128u);
+            if (kNarrowGather && t == NR - 1) {
+                // the first all-gather hop: the rounded values in the payload type, 8 bytes a lane
+                if (lane == 0) mbar_arrive_expect_tx_peer(bar, nlive * 64u);
 #pragma unroll
-            for (int i = 0; i < kI; ++i) {
-                if ((uint32_t)(4 * i + g) >= nlive) continue;
-                const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
-                st16_async_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
-                                              __float_as_uint(v[i][2]), __float_as_uint(v[i][3])), bar);
+                for (int i = 0; i < kI; ++i) {
+                    if ((uint32_t)(4 * i + g) >= nlive) continue;
+                    st8_async_peer(slot + (uint32_t)((4 * i + g) * 64 + 8 * j), Payload<DT>::narrow(v[i]),
+                                   Payload<DT>::narrow(v[i] + 2), bar);
+                }
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx_peer(bar, nlive * 128u);
+#pragma unroll
+                for (int i = 0; i < kI; ++i) {
+                    if ((uint32_t)(4 * i + g) >= nlive) continue;
+                    const uint32_t a = slot + (uint32_t)((4 * i + g) * 128 + 16 * j);
+                    st16_async_peer(a, make_uint4(__float_as_uint(v[i][0]), __float_as_uint(v[i][1]),
+                                                  __float_as_uint(v[i][2]), __float_as_uint(v[i][3])), bar);
+                }
             }
             ++q_send;
         }
-        // this rank's output last, after the hop is on its way
-        if (t >= NR - 1) {
+        // the completing step's output last, after the hop is on its way
+        if (t == NR - 1) {
 #pragma unroll
             for (int i = 0; i < kI; ++i) {
                 const size_t l = base + 4 * i + g;
