@@ -444,7 +444,8 @@ int ar_create(int n_ranks, size_t max_bytes, ar_handle* out)
     h.max_bytes = max_bytes;
     int rc = AR_OK;
     if (cudaGetDevice(&h.device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&h.sm_count, cudaDevAttrMultiProcessorCount, h.device) != cudaSuccess)
+        cudaDeviceGetAttribute(&h.sm_count, cudaDevAttrMultiProcessorCount, h.device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h.l2_bytes, cudaDevAttrL2CacheSize, h.device) != cudaSuccess)
         rc = AR_ERR_CUDA;
     // ring scratch: the largest chunk over the payload types
     size_t cmax = 0;

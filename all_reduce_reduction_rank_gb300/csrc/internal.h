@@ -36,6 +36,7 @@ struct Handle {
     size_t max_bytes = 0;
     int device = 0;
     int sm_count = 0;
+    int l2_bytes = 0;   // the device's L2 size
     int ctas_per_sm = 0;  // 0: one full wave, from each kernel's occupancy
     int64_t spin_ns = 1000000;
     int one_shot_impl = 0;

@@ -33,14 +33,43 @@ namespace {
 constexpr int kRsUnroll = 2;  // vectors per thread per iteration
 constexpr int kAgUnroll = 4;
 
-// Reduce-scatter step s.  Grid: blockIdx.y = sending rank r (block-uniform
-// chunk, pointers and step role), blockIdx.x strides over the chunk's 16-byte
-// vectors.  p_read / p_write: partials, rank-major, C elements per rank; fp32,
+// The rank (row) r and the x position bx of this CTA in step g of the ring's
+// 2(n-1) steps (g = s in the reduce-scatter, n - 1 + s in the all-gather).
+// Every step reads what the step before wrote: row r reads the data row r - 1
+// wrote.  When a step's data is larger than L2 (reorder), each step takes its
+// tiles in the reverse of the order in which the step before wrote the data
+// they read: CTAs are dispatched roughly in linear block order and L2 keeps
+// the most recently written lines, so the first tiles a step reads are the
+// last written, still in L2.  Hence odd steps reverse the block order (rows
+// and x), and every step rotates its rows by g so that row r's reads follow
+// row r - 1's writes.  Measured on GB300 (n = 8 bf16, 64 MiB per rank): 4.6%
+// fewer DRAM bytes per reduce-scatter step, 29% fewer per all-gather step, the
+// ring 3% faster; at 8 MiB (everything in L2) the plain order is 2% faster.
+// Which CTA does which tile changes nothing in the sums.
+// A template flag, not a runtime one: a runtime flag cost the step kernel 14
+// registers and with them a CTA per SM.
+template <int NR, bool RO>
+__device__ __forceinline__ void ring_tile(int g, int& r, unsigned& bx)
+{
+    if constexpr (RO) {
+        const bool rev = (g & 1) != 0;
+        const int yb = rev ? NR - 1 - (int)blockIdx.y : (int)blockIdx.y;
+        r = (yb + g) % NR;
+        bx = rev ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
+    } else {
+        r = (int)blockIdx.y;
+        bx = blockIdx.x;
+    }
+}
+
+// Reduce-scatter step s.  Grid: blockIdx.y gives the sending rank r
+// (block-uniform chunk, pointers and step role; see ring_tile), blockIdx.x
+// strides over the chunk's 16-byte vectors.  p_read / p_write: partials, rank-major, C elements per rank; fp32,
 // or (HR, hop rounding) the payload type.  The fp32-partial step is compiled
 // for three CTAs per SM (at most 80 registers; the ring measured 3% faster at
 // 8 MiB per rank); the hop-rounded step keeps the compiler's own choice (a
 // minimum of 0), which ran 10-16% faster at 8-64 MiB than that bound.
-template <int NR, int DT, bool HR>
+template <int NR, int DT, bool HR, bool RO>
 __global__ void __launch_bounds__(kThreads, HR ? 0 : 3)
 ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
                     const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s)
@@ -50,7 +79,9 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     constexpr int PW = HR ? 1 : VE / 4;  // 16-byte words of partial per payload vector
     constexpr int U = kRsUnroll;
     using T = typename Payload<DT>::scalar_t;
-    const int r = blockIdx.y;
+    int r;
+    unsigned bx;
+    ring_tile<NR, RO>(s, r, bx);
     const int d = (r + 1) % NR;
     const int c = (r - s + NR) % NR;
     const bool first = (s == 0), last = (s == NR - 2);
@@ -66,7 +97,7 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     const T* const prh = reinterpret_cast<const T*>(p_read) + (size_t)r * C;   // HR layout
     T* const pwh = reinterpret_cast<T*>(p_write) + (size_t)d * C;
     const size_t span = (size_t)kThreads * U;
-    for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
+    for (size_t base = (size_t)bx * span; base < nv; base += (size_t)gridDim.x * span) {
         uint4 up[U][PW], own[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -134,8 +165,8 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 }
 
 // All-gather step s: out[r+1][chunk (r+1-s)] = out[r][chunk (r+1-s)].
-// Grid: blockIdx.y = sending rank r.
-template <int NR, int DT>
+// Grid: blockIdx.y gives the sending rank r (see ring_tile).
+template <int NR, int DT, bool RO>
 __global__ void __launch_bounds__(kThreads)
 ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t count, int s)
 {
@@ -143,7 +174,9 @@ ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t coun
     constexpr int VE = kVecElems<DT>;
     constexpr int U = kAgUnroll;
     using T = typename Payload<DT>::scalar_t;
-    const int r = blockIdx.y;
+    int r;
+    unsigned bx;
+    ring_tile<NR, RO>(NR - 1 + s, r, bx);
     const int d = (r + 1) % NR;
     const int c = (r + 1 - s + NR) % NR;
     const size_t e_lo = (size_t)c * C;
@@ -153,7 +186,7 @@ ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t coun
     const T* const src = static_cast<const T*>(out.p[r]) + e_lo;
     T* const dst = static_cast<T*>(out.p[d]) + e_lo;
     const size_t span = (size_t)kThreads * U;
-    for (size_t base = (size_t)blockIdx.x * span; base < nv; base += (size_t)gridDim.x * span) {
+    for (size_t base = (size_t)bx * span; base < nv; base += (size_t)gridDim.x * span) {
         uint4 x[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -195,6 +228,9 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             const dim3 g_rs(grid_for_rows(h, (cvec + kRsUnroll - 1) / kRsUnroll, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
             float* buf[2] = {h.ring_scratch, h.ring_scratch + (size_t)NR * C};
+            // a step's partials (fp32, or the payload when rounded per hop) larger than half of L2
+            const uint64_t step_bytes = (uint64_t)count * (HR ? sizeof(typename Payload<DT>::scalar_t) : 4u);
+            const bool reorder = h.l2_bytes > 0 && step_bytes > (uint64_t)h.l2_bytes / 2;
             int n_launch = 0;
             // per step every chunk moves once: N elements in all
             const uint64_t N = count, e = sizeof(typename Payload<DT>::scalar_t);
@@ -204,15 +240,22 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             for (int step = 0; step < NR - 1; ++step) {
                 const uint64_t pe = HR ? e : 4;   // bytes of one partial
                 rs_bytes += (step == 0 ? e : pe) * N + e * N + (step == NR - 2 ? e : pe) * N;
-                launch_kernel(h, ring_rs_step_kernel<NR, DT, HR>, g_rs, kThreads, 0, s, ip, op, buf[(step + 1) & 1],
-                              buf[step & 1], C, count, step);
+                if (reorder)
+                    launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, true>, g_rs, kThreads, 0, s, ip, op,
+                                  buf[(step + 1) & 1], buf[step & 1], C, count, step);
+                else
+                    launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, false>, g_rs, kThreads, 0, s, ip, op,
+                                  buf[(step + 1) & 1], buf[step & 1], C, count, step);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }
             rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, NR - 1);
             rec_begin(h, s);
             for (int step = 0; step < NR - 1; ++step) {
-                launch_kernel(h, ring_ag_step_kernel<NR, DT>, g_ag, kThreads, 0, s, op, C, count, step);
+                if (reorder)
+                    launch_kernel(h, ring_ag_step_kernel<NR, DT, true>, g_ag, kThreads, 0, s, op, C, count, step);
+                else
+                    launch_kernel(h, ring_ag_step_kernel<NR, DT, false>, g_ag, kThreads, 0, s, op, C, count, step);
                 ++n_launch;
                 if (launch_status() != AR_OK) return AR_ERR_CUDA;
             }

@@ -212,17 +212,20 @@ def test_cluster_ring_timing_record_and_plan():
     assert recs[0][3] == t.hbm_read_bytes + t.hbm_write_bytes == 2 * n * N * 4
 
 
-@pytest.mark.parametrize("n,N", [(2, 16 << 20), (8, 32 << 20)])
-def test_cluster_ring_large_slices(n, N):
-    # sizes where one wave of clusters would give a warp many batches per
-    # step: the slices are capped so that a step's batches fit the inbox
-    ins = workloads.rank_inputs_device(n, N, "bf16", "normal_over_n", 4321 + n)
+@pytest.mark.parametrize("n,N,dtype", [(2, 16 << 20, "bf16"), (8, 32 << 20, "bf16"), (8, 8 << 20, "f32"),
+                                       (4, 16 << 20, "f16"), (16, 4 << 20, "bf16")])
+def test_cluster_ring_large_slices(n, N, dtype):
+    # sizes where one wave of clusters would give a warp many batches per step: the slices
+    # are capped so that a step's batches fit the inbox, the calls run in several waves, and
+    # every inbox slot is reused many times (fp32 lines in every hop for f32, payload-type
+    # all-gather hops for 16-bit data)
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", 4321 + n)
     a = [torch.empty_like(t) for t in ins]
     c = [torch.empty_like(t) for t in ins]
-    h = ar.ar_create(n, 2 * N)
+    h = ar.ar_create(n, E[dtype] * N)
     try:
-        assert ar.ar_ring(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in a], N, "bf16") == ar.AR_OK
-        assert ar.ar_ring_cluster(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in c], N, "bf16") == ar.AR_OK
+        assert ar.ar_ring(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in a], N, dtype) == ar.AR_OK
+        assert ar.ar_ring_cluster(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in c], N, dtype) == ar.AR_OK
         torch.cuda.synchronize()
         assert ar.ar_status(h) == ar.AR_OK
     finally:
