@@ -172,3 +172,30 @@ def test_fused_rings_at_the_prefill_size():
     for r in (0, 4, 7):
         np.testing.assert_array_equal(outs["fused"][r].cpu().numpy().view(np.uint16), want[r])
         np.testing.assert_array_equal(outs["rounded_fused"][r].cpu().numpy().view(np.uint16), want_rounded[r])
+
+
+def test_prefill_64mib_whole_buffers_against_the_oracle():
+    # the bench's own size, n = 8 bf16 at 64 MiB per rank, every element of every rank's output
+    # against the oracle: one-shot and two-shot (the default, one launch) against the rank-order
+    # sum, the step ring and the cluster ring against the ring's order
+    n, dtype, S = 8, "bf16", 64 * MiB
+    N = S // 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(3) + 7)
+    xs = [t.cpu().numpy().view(np.uint16) for t in ins]
+    want_sum = oracle.all_reduce(xs, dtype)[0]
+    want_ring = oracle.ring(xs, dtype)[0]
+    outs = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, S)
+    try:
+        for call, want in ((ar.ar_one_shot, want_sum), (ar.ar_two_shot, want_sum), (ar.ar_ring, want_ring),
+                           (ar.ar_ring_cluster, want_ring)):
+            for o in outs:
+                o.fill_(0x5A5A)
+            _run(call, h, ins, outs, N, dtype)
+            assert ar.ar_status(h) == ar.AR_OK
+            for r in range(n):
+                got = outs[r].cpu().numpy().view(np.uint16)
+                bad = np.flatnonzero(got != want)
+                assert bad.size == 0, (call.__name__, r, bad[:5])
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
