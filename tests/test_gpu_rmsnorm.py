@@ -64,7 +64,7 @@ def _run(n, T, H, dtype, seed, in_place=False, res_in_place=False, eps=1e-6, h=N
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("n,T,H", [(8, 1, 8192), (8, 64, 4096), (2, 7, 512), (16, 3, 8200), (4, 5, 16), (8, 2, 65536),
-                                   (8, 9, 4096), (8, 10, 4096)])
+                                   (8, 9, 4096), (8, 10, 4096), (8, 48, 6144)])
 def test_fused_epilogue_matches_the_unfused_chain(dtype, n, T, H):
     if H % (16 // E[dtype]):
         pytest.skip("hidden must be whole 16-byte vectors")
