@@ -401,11 +401,12 @@ int ar_ring_noalloc(int n_ranks, const void* const* in, void* const* out, size_t
  * in tensor parallelism every rank holds the same residual; residual_out may
  * equal residual); weight: [hidden].  hidden must be a whole number of
  * 16-byte vectors and at most 327680 elements of any payload type (r is
- * kept in fp32 in shared memory, at most 160 KiB per CTA of a cluster of 8);
- * eps >= 0.  In place (norm_out[r] == in[r]) is allowed; otherwise no output
- * may overlap an input or another output.  Each token row is handled by a
- * thread-block cluster of 8 CTAs, whose partial sums of squares are combined
- * through distributed shared memory.  a and r match the unfused chain bit for
+ * kept in fp32, in registers and shared memory: a row of that length spread
+ * over 8 CTAs is 160 KiB per CTA); eps >= 0.  In place (norm_out[r] == in[r])
+ * is allowed; otherwise no output may overlap an input or another output.
+ * Each token row is handled by a thread-block cluster of 16 CTAs (8 for many
+ * short rows); each warp sends its partial sum of squares to every CTA of the
+ * cluster through distributed shared memory.  a and r match the unfused chain bit for
  * bit; y within one payload ulp (the order of the sum of squares is the
  * kernel's).  ar_plan(AR_OP_ALLREDUCE_RMSNORM) omits the weight's H bytes,
  * which ar_traffic includes after a call. */

@@ -107,10 +107,59 @@ def test_fused_epilogue_argument_errors():
         assert ar.ar_traffic(h).launches == 0
 
 
+@pytest.mark.parametrize("mode", ["stream", "graph"])
+@pytest.mark.parametrize("pdl", [0, 1])
+@pytest.mark.parametrize("T,H", [(1, 4096), (8, 8192), (48, 6144), (64, 8192)])
+def test_chained_calls_each_read_the_previous_results(mode, pdl, T, H):
+    # call k + 1 takes call k's normalized outputs as its rank inputs and call k's residual
+    # output as its residual, back to back on one stream (or replayed from a CUDA graph).
+    # With programmatic launch a call may start before the one before it has ended (small
+    # grids let the next launch in at once); it must still read that call's results.  Every
+    # output starts as a sentinel, and each call is checked against the oracle run on the
+    # values its predecessor actually left.
+    n, K, dtype = 8, 4, "bf16"
+    xs = workloads.rank_inputs(n, T * H, dtype, "normal", seed=T + H + pdl)
+    res = workloads.rank_inputs(1, T * H, dtype, "normal", seed=T + H + 1)[0]
+    w = workloads.rank_inputs(1, H, dtype, "uniform", seed=T + H + 2)[0]
+    S = T * H * 2
+    ins, rb, wb = upload_ranks(xs), Buf(S).upload(res), Buf(2 * H).upload(w)
+    outs = [empty_ranks(n, S, byte=0x3C) for _ in range(K)]
+    ros = [Buf(S).fill(0x3C) for _ in range(K)]
+    with Handle(n, S, pdl=pdl) as h:
+        s = torch.cuda.Stream()
+
+        def chain():
+            for k in range(K):
+                src, r_in = (ins, rb) if k == 0 else (outs[k - 1], ros[k - 1])
+                rc = ar.ar_allreduce_rmsnorm(h, ptrs(src), r_in.ptr, wb.ptr, 1e-6, ptrs(outs[k]), ros[k].ptr, T, H,
+                                             dtype, s)
+                assert rc == ar.AR_OK
+
+        if mode == "stream":
+            chain()
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                chain()
+            g.replay()
+        torch.cuda.synchronize()
+        assert ar.ar_status(h) == ar.AR_OK
+    prev_in, prev_res = xs, res
+    for k in range(K):
+        want_y, want_r = oracle.allreduce_rmsnorm(prev_in, prev_res, w, 1e-6, T, H, dtype)
+        got_r = ros[k].download(np.uint16)
+        got_y = [o.download(np.uint16) for o in outs[k]]
+        np.testing.assert_array_equal(got_r, want_r, err_msg=f"call {k}: residual")
+        assert _within_one_ulp(got_y[0], want_y, dtype).all(), f"call {k}: normalized output"
+        for y in got_y[1:]:
+            np.testing.assert_array_equal(y, got_y[0])
+        prev_in, prev_res = got_y, got_r
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_fused_epilogue_largest_hidden(dtype):
-    # the largest row the kernel keeps in shared memory (327680 elements: 160 KiB of fp32 per
-    # CTA of a cluster of 8), and the next whole vector past it refused
+    # the largest row the call accepts (327680 elements: its slice over a cluster of 8 CTAs
+    # is 160 KiB of fp32), and the next whole vector past it refused
     H = 327680
     got_y, got_r, want_y, want_r, _ = _run(2, 1, H, dtype, seed=77)
     np.testing.assert_array_equal(bits(got_r), bits(want_r))
