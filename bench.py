@@ -21,8 +21,8 @@ The run ends with ONE short JSON line (under 2 KB): the headline value, the
 roofline of the dominant kernel (algorithmic and DRAM rates), the oracle
 timed on the host (cpu_baseline), the end-to-end leg through host buffers
 (e2e) and the SM clocks seen during the timed region.  Everything else it
-measures goes to a details file (--details, default
-gpurun_out/bench_details.json): a decode/prefill sweep of one-shot and
+measures goes to a details file (--details; by default bench_details.json
+in the run's output directory): a decode/prefill sweep of one-shot and
 two-shot, the fused all-reduce + RMSNorm epilogue, every all-reduce call
 side by side (variants), the LL payload sweep, the n = 16 doubling sweep,
 the per-kernel table and the other CPU legs (cpu_parallel, cpu_calls).
