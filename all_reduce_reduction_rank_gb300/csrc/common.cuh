@@ -38,6 +38,26 @@ __device__ __forceinline__ void st16(void* p, const uint4& v)
                  : "memory");
 }
 
+// For a call of several launches, where one launch reads what the one before
+// wrote (the ring's steps, the tree's levels, staged copies): the store keeps
+// the default write-back policy, since st16's streaming hint marks its lines
+// first to be evicted from L2 and the next launch would then read them from
+// DRAM; and a load that is the last use of its data in the call takes the
+// streaming hint, so its lines are the first to leave L2 and the lines the
+// launch writes for the next one stay.
+__device__ __forceinline__ void st16_next(void* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld16_last(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 // Re-read for flag polling: a volatile load is never served from a stale
 // register copy and is issued every time.
 __device__ __forceinline__ uint4 ld16_volatile(const void* p)

@@ -44,7 +44,7 @@ push_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ stage, s
         const uint4 x = ld16(src + v);
 #pragma unroll
         for (int q = 0; q < NR; ++q)
-            if (q != r) st16(reinterpret_cast<uint4*>(stage + ((size_t)q * NR + r) * slot_bytes) + v, x);
+            if (q != r) st16_next(reinterpret_cast<uint4*>(stage + ((size_t)q * NR + r) * slot_bytes) + v, x);
     }
     pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
@@ -76,7 +76,7 @@ push_reduce_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__
     for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs) {
         uint4 x[NR];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) x[r] = ld16(static_cast<const uint4*>(slot(r)) + v);
+        for (int r = 0; r < NR; ++r) x[r] = ld16_last(static_cast<const uint4*>(slot(r)) + v);   // staged once
         st16(dst + v, reduce_rank_order<DT, NR>(x));
     }
     pdl_release();
@@ -104,7 +104,7 @@ copyin_kernel(const __grid_constant__ CPtrs<NR> in, uint8_t* __restrict__ reg, s
     uint4* const dst = reinterpret_cast<uint4*>(reg + (size_t)r * slot_bytes);
     const size_t bs = Small ? (size_t)blockDim.x : (size_t)kThreads;
     for (size_t v = (size_t)blockIdx.x * bs + threadIdx.x; v < nvec; v += (size_t)gridDim.x * bs)
-        st16(dst + v, ld16(src + v));
+        st16_next(dst + v, ld16(src + v));   // the one-shot launch after it reads it
     pdl_release();
     if (blockIdx.x == gridDim.x - 1) {
         const size_t i = nvec * kVecElems<DT> + threadIdx.x;

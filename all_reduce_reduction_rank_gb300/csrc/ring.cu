@@ -32,32 +32,15 @@ namespace {
 
 // Every store of a ring step is read by the next step (the partial the next
 // hop adds to, the chunk the next all-gather hop passes on), so it keeps the
-// default write-back policy: st16's streaming hint marks its lines first to
-// be evicted from L2, and the next launch then reads them from DRAM.
-// Measured on GB300 (n = 8 bf16, back-to-back calls): at 64 MiB per rank the
-// ring 385 against 421 us and the hop-rounded ring 294 against 317 us; no
-// change at 8 MiB.  Evict-last stores, and discarding the dead partial lines
-// from L2 after their last read, were each slower.
-__device__ __forceinline__ void st16_next(void* p, const uint4& v)
-{
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// A reduce-scatter step's reads are each the last use of their data in the
-// ring (the partial it adds to is dead once read; the payload chunk is read
-// once), so they load with the streaming hint: their lines are the first to
-// leave L2, which keeps the partials the step writes there for the next step.
-// Measured on GB300 (n = 8 bf16, back to back): the ring 376.5 against
-// 380.6 us at 64 MiB per rank, 60.8 against 62.9 us at 8 MiB; the hint on the
-// payload reads alone changed nothing, nor did it on the all-gather's reads.
-__device__ __forceinline__ uint4 ld16_last(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
+// default write-back policy (st16_next), and a reduce-scatter step's reads are
+// each the last use of their data (the partial it adds to is dead once read,
+// the payload chunk is read once), so they load with the streaming hint
+// (ld16_last).  Measured on GB300 (n = 8 bf16, back-to-back calls): the stores
+// took the ring from 421 to 385 us at 64 MiB per rank and the hop-rounded ring
+// from 317 to 294 us (no change at 8 MiB); the loads then 380.6 -> 376.5 us at
+// 64 MiB and 62.9 -> 60.8 us at 8 MiB.  Evict-last stores (an L2 cache
+// policy), discarding the dead partial lines from L2 after their last read,
+// and the streaming hint on the all-gather's reads were each no faster.
 constexpr int kRsUnroll = 2;  // vectors per thread per iteration
 constexpr int kAgUnroll = 4;
 

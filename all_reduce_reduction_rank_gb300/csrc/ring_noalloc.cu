@@ -22,8 +22,9 @@
 // streams, or different host threads) race on the array; issue them in order.
 //
 // The kernels are variants of the ring step kernels of ring.cu (same chunks,
-// same rotation, same fp32 partials, same single rounding), reading and
-// writing their partials in the static array.
+// same rotation, same fp32 partials, same single rounding, the same L2 hints:
+// write-back stores for what the next step reads, streaming last-use loads),
+// reading and writing their partials in the static array.
 #include <atomic>
 #include <mutex>
 
@@ -107,27 +108,27 @@ noalloc_ring_rs_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_consta
     for (size_t k = (size_t)blockIdx.x * kThreads + threadIdx.x; k < nv; k += (size_t)gridDim.x * kThreads) {
         float a[VE];
         if (first) {
-            const uint4 x = ld16(xr + k * VE);
+            const uint4 x = ld16_last(xr + k * VE);
 #pragma unroll
             for (int j = 0; j < 4; ++j) Payload<DT>::widen(word(x, j), a + j * Payload<DT>::kPerWord);
         } else {
 #pragma unroll
             for (int j = 0; j < PW; ++j) {
-                const uint4 t = ld16(pr + k * VE + 4 * j);
+                const uint4 t = ld16_last(pr + k * VE + 4 * j);
                 a[4 * j] = __uint_as_float(t.x);
                 a[4 * j + 1] = __uint_as_float(t.y);
                 a[4 * j + 2] = __uint_as_float(t.z);
                 a[4 * j + 3] = __uint_as_float(t.w);
             }
         }
-        accumulate<DT>(a, ld16(xd + k * VE));
+        accumulate<DT>(a, ld16_last(xd + k * VE));
         if (last) {
-            st16(od + k * VE, round_vec<DT>(a));
+            st16_next(od + k * VE, round_vec<DT>(a));
         } else {
 #pragma unroll
             for (int j = 0; j < PW; ++j)
-                st16(pw + k * VE + 4 * j, make_uint4(__float_as_uint(a[4 * j]), __float_as_uint(a[4 * j + 1]),
-                                                     __float_as_uint(a[4 * j + 2]), __float_as_uint(a[4 * j + 3])));
+                st16_next(pw + k * VE + 4 * j, make_uint4(__float_as_uint(a[4 * j]), __float_as_uint(a[4 * j + 1]),
+                                                          __float_as_uint(a[4 * j + 2]), __float_as_uint(a[4 * j + 3])));
         }
     }
     if (blockIdx.x == gridDim.x - 1) {  // the ragged end of the last chunk
@@ -158,7 +159,7 @@ noalloc_ring_ag_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t c
     const T* const src = static_cast<const T*>(out.p[r]) + e_lo;
     T* const dst = static_cast<T*>(out.p[d]) + e_lo;
     for (size_t k = (size_t)blockIdx.x * kThreads + threadIdx.x; k < nv; k += (size_t)gridDim.x * kThreads)
-        st16(dst + k * VE, ld16(src + k * VE));
+        st16_next(dst + k * VE, ld16(src + k * VE));
     if (blockIdx.x == gridDim.x - 1) {
         const size_t j = nv * VE + threadIdx.x;
         if (j < len) dst[j] = src[j];

@@ -45,8 +45,8 @@ tree_level_kernel(const __grid_constant__ CPtrs<NR> src, const __grid_constant__
 #pragma unroll
         for (int k = 0; k < VE; ++k) fa[k] = fa[k] + fb[k];
         const uint4 y = round_vec<DT>(fa);
-        st16(oa + v, y);
-        st16(ob + v, y);
+        st16_next(oa + v, y);   // the next level reads it
+        st16_next(ob + v, y);
     }
     pdl_release();
     if (blockIdx.x == gridDim.x - 1) {   // the ragged tail (< VE elements)

@@ -70,7 +70,7 @@ reduce_scatter_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constan
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const size_t v = base + (size_t)u * bs + threadIdx.x;
-            if (v < hi) st16(dst + v, reduce_rank_order<DT, NR>(x[u]));
+            if (v < hi) st16_next(dst + v, reduce_rank_order<DT, NR>(x[u]));   // the all-gather launch reads it
         }
     }
     pdl_release();
