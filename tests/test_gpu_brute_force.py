@@ -10,8 +10,11 @@ subnormal inputs and results, exact ties, overflow of a finite sum to
 infinity, infinities and NaNs.  NaNs are compared by class (any NaN equals
 any NaN); every other result must match bit for bit.  A second test checks
 hand-worked results (ties, overflow, fp16 subnormal sums) against values
-written down here, independent of the oracle.
+written down here, independent of the oracle, and a third every pair of
+16-bit encodings (a 2^28 sample by default, all 2^32 with AR_EXHAUSTIVE=1).
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -105,6 +108,50 @@ def test_every_encoding_against_a_stratified_set(dtype, per_class):
                     i = int(np.flatnonzero(~ok)[0])
                     raise AssertionError(f"{name} rank {r}: {int((~ok).sum())} mismatches; first a=0x{a[i]:04x} "
                                          f"b=0x{b[i]:04x} got=0x{got[i]:04x} want=0x{want[r][i]:04x}")
+
+
+# Every pair of 16-bit encodings (2^32 sums per payload type) through ar_one_shot,
+# whose conversions (common to every kernel) are the ones under test.  By default
+# 4096 values of a, spread over the encodings by an odd multiplier (a bijection
+# of the 16-bit codes), against every b: 2^28 pairs per type.  AR_EXHAUSTIVE=1
+# runs all 65536 values of a.
+EXHAUSTIVE = os.environ.get("AR_EXHAUSTIVE") == "1"
+A_PER_CALL = 4096   # 2^28 elements of 2 bytes per rank and call
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_every_pair_of_encodings(dtype):
+    codes = np.arange(1 << 16, dtype=np.uint32)
+    a_all = codes if EXHAUSTIVE else (codes[:A_PER_CALL] * 40503) % (1 << 16)
+    b_all = codes.astype(np.uint16)
+    N = A_PER_CALL << 16
+    dev = torch.device("cuda")
+    d_in = [torch.empty(N, dtype=torch.int16, device=dev) for _ in range(2)]
+    d_out = [torch.empty(N, dtype=torch.int16, device=dev) for _ in range(2)]
+    checked = 0
+    with Handle(2, N * 2) as h:
+        for lo in range(0, a_all.size, A_PER_CALL):
+            a = np.repeat(a_all[lo:lo + A_PER_CALL].astype(np.uint16), b_all.size)
+            b = np.tile(b_all, A_PER_CALL)
+            for t, x in zip(d_in, (a, b)):
+                t.copy_(torch.from_numpy(x.view(np.int16)))
+            rc = ar.ar_one_shot(h, d_in, d_out, N, dtype)
+            assert rc == ar.AR_OK, ar.ar_strerror(rc)
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK
+            want = oracle.all_reduce([a, b], dtype)
+            for r in range(2):
+                got = d_out[r].cpu().numpy().view(np.uint16)
+                bad = np.flatnonzero(got != want[r])
+                if bad.size:   # NaNs compare by class
+                    nan = np.isnan(oracle.to_f32(got[bad], dtype)) & np.isnan(oracle.to_f32(want[r][bad], dtype))
+                    bad = bad[~nan]
+                if bad.size:
+                    i = int(bad[0])
+                    raise AssertionError(f"rank {r}: {bad.size} mismatches; first a=0x{a[i]:04x} b=0x{b[i]:04x} "
+                                         f"got=0x{got[i]:04x} want=0x{want[r][i]:04x}")
+            checked += N
+    assert checked == a_all.size << 16
 
 
 # (a, b, expected) as bit patterns, worked by hand from IEEE-754:
