@@ -199,3 +199,34 @@ def test_prefill_64mib_whole_buffers_against_the_oracle():
                 assert bad.size == 0, (call.__name__, r, bad[:5])
     finally:
         assert ar.ar_destroy(h) == ar.AR_OK
+
+
+@pytest.mark.parametrize("dtype,n,N,call,ref", [
+    ("f32", 4, (16 << 20) + 3, "ar_ring", "ring"),
+    ("f16", 3, (32 << 20) + 5, "ar_ring", "ring"),
+    ("bf16", 4, (40 << 20) + 1, "ar_ring_rounded", "ring_rounded"),
+])
+def test_ring_steps_in_the_l2_order_whole_buffers(dtype, n, N, call, ref):
+    # sizes whose step data (fp32 partials, or the payload when rounded per hop) exceeds half of
+    # L2, so the steps take their tiles in the reversed, rotated order and keep their partials in
+    # L2 with write-back stores and streaming last-use loads: every element of every rank against
+    # the oracle, with ragged chunk ends
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + n)
+    np_t = np.float32 if dtype == "f32" else np.uint16
+    xs = [t.cpu().numpy().view(np_t) for t in ins]
+    want = getattr(oracle, ref)(xs, dtype)[0]
+    outs = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, N * ins[0].element_size())
+    try:
+        for rep in range(2):   # the second call finds the first call's partials in the scratch
+            for o in outs:
+                o.fill_(0x5A5A if dtype != "f32" else 7.0)
+            _run(getattr(ar, call), h, ins, outs, N, dtype)
+            assert ar.ar_status(h) == ar.AR_OK
+            for r in range(n):
+                got = outs[r].cpu().numpy().view(np_t)
+                bad = np.flatnonzero(got.view(np.uint32 if dtype == "f32" else np.uint16)
+                                     != want.view(np.uint32 if dtype == "f32" else np.uint16))
+                assert bad.size == 0, (call, rep, r, bad[:5])
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
