@@ -771,6 +771,9 @@ def e2e_leg(wl, K: int, bytes_per_step: int) -> dict:
     # E2E_WINDOWS timed regions, the median reported: the leg issues ~50 host calls per step from
     # Python, and a region that met a busy host (one run on a shared box: 6.4 ms per step with
     # the host link measured at its usual rate right after) would otherwise set the figure alone
+    # one untimed region first: on one box the first region after the warm-up passes read 7.4 ms
+    # per step and the next two 3.5 ms
+    window()
     wins = [window() for _ in range(E2E_WINDOWS)]
     import all_reduce_reduction_rank_gb300 as ar
     for w in sets:
