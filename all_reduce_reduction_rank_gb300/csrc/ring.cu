@@ -9,7 +9,14 @@
 // over 2(p-1) steps.
 //
 // Emulation: one launch per step; one launch performs the n transfers of
-// that step.  Reduce-scatter step s: rank r sends chunk c = (r - s) mod n to
+// that step.  A call whose step data (the n chunks' partials) is larger than
+// half of L2 runs in pieces: each chunk is cut into P equal pieces (P = that
+// data over half of L2, rounded), and the whole ring -- all reduce-scatter
+// steps, then all all-gather steps -- runs on piece 0 of every chunk, then on
+// piece 1, and so on, so one piece's partials stay in L2 from step to step
+// (handbook "集合通信：NCCL 的算法、协议与推理框架的定制 all-reduce", §算法:
+// a large message cut into blocks and pipelined; every element keeps its
+// chunk and its order of summation, so the sums are the same).  Reduce-scatter step s: rank r sends chunk c = (r - s) mod n to
 // d = (r + 1) mod n.  The partial sums stay fp32 between hops, in the
 // handle's scratch [2][n][C] (double-buffered by step parity, since in one
 // step rank d both sends the partial it received in the step before and
@@ -87,7 +94,8 @@ __device__ __forceinline__ void ring_tile(int g, int& r, unsigned& bx)
 template <int NR, int DT, bool HR, bool RO>
 __global__ void __launch_bounds__(kThreads, HR ? 0 : 3)
 ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
-                    const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s)
+                    const float* __restrict__ p_read, float* __restrict__ p_write, size_t C, size_t count, int s,
+                    size_t p_len)
 {
     pdl_acquire();
     constexpr int VE = kVecElems<DT>;
@@ -102,7 +110,7 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
     const bool first = (s == 0), last = (s == NR - 2);
     const size_t e_lo = (size_t)c * C;
     if (e_lo >= count) return;
-    const size_t len = count - e_lo < C ? count - e_lo : C;   // elements of chunk c
+    const size_t len = count - e_lo < p_len ? count - e_lo : p_len;   // elements of chunk c's piece
     const size_t nv = len / VE;                                 // whole vectors
     const T* const xr = static_cast<const T*>(in.p[r]) + e_lo;
     const T* const xd = static_cast<const T*>(in.p[d]) + e_lo;
@@ -183,7 +191,7 @@ ring_rs_step_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant_
 // Grid: blockIdx.y gives the sending rank r (see ring_tile).
 template <int NR, int DT, bool RO>
 __global__ void __launch_bounds__(kThreads, 2)
-ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t count, int s)
+ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t count, int s, size_t p_len)
 {
     pdl_acquire();
     constexpr int VE = kVecElems<DT>;
@@ -196,7 +204,7 @@ ring_ag_step_kernel(const __grid_constant__ MPtrs<NR> out, size_t C, size_t coun
     const int c = (r + 1 - s + NR) % NR;
     const size_t e_lo = (size_t)c * C;
     if (e_lo >= count) return;
-    const size_t len = count - e_lo < C ? count - e_lo : C;
+    const size_t len = count - e_lo < p_len ? count - e_lo : p_len;
     const size_t nv = len / VE;
     const T* const src = static_cast<const T*>(out.p[r]) + e_lo;
     T* const dst = static_cast<T*>(out.p[d]) + e_lo;
@@ -239,42 +247,85 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             }
             const size_t C = chunk_elems(NR, count, DT);
             if (C > h.ring_chunk_max) return AR_ERR_TOO_LARGE;
-            const size_t cvec = C / kVecElems<DT>;
+            const uint64_t e = sizeof(typename Payload<DT>::scalar_t);
+            const uint64_t pe = HR ? e : 4;   // bytes of one partial
+            // pieces: a step's partials over half of L2, rounded (measured on GB300, n = 8 bf16 and
+            // n = 16: at 64 MiB per rank 2 pieces ran the ring 372 against 388 us at n = 8 and 809
+            // against 853 us at n = 16; at 256 MiB and n = 16, 8 pieces 3313 against 3774 us and the
+            // hop-rounded ring in 4 pieces 2224 against 2685 us; below half of L2 every extra
+            // piece was slower, by about 1.4 us per added launch)
+            const uint64_t half_l2 = h.l2_bytes / 2;
+            uint64_t P = half_l2 ? ((uint64_t)count * pe + half_l2 / 2) / half_l2 : 1;
+            if (P < 1) P = 1;
+            size_t PL = (C + P - 1) / P;
+            PL = (PL + 255) / 256 * 256;   // whole vectors of every payload type
+            if (PL > C) PL = C;
+            const size_t cvec = (PL + kVecElems<DT> - 1) / kVecElems<DT>;
             const dim3 g_rs(grid_for_rows(h, (cvec + kRsUnroll - 1) / kRsUnroll, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
             float* buf[2] = {h.ring_scratch, h.ring_scratch + (size_t)NR * C};
-            // a step's partials (fp32, or the payload when rounded per hop) larger than half of L2
-            const uint64_t step_bytes = (uint64_t)count * (HR ? sizeof(typename Payload<DT>::scalar_t) : 4u);
-            const bool reorder = h.l2_bytes > 0 && step_bytes > (uint64_t)h.l2_bytes / 2;
-            int n_launch = 0;
+            // a piece's step data (its partials) larger than half of L2: the reversed tile order
+            const uint64_t step_bytes = (uint64_t)PL * NR * pe;
+            const bool reorder = half_l2 > 0 && step_bytes > half_l2;
+            int n_launch = 0, pieces = 0;
             // per step every chunk moves once: N elements in all
-            const uint64_t N = count, e = sizeof(typename Payload<DT>::scalar_t);
-            // one timing record per phase: the n-1 steps run back to back
+            const uint64_t N = count;
             uint64_t rs_bytes = 0;
-            rec_begin(h, s);
-            for (int step = 0; step < NR - 1; ++step) {
-                const uint64_t pe = HR ? e : 4;   // bytes of one partial
+            for (int step = 0; step < NR - 1; ++step)
                 rs_bytes += (step == 0 ? e : pe) * N + e * N + (step == NR - 2 ? e : pe) * N;
-                if (reorder)
-                    launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, true>, g_rs, kThreads, 0, s, ip, op,
-                                  buf[(step + 1) & 1], buf[step & 1], C, count, step);
-                else
-                    launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, false>, g_rs, kThreads, 0, s, ip, op,
-                                  buf[(step + 1) & 1], buf[step & 1], C, count, step);
-                ++n_launch;
-                if (launch_status() != AR_OK) return AR_ERR_CUDA;
-            }
-            rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, NR - 1);
+            // one timing record per phase: every piece's reduce-scatter steps, then every piece's
+            // all-gather steps, back to back
             rec_begin(h, s);
-            for (int step = 0; step < NR - 1; ++step) {
-                if (reorder)
-                    launch_kernel(h, ring_ag_step_kernel<NR, DT, true>, g_ag, kThreads, 0, s, op, C, count, step);
-                else
-                    launch_kernel(h, ring_ag_step_kernel<NR, DT, false>, g_ag, kThreads, 0, s, op, C, count, step);
-                ++n_launch;
-                if (launch_status() != AR_OK) return AR_ERR_CUDA;
+            // a piece is passed as every pointer moved to its first element and the count moved
+            // with it, so the kernels' chunk arithmetic is the unpieced one (in-kernel piece offsets
+            // cost the reduce-scatter step 19 registers and with them a CTA per SM)
+            using T = typename Payload<DT>::scalar_t;
+            auto shifted = [&](size_t p_lo, CPtrs<NR>& ipp, MPtrs<NR>& opp, float** bp) {
+                for (int q = 0; q < NR; ++q) {
+                    ipp.p[q] = static_cast<const T*>(ip.p[q]) + p_lo;
+                    opp.p[q] = static_cast<T*>(op.p[q]) + p_lo;
+                }
+                for (int k = 0; k < 2; ++k)
+                    bp[k] = HR ? reinterpret_cast<float*>(reinterpret_cast<T*>(buf[k]) + p_lo) : buf[k] + p_lo;
+            };
+            for (size_t p_lo = 0; p_lo < C; p_lo += PL) {
+                const size_t p_len = C - p_lo < PL ? C - p_lo : PL;
+                ++pieces;
+                CPtrs<NR> ipp;
+                MPtrs<NR> opp;
+                float* bp[2];
+                shifted(p_lo, ipp, opp, bp);
+                for (int step = 0; step < NR - 1; ++step) {
+                    if (reorder)
+                        launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, true>, g_rs, kThreads, 0, s, ipp, opp,
+                                      bp[(step + 1) & 1], bp[step & 1], C, count - p_lo, step, p_len);
+                    else
+                        launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, false>, g_rs, kThreads, 0, s, ipp, opp,
+                                      bp[(step + 1) & 1], bp[step & 1], C, count - p_lo, step, p_len);
+                    ++n_launch;
+                    if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                }
             }
-            rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N * (NR - 1), NR - 1);
+            rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, pieces * (NR - 1));
+            rec_begin(h, s);
+            for (size_t p_lo = 0; p_lo < C; p_lo += PL) {
+                const size_t p_len = C - p_lo < PL ? C - p_lo : PL;
+                CPtrs<NR> ipp;
+                MPtrs<NR> opp;
+                float* bp[2];
+                shifted(p_lo, ipp, opp, bp);
+                for (int step = 0; step < NR - 1; ++step) {
+                    if (reorder)
+                        launch_kernel(h, ring_ag_step_kernel<NR, DT, true>, g_ag, kThreads, 0, s, opp, C, count - p_lo,
+                                      step, p_len);
+                    else
+                        launch_kernel(h, ring_ag_step_kernel<NR, DT, false>, g_ag, kThreads, 0, s, opp, C, count - p_lo,
+                                      step, p_len);
+                    ++n_launch;
+                    if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                }
+            }
+            rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N * (NR - 1), pieces * (NR - 1));
             *launches = n_launch;
             return AR_OK;
         });

@@ -108,7 +108,8 @@ typedef enum {
  *     LL/LL128 calls (whose reduce counts as 1 step).
  *   hbm_read_bytes / hbm_write_bytes: the bytes the call must move in this
  *     GPU's HBM (algorithmic, not measured).
- *   launches: kernels the call launched (ar_plan: with the default options). */
+ *   launches: kernels the call launched (ar_plan: with the default options,
+ *     and for ar_ring / ar_ring_rounded one piece, 2(n-1); see ar_ring). */
 typedef struct {
     int op;                  /* ar_op */
     int n_ranks;             /* 1 for the per-buffer LL/LL128 pack/unpack */
@@ -263,7 +264,13 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
  * sends; partials stay fp32 in the handle's scratch and the rank completing
  * a chunk rounds it into its output.  All-gather step s: rank r+1 copies
  * chunk r+1-s (mod n) from rank r.  One launch per step, 2(n-1) launches.
- * Chunk c is summed in the order c, c+1, ..., c+n-1. */
+ * Chunk c is summed in the order c, c+1, ..., c+n-1.  When a step's partials
+ * (4 count bytes) exceed half of the device's L2, every chunk is cut into P
+ * pieces (P = those bytes over half of L2, rounded) and the ring runs piece by
+ * piece -- every piece's reduce-scatter steps, then every piece's all-gather
+ * steps -- so one piece's partials stay in L2 between steps (handbook "集合通
+ * 信：NCCL 的算法、协议…", §算法: a large message cut into blocks and
+ * pipelined): 2(n-1) P launches, the same sums and HBM bytes. */
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
             ar_dtype dt, ar_stream_t stream);
 
@@ -293,7 +300,8 @@ int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, siz
  *   RN( ... RN( RN(x_c + x_{c+1}) + x_{c+2} ) ... + x_{c+n-1} ).
  * Equal to ar_ring for fp32; for bf16 / fp16 it may differ from it by the
  * hops' roundings.  HBM: reads 2 e N and writes e N per reduce-scatter step,
- * reads and writes e N per all-gather step. */
+ * reads and writes e N per all-gather step.  Runs in pieces as ar_ring does,
+ * its step data being e count bytes. */
 int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                     ar_stream_t stream);
 

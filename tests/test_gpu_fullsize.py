@@ -32,6 +32,18 @@ def _cols(ts, idx, dtype):
     return [t[ti].cpu().numpy().view(np_t) for t in ts]
 
 
+def _ring_pieces(n, N, dtype, rounded):
+    """Pieces of a ring call: a step's partials (fp32, or the payload when rounded per hop) over
+    half of this device's L2, rounded; each chunk cut into that many pieces of whole 256-element
+    blocks."""
+    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    pe = {"f32": 4, "bf16": 2, "f16": 2}[dtype] if rounded else 4
+    P = max(1, (N * pe + half // 2) // half)
+    C = oracle.chunk_elems(n, N, dtype)
+    PL = min(C, -(-(-(-C // P)) // 256) * 256)
+    return -(-C // PL)
+
+
 def _run(call, h, ins, outs, N, dtype):
     rc = call(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], N, dtype)
     assert rc == ar.AR_OK, ar.ar_strerror(rc)
@@ -208,9 +220,10 @@ def test_prefill_64mib_whole_buffers_against_the_oracle():
 ])
 def test_ring_steps_in_the_l2_order_whole_buffers(dtype, n, N, call, ref):
     # sizes whose step data (fp32 partials, or the payload when rounded per hop) exceeds half of
-    # L2, so the steps take their tiles in the reversed, rotated order and keep their partials in
-    # L2 with write-back stores and streaming last-use loads: every element of every rank against
-    # the oracle, with ragged chunk ends
+    # L2, so the steps take their tiles in the reversed, rotated order, keep their partials in
+    # L2 with write-back stores and streaming last-use loads, and (f16 here) run in pieces:
+    # every element of every rank against the oracle, with ragged chunk ends, and the launches
+    # the documented piece rule gives
     ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + n)
     np_t = np.float32 if dtype == "f32" else np.uint16
     xs = [t.cpu().numpy().view(np_t) for t in ins]
@@ -223,6 +236,7 @@ def test_ring_steps_in_the_l2_order_whole_buffers(dtype, n, N, call, ref):
                 o.fill_(0x5A5A if dtype != "f32" else 7.0)
             _run(getattr(ar, call), h, ins, outs, N, dtype)
             assert ar.ar_status(h) == ar.AR_OK
+            assert ar.ar_traffic(h).launches == 2 * (n - 1) * _ring_pieces(n, N, dtype, call == "ar_ring_rounded")
             for r in range(n):
                 got = outs[r].cpu().numpy().view(np_t)
                 bad = np.flatnonzero(got.view(np.uint32 if dtype == "f32" else np.uint16)
