@@ -11,7 +11,11 @@
 // Emulation: one launch per level.  Level 0 reads in[r], in[r ^ 1] and writes
 // out[r], out[r ^ 1]; later levels work in place on out[].  Every element of
 // every rank is read once and written once per level: HBM per level n S read,
-// n S write.
+// n S write.  A call whose level output (n S) is larger than half of L2 runs
+// in pieces, each through all levels (handbook "集合通信：NCCL 的算法、协议与
+// 推理框架的定制 all-reduce", §算法: a tree cuts a large message into blocks
+// and pipelines them): P = n S over half of L2, rounded, so one piece's level
+// output stays in L2 for the next level.  Same sums, same HBM bytes.
 #include "common.cuh"
 
 namespace argb {
@@ -70,25 +74,42 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
         constexpr int DT = decltype(dtc)::value;
         return dispatch_ranks(h.n, [&](auto nrc) -> int {
             constexpr int NR = decltype(nrc)::value;
-            CPtrs<NR> ip, op_c;
-            MPtrs<NR> op;
-            for (int q = 0; q < NR; ++q) {
-                ip.p[q] = in[q];
-                op_c.p[q] = out[q];
-                op.p[q] = out[q];
-            }
-            const size_t nvec = count / kVecElems<DT>;
-            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
-            const dim3 grid(grid_for_rows(h, nvec, NR / 2), NR / 2);
-            int levels = 0;
+            using T = typename Payload<DT>::scalar_t;
+            const uint64_t S = (uint64_t)count * sizeof(T);
+            // pieces: a level's output (n S) over half of L2, rounded.  Measured on GB300 (bf16,
+            // back to back; pieces -> us): n = 8 at 64 MiB per rank 1 -> 472, 4 -> 444, 6 -> 381,
+            // 8 -> 364, 12 -> 370, 16 -> 384; at 16 MiB 1 -> 112, 2 -> 89, 4 -> 96; at 8 MiB and
+            // below one piece was fastest; n = 16 at 16 MiB 1 -> 317, 4 -> 226, 8 -> 244, and at
+            // 64 MiB 1 -> 1258, 16 -> 959, 24 -> 939; n = 4 at 64 MiB 1 -> 159, 4 -> 131.  A piece
+            // is passed as every pointer moved to its first element.
+            const uint64_t half_l2 = h.l2_bytes / 2;
+            uint64_t P = half_l2 ? ((uint64_t)NR * S + half_l2 / 2) / half_l2 : 1;
+            if (P < 1) P = 1;
+            size_t PL = (count + P - 1) / P;
+            PL = (PL + 255) / 256 * 256;   // whole vectors of every payload type
+            if (PL > count) PL = count;
+            const size_t pvec = PL / kVecElems<DT>;
+            const dim3 grid(grid_for_rows(h, pvec ? pvec : 1, NR / 2), NR / 2);
+            int levels = 0, n_launch = 0;
             rec_begin(h, s);
-            for (int d = 1; d < NR; d <<= 1, ++levels) {
-                if (launch_kernel(h, tree_level_kernel<NR, DT>, grid, kThreads, 0, s, d == 1 ? ip : op_c, op, d, nvec,
-                                  count) != cudaSuccess)
-                    return AR_ERR_CUDA;
+            for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+                const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
+                CPtrs<NR> ipp, opc;
+                MPtrs<NR> opp;
+                for (int q = 0; q < NR; ++q) {
+                    ipp.p[q] = static_cast<const T*>(in[q]) + p_lo;
+                    opc.p[q] = static_cast<const T*>(out[q]) + p_lo;
+                    opp.p[q] = static_cast<T*>(out[q]) + p_lo;
+                }
+                levels = 0;
+                for (int d = 1; d < NR; d <<= 1, ++levels, ++n_launch) {
+                    if (launch_kernel(h, tree_level_kernel<NR, DT>, grid, kThreads, 0, s, d == 1 ? ipp : opc, opp, d,
+                                      pc / kVecElems<DT>, pc) != cudaSuccess)
+                        return AR_ERR_CUDA;
+                }
             }
-            rec_end(h, s, AR_K_TREE_LEVEL, 2ull * NR * S * (uint64_t)levels, levels);
-            *launches = levels;
+            rec_end(h, s, AR_K_TREE_LEVEL, 2ull * NR * S * (uint64_t)levels, n_launch);
+            *launches = n_launch;
             return launch_status();
         });
     });

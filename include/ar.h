@@ -109,7 +109,7 @@ typedef enum {
  *   hbm_read_bytes / hbm_write_bytes: the bytes the call must move in this
  *     GPU's HBM (algorithmic, not measured).
  *   launches: kernels the call launched (ar_plan: with the default options,
- *     and for ar_ring / ar_ring_rounded one piece, 2(n-1); see ar_ring). */
+ *     and for ar_ring / ar_ring_rounded / ar_tree one piece; see ar_ring). */
 typedef struct {
     int op;                  /* ar_op */
     int n_ranks;             /* 1 for the per-buffer LL/LL128 pack/unpack */
@@ -312,7 +312,12 @@ int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t
  * handle's n_ranks must be a power of two (2, 4, 8 or 16), else
  * AR_ERR_INVALID.  Every rank ends with the same bits; for bf16 / fp16 they
  * may differ from one-shot's by the levels' roundings, for fp32 by the order
- * of the adds.  log2(n) launches; HBM per level: n S read, n S written. */
+ * of the adds.  log2(n) launches; HBM per level: n S read, n S written.
+ * When a level's output (n S) exceeds half of the device's L2 the buffer is
+ * cut into P pieces (P = n S over half of L2, rounded), each taken through
+ * all levels in turn, so one piece's level output stays in L2 for the next
+ * level (handbook "集合通信：NCCL 的算法、协议…", §算法: the tree cuts a large
+ * message into blocks and pipelines them): log2(n) P launches, same bits. */
 int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t stream);
 
 /* The pairwise tree of ar_tree with all log2(n) levels done in registers in
