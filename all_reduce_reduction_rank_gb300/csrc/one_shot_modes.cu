@@ -21,6 +21,11 @@
 // Both give the one-shot result bit for bit: fp32 sums in rank order from +0,
 // one rounding.
 //
+// Pieces: when the staged bytes (push: n (n-1) S; copy-in: n S) exceed half
+// of L2, the buffers are cut into pieces that each go through both launches
+// in turn, so the second launch reads the staging back from L2 (same bits,
+// same HBM bytes, twice the launches per piece).
+//
 // Small: a call too small to give every SM a full CTA runs its kernels in
 // narrower CTAs compiled for three CTAs per SM, as the one-shot kernel's small
 // form (blockIdx.y = rank rows; one 16-byte vector per thread).
@@ -127,31 +132,52 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
                 ip.p[q] = in[q];
                 op.p[q] = out[q];
             }
-            const size_t nvec = count / kVecElems<DT>;
-            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
-            const dim3 grid(grid_for_rows(h, nvec, NR), NR);
+            using T = typename Payload<DT>::scalar_t;
+            // pieces: the staged bytes, n (n - 1) S, over half of L2, rounded; each piece staged
+            // and reduced in turn, so its staging is read back from L2.  Measured on GB300 (n = 8
+            // bf16, back to back; pieces -> us): at 8 MiB per rank 1 -> 162.6, 4 -> 148.5,
+            // 7 -> 143.4, 8 -> 142.4, 12 -> 156.0; at 64 MiB 1 -> 1357, 32 -> 1210, 57 -> 1150,
+            // 64 -> 1152; at 2 MiB 1 -> 36.3, 2 -> 34.8; at 1 MiB one piece is fastest.
+            const size_t PL = piece_elems(h, (uint64_t)NR * (NR - 1) * count * sizeof(T), count);
+            const size_t pv = PL / kVecElems<DT>;
+            const dim3 grid(grid_for_rows(h, pv ? pv : 1, NR), NR);
             const bool small = grid.x * NR < (unsigned)h.sm_count;   // narrower CTAs, as one-shot's small form
-            const Shape sh = narrow_shape(h, nvec, NR);
+            const Shape sh = narrow_shape(h, pv ? pv : 1, NR);
             const dim3 g_small(sh.grid_x, NR);
-            rec_begin(h, s);
-            if (small)
-                launch_kernel(h, push_kernel<NR, DT, true>, g_small, sh.block, 0, s, ip, h.push_stage, h.stage_slot,
-                              nvec, count);
-            else
-                launch_kernel(h, push_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, h.push_stage, h.stage_slot,
-                              nvec, count);
-            rec_end(h, s, AR_K_PUSH, (uint64_t)NR * S + (uint64_t)NR * (NR - 1) * S);
-            if (launch_status() != AR_OK) return AR_ERR_CUDA;
-            rec_begin(h, s);
-            if (small)
-                launch_kernel(h, push_reduce_kernel<NR, DT, true>, g_small, sh.block, 0, s, ip, op,
-                              (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
-            else
-                launch_kernel(h, push_reduce_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, op,
-                              (const uint8_t*)h.push_stage, h.stage_slot, nvec, count);
-            rec_end(h, s, AR_K_PUSH_REDUCE, (uint64_t)NR * NR * S + (uint64_t)NR * S);
-            *launches = 2;
-            return launch_status();
+            int nl = 0;
+            for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+                const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
+                const uint64_t S = (uint64_t)pc * sizeof(T);
+                // the piece: every pointer moved to its first element (within each staging slot too)
+                CPtrs<NR> ipp;
+                MPtrs<NR> opp;
+                for (int q = 0; q < NR; ++q) {
+                    ipp.p[q] = static_cast<const T*>(in[q]) + p_lo;
+                    opp.p[q] = static_cast<T*>(out[q]) + p_lo;
+                }
+                uint8_t* const st = h.push_stage + p_lo * sizeof(T);
+                rec_begin(h, s);
+                if (small)
+                    launch_kernel(h, push_kernel<NR, DT, true>, g_small, sh.block, 0, s, ipp, st, h.stage_slot,
+                                  pc / kVecElems<DT>, pc);
+                else
+                    launch_kernel(h, push_kernel<NR, DT, false>, grid, kThreads, 0, s, ipp, st, h.stage_slot,
+                                  pc / kVecElems<DT>, pc);
+                rec_end(h, s, AR_K_PUSH, (uint64_t)NR * S + (uint64_t)NR * (NR - 1) * S);
+                if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                rec_begin(h, s);
+                if (small)
+                    launch_kernel(h, push_reduce_kernel<NR, DT, true>, g_small, sh.block, 0, s, ipp, opp,
+                                  (const uint8_t*)st, h.stage_slot, pc / kVecElems<DT>, pc);
+                else
+                    launch_kernel(h, push_reduce_kernel<NR, DT, false>, grid, kThreads, 0, s, ipp, opp,
+                                  (const uint8_t*)st, h.stage_slot, pc / kVecElems<DT>, pc);
+                rec_end(h, s, AR_K_PUSH_REDUCE, (uint64_t)NR * NR * S + (uint64_t)NR * S);
+                if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                nl += 2;
+            }
+            *launches = nl;
+            return AR_OK;
         });
     });
 }
@@ -159,34 +185,53 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
 int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                            cudaStream_t s, int* launches)
 {
-    const int rc = dispatch_dtype(dt, [&](auto dtc) -> int {
-        constexpr int DT = decltype(dtc)::value;
-        return dispatch_ranks(h.n, [&](auto nrc) -> int {
-            constexpr int NR = decltype(nrc)::value;
-            CPtrs<NR> ip;
-            for (int q = 0; q < NR; ++q) ip.p[q] = in[q];
-            const size_t nvec = count / kVecElems<DT>;
-            const uint64_t S = (uint64_t)count * sizeof(typename Payload<DT>::scalar_t);
-            const dim3 grid(grid_for_rows(h, nvec, NR), NR);
-            const Shape sh = narrow_shape(h, nvec, NR);
-            rec_begin(h, s);
-            if (grid.x * NR < (unsigned)h.sm_count)   // narrower CTAs, as one-shot's small form
-                launch_kernel(h, copyin_kernel<NR, DT, true>, dim3(sh.grid_x, NR), sh.block, 0, s, ip, h.registered,
-                              h.stage_slot, nvec, count);
-            else
-                launch_kernel(h, copyin_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, h.registered, h.stage_slot,
-                              nvec, count);
-            rec_end(h, s, AR_K_COPYIN, 2ull * NR * S);
-            return launch_status();
+    // pieces: the registered copy, n S, over half of L2, rounded; each piece copied and then
+    // reduced by the one-shot kernel, so the one-shot reads the copy back from L2.  Measured on
+    // GB300 (n = 8 bf16, back to back; pieces -> us): at 64 MiB per rank 1 -> 308.4, 4 -> 286.0,
+    // 8 -> 277.1, 12 -> 286.7; at 16 MiB 1 -> 71.8, 2 -> 68.2, 4 -> 76.4; at 8 MiB one piece is
+    // fastest.
+    const size_t e = elem_bytes(dt);
+    const size_t PL = piece_elems(h, (uint64_t)h.n * count * e, count);
+    int total = 0;
+    for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+        const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
+        const int rc = dispatch_dtype(dt, [&](auto dtc) -> int {
+            constexpr int DT = decltype(dtc)::value;
+            return dispatch_ranks(h.n, [&](auto nrc) -> int {
+                constexpr int NR = decltype(nrc)::value;
+                using T = typename Payload<DT>::scalar_t;
+                CPtrs<NR> ip;
+                for (int q = 0; q < NR; ++q) ip.p[q] = static_cast<const T*>(in[q]) + p_lo;
+                const size_t nvec = pc / kVecElems<DT>;
+                const uint64_t S = (uint64_t)pc * sizeof(T);
+                const dim3 grid(grid_for_rows(h, nvec ? nvec : 1, NR), NR);
+                const Shape sh = narrow_shape(h, nvec ? nvec : 1, NR);
+                uint8_t* const reg = h.registered + p_lo * sizeof(T);
+                rec_begin(h, s);
+                if (grid.x * NR < (unsigned)h.sm_count)   // narrower CTAs, as one-shot's small form
+                    launch_kernel(h, copyin_kernel<NR, DT, true>, dim3(sh.grid_x, NR), sh.block, 0, s, ip, reg,
+                                  h.stage_slot, nvec, pc);
+                else
+                    launch_kernel(h, copyin_kernel<NR, DT, false>, grid, kThreads, 0, s, ip, reg, h.stage_slot,
+                                  nvec, pc);
+                rec_end(h, s, AR_K_COPYIN, 2ull * NR * S);
+                return launch_status();
+            });
         });
-    });
-    if (rc != AR_OK) return rc;
-    const void* reg[kMaxRanks];
-    for (int r = 0; r < h.n; ++r) reg[r] = h.registered + (size_t)r * h.stage_slot;
-    int one = 0;
-    const int rc2 = launch_one_shot(h, reg, out, count, dt, s, &one);
-    *launches = 1 + one;
-    return rc2;
+        if (rc != AR_OK) return rc;
+        const void* reg[kMaxRanks];
+        void* op[kMaxRanks];
+        for (int r = 0; r < h.n; ++r) {
+            reg[r] = h.registered + (size_t)r * h.stage_slot + p_lo * e;
+            op[r] = static_cast<uint8_t*>(out[r]) + p_lo * e;
+        }
+        int one = 0;
+        const int rc2 = launch_one_shot(h, reg, op, pc, dt, s, &one);
+        if (rc2 != AR_OK) return rc2;
+        total += 1 + one;
+    }
+    *launches = total;
+    return AR_OK;
 }
 
 }  // namespace argb

@@ -255,11 +255,7 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             // hop-rounded ring in 4 pieces 2224 against 2685 us; below half of L2 every extra
             // piece was slower, by about 1.4 us per added launch)
             const uint64_t half_l2 = h.l2_bytes / 2;
-            uint64_t P = half_l2 ? ((uint64_t)count * pe + half_l2 / 2) / half_l2 : 1;
-            if (P < 1) P = 1;
-            size_t PL = (C + P - 1) / P;
-            PL = (PL + 255) / 256 * 256;   // whole vectors of every payload type
-            if (PL > C) PL = C;
+            const size_t PL = piece_elems(h, (uint64_t)count * pe, C);
             const size_t cvec = (PL + kVecElems<DT> - 1) / kVecElems<DT>;
             const dim3 g_rs(grid_for_rows(h, (cvec + kRsUnroll - 1) / kRsUnroll, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);

@@ -82,12 +82,7 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
             // below one piece was fastest; n = 16 at 16 MiB 1 -> 317, 4 -> 226, 8 -> 244, and at
             // 64 MiB 1 -> 1258, 16 -> 959, 24 -> 939; n = 4 at 64 MiB 1 -> 159, 4 -> 131.  A piece
             // is passed as every pointer moved to its first element.
-            const uint64_t half_l2 = h.l2_bytes / 2;
-            uint64_t P = half_l2 ? ((uint64_t)NR * S + half_l2 / 2) / half_l2 : 1;
-            if (P < 1) P = 1;
-            size_t PL = (count + P - 1) / P;
-            PL = (PL + 255) / 256 * 256;   // whole vectors of every payload type
-            if (PL > count) PL = count;
+            const size_t PL = piece_elems(h, (uint64_t)NR * S, count);
             const size_t pvec = PL / kVecElems<DT>;
             const dim3 grid(grid_for_rows(h, pvec ? pvec : 1, NR / 2), NR / 2);
             int levels = 0, n_launch = 0;

@@ -109,7 +109,8 @@ typedef enum {
  *   hbm_read_bytes / hbm_write_bytes: the bytes the call must move in this
  *     GPU's HBM (algorithmic, not measured).
  *   launches: kernels the call launched (ar_plan: with the default options,
- *     and for ar_ring / ar_ring_rounded / ar_tree one piece; see ar_ring). */
+ *     and for the calls that run in pieces -- ar_ring, ar_ring_rounded,
+ *     ar_tree, ar_one_shot_push, ar_one_shot_copyin -- one piece). */
 typedef struct {
     int op;                  /* ar_op */
     int n_ranks;             /* 1 for the per-buffer LL/LL128 pack/unpack */
@@ -279,7 +280,9 @@ int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
  * every peer, then every rank sums its own slots (its own input for its own
  * term) in rank order.  Needs AR_OPT_PUSH_STAGING (AR_ERR_INVALID
  * otherwise).  Same bits as ar_one_shot.  HBM: reads n S + n^2 S, writes
- * n (n-1) S + n S.  Two launches. */
+ * n (n-1) S + n S.  Two launches; when the staged bytes, n (n-1) S, exceed
+ * half of the device's L2, the buffers are cut into P pieces (those bytes over
+ * half of L2, rounded), each staged and reduced in turn: 2 P launches. */
 int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                      ar_stream_t stream);
 
@@ -289,7 +292,10 @@ int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_
  * input itself): one copy kernel fills the handle's n registered buffers
  * (the pages use one cudaMemcpyAsync per rank), then the one-shot kernel
  * reads those.  Needs AR_OPT_REGISTERED (AR_ERR_INVALID otherwise).  Same
- * bits as ar_one_shot.  Two launches.  HBM: reads 2 n S, writes 2 n S. */
+ * bits as ar_one_shot.  Two launches.  HBM: reads 2 n S, writes 2 n S.
+ * When n S exceeds half of the device's L2, the buffers are cut into P
+ * pieces (n S over half of L2, rounded), each copied and reduced in turn:
+ * 2 P launches. */
 int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
 

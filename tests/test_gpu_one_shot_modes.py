@@ -97,3 +97,32 @@ def test_copyin_timing_records_copy_and_one_shot():
     assert [r[0] for r in recs] == ["copyin", "one_shot"]
     t = ar.ar_plan(ar.AR_OP_ONE_SHOT_COPYIN, n, N, "bf16")
     assert recs[0][3] + recs[1][3] == t.hbm_read_bytes + t.hbm_write_bytes
+
+
+@pytest.mark.parametrize("mode,N", [("push", (1 << 20) + 5), ("copyin", (8 << 20) + 3)])
+def test_pieces_whole_buffers_launches_and_records(mode, N):
+    # staged bytes (push: n (n-1) S; copy-in: n S) over half of L2: the call runs in pieces, each
+    # staged and reduced in turn; every element of every rank against the oracle, the launches
+    # the piece rule gives, and per-launch timing records whose bytes add up to the plan's
+    n, dtype = 8, "bf16"
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=17 + N % 7)
+    want = oracle.all_reduce(xs, dtype)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
+    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    staged = n * (n - 1) * N * 2 if mode == "push" else n * N * 2
+    P = max(1, (staged + half // 2) // half)
+    PL = min(N, -(-(-(-N // P)) // 256) * 256)
+    pieces = -(-N // PL)
+    assert pieces > 1
+    opts = {"push_staging": 1} if mode == "push" else {"registered": 1}
+    with Handle(n, N * 2, timing=64, **opts) as h:
+        call = ar.ar_one_shot_push if mode == "push" else ar.ar_one_shot_copyin
+        assert call(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+        assert ar.ar_status(h) == ar.AR_OK
+        assert ar.ar_traffic(h).launches == 2 * pieces
+        recs = ar.ar_timing(h)
+        t = ar.ar_plan(ar.AR_OP_ONE_SHOT_PUSH if mode == "push" else ar.AR_OP_ONE_SHOT_COPYIN, n, N, dtype)
+        assert len(recs) == 2 * pieces
+        assert sum(r[3] for r in recs) == t.hbm_read_bytes + t.hbm_write_bytes
+    for r in range(n):
+        np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
