@@ -264,14 +264,6 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             const uint64_t step_bytes = (uint64_t)PL * NR * pe;
             const bool reorder = half_l2 > 0 && step_bytes > half_l2;
             int n_launch = 0, pieces = 0;
-            // per step every chunk moves once: N elements in all
-            const uint64_t N = count;
-            uint64_t rs_bytes = 0;
-            for (int step = 0; step < NR - 1; ++step)
-                rs_bytes += (step == 0 ? e : pe) * N + e * N + (step == NR - 2 ? e : pe) * N;
-            // one timing record per phase: every piece's reduce-scatter steps, then every piece's
-            // all-gather steps, back to back
-            rec_begin(h, s);
             // a piece is passed as every pointer moved to its first element and the count moved
             // with it, so the kernels' chunk arithmetic is the unpieced one (in-kernel piece offsets
             // cost the reduce-scatter step 19 registers and with them a CTA per SM)
@@ -284,13 +276,25 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
                 for (int k = 0; k < 2; ++k)
                     bp[k] = HR ? reinterpret_cast<float*>(reinterpret_cast<T*>(buf[k]) + p_lo) : buf[k] + p_lo;
             };
+            // piece by piece: its reduce-scatter steps, then its all-gather steps, whose first step
+            // finds the chunk the last reduce-scatter step completed still in L2; one timing record
+            // per piece and phase (the n-1 steps run back to back)
             for (size_t p_lo = 0; p_lo < C; p_lo += PL) {
                 const size_t p_len = C - p_lo < PL ? C - p_lo : PL;
                 ++pieces;
+                uint64_t pn = 0;   // the piece's elements over all n chunks
+                for (int c = 0; c < NR; ++c) {
+                    const size_t lo = (size_t)c * C + p_lo;
+                    if (lo < count) pn += count - lo < p_len ? count - lo : p_len;
+                }
+                uint64_t rs_bytes = 0;
+                for (int step = 0; step < NR - 1; ++step)
+                    rs_bytes += (step == 0 ? e : pe) * pn + e * pn + (step == NR - 2 ? e : pe) * pn;
                 CPtrs<NR> ipp;
                 MPtrs<NR> opp;
                 float* bp[2];
                 shifted(p_lo, ipp, opp, bp);
+                rec_begin(h, s);
                 for (int step = 0; step < NR - 1; ++step) {
                     if (reorder)
                         launch_kernel(h, ring_rs_step_kernel<NR, DT, HR, true>, g_rs, kThreads, 0, s, ipp, opp,
@@ -301,15 +305,8 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
                     ++n_launch;
                     if (launch_status() != AR_OK) return AR_ERR_CUDA;
                 }
-            }
-            rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, pieces * (NR - 1));
-            rec_begin(h, s);
-            for (size_t p_lo = 0; p_lo < C; p_lo += PL) {
-                const size_t p_len = C - p_lo < PL ? C - p_lo : PL;
-                CPtrs<NR> ipp;
-                MPtrs<NR> opp;
-                float* bp[2];
-                shifted(p_lo, ipp, opp, bp);
+                rec_end(h, s, HR ? AR_K_RING_RS_STEP_ROUNDED : AR_K_RING_RS_STEP, rs_bytes, NR - 1);
+                rec_begin(h, s);
                 for (int step = 0; step < NR - 1; ++step) {
                     if (reorder)
                         launch_kernel(h, ring_ag_step_kernel<NR, DT, true>, g_ag, kThreads, 0, s, opp, C, count - p_lo,
@@ -320,8 +317,8 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
                     ++n_launch;
                     if (launch_status() != AR_OK) return AR_ERR_CUDA;
                 }
+                rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * pn * (NR - 1), NR - 1);
             }
-            rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * N * (NR - 1), pieces * (NR - 1));
             *launches = n_launch;
             return AR_OK;
         });

@@ -268,8 +268,8 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
  * Chunk c is summed in the order c, c+1, ..., c+n-1.  When a step's partials
  * (4 count bytes) exceed half of the device's L2, every chunk is cut into P
  * pieces (P = those bytes over half of L2, rounded) and the ring runs piece by
- * piece -- every piece's reduce-scatter steps, then every piece's all-gather
- * steps -- so one piece's partials stay in L2 between steps (handbook "集合通
+ * piece -- a piece's reduce-scatter steps, then its all-gather steps, then
+ * the next piece -- so one piece's partials stay in L2 between steps (handbook "集合通
  * 信：NCCL 的算法、协议…", §算法: a large message cut into blocks and
  * pipelined): 2(n-1) P launches, the same sums and HBM bytes. */
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
