@@ -246,7 +246,7 @@ def test_ring_steps_in_the_l2_order_whole_buffers(dtype, n, N, call, ref):
         assert ar.ar_destroy(h) == ar.AR_OK
 
 
-@pytest.mark.parametrize("n,N,dtype", [(8, 8 << 20, "bf16"), (4, (10 << 20) + 3, "f32")])
+@pytest.mark.parametrize("n,N,dtype", [(8, 8 << 20, "bf16"), (4, (10 << 20) + 3, "f32"), (16, (8 << 20) + 5, "f16")])
 def test_tree_in_pieces_whole_buffers(n, N, dtype):
     # a level's output (n S) over half of L2: the tree runs piece by piece through its levels;
     # every element of every rank against the oracle's tree, and the launches the piece rule gives

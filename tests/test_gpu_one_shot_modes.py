@@ -99,12 +99,13 @@ def test_copyin_timing_records_copy_and_one_shot():
     assert recs[0][3] + recs[1][3] == t.hbm_read_bytes + t.hbm_write_bytes
 
 
-@pytest.mark.parametrize("mode,N", [("push", (1 << 20) + 5), ("copyin", (8 << 20) + 3)])
-def test_pieces_whole_buffers_launches_and_records(mode, N):
+@pytest.mark.parametrize("mode,n,N", [("push", 8, (1 << 20) + 5), ("push", 3, (12 << 20) + 7),
+                                      ("copyin", 8, (8 << 20) + 3), ("copyin", 16, (4 << 20) + 1)])
+def test_pieces_whole_buffers_launches_and_records(mode, n, N):
     # staged bytes (push: n (n-1) S; copy-in: n S) over half of L2: the call runs in pieces, each
     # staged and reduced in turn; every element of every rank against the oracle, the launches
     # the piece rule gives, and per-launch timing records whose bytes add up to the plan's
-    n, dtype = 8, "bf16"
+    dtype = "bf16"
     xs = workloads.rank_inputs(n, N, dtype, "normal", seed=17 + N % 7)
     want = oracle.all_reduce(xs, dtype)
     ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
