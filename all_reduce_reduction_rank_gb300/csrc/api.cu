@@ -142,7 +142,7 @@ void plan(int op, int n, size_t count, int dt, ar_traffic_t* t)
         // summed over ranks that is 2 (n-1) S for any chunking.
         t->link_bytes_per_rank = 2.0 * (double)(nn - 1) * (double)S / (double)nn;
         t->steps = 2;
-        t->launches = count ? (two_shot_one_launch(0, S) ? 1 : 2) : 0;  // the default form's launches
+        t->launches = count ? (two_shot_one_launch(0) ? 1 : 2) : 0;  // the default form's launches
         t->hbm_read_bytes = (nn + 1) * S;
         t->hbm_write_bytes = nn * S;
         break;

@@ -92,7 +92,7 @@ inline size_t chunk_elems(int n, size_t N, int dt)
 // ar_two_shot's form: AR_OPT_TWO_SHOT_IMPL 1 = two launches, 2 = one launch
 // (per-tile CTA barrier), 3 = one launch (per-tile flags between CTAs);
 // 0 (auto) = form 2, measured fastest at every size on GB300.
-inline bool two_shot_one_launch(int impl, uint64_t /*bytes_per_rank*/) { return impl != 1; }
+inline bool two_shot_one_launch(int impl) { return impl != 1; }
 
 // CTAs of `kernel` (kThreads threads, no dynamic shared memory) that fit on
 // one SM at once.  Callers cache it in a function-local static per kernel

@@ -370,7 +370,7 @@ int launch_two_shot(Handle& h, const void* const* in, void* const* out, size_t c
             // a call too small to give every SM a full CTA: narrower CTAs, one vector per thread
             const bool narrow = g_rs.x * NR < (unsigned)h.sm_count;
             const Shape sh = narrow_shape(h, cvec, NR);
-            const bool one_launch = two_shot_one_launch(h.two_shot_impl, S);
+            const bool one_launch = two_shot_one_launch(h.two_shot_impl);
             if (one_launch) {
                 // one tile per CTA: phase 1 of tile t, then phase 2 of tile t (form 2) or of
                 // the tile of ticket t - lag (form 3)
