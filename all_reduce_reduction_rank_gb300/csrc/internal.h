@@ -128,16 +128,21 @@ inline unsigned grid_for(const Handle& h, size_t work)
 // Piece length (elements) for a call of several launches that hands
 // `handed_bytes` from one launch to the next over a range of `len` elements:
 // the range is cut into P = handed_bytes over half of L2, rounded (at least
-// 1), equal pieces of whole 256-element blocks (whole 16-byte vectors of
-// every payload type), so that what one launch hands the next stays in L2;
-// each piece then goes through all of the call's launches in turn.  `len`
-// when the device's L2 size is unknown or one piece is enough.
+// 1, at most kMaxPieces), equal pieces of whole 256-element blocks (whole
+// 16-byte vectors of every payload type), so that what one launch hands the
+// next stays in L2; each piece then goes through all of the call's launches
+// in turn.  `len` when the device's L2 size is unknown or one piece is
+// enough.  The cap: every piece adds its launches' ramp and drain (about
+// 1.4 us each on GB300), and the largest count measured to help was 57 (push,
+// n = 8 bf16, 64 MiB per rank: 57 and 64 pieces took the same time).
+constexpr uint64_t kMaxPieces = 64;
 inline size_t piece_elems(const Handle& h, uint64_t handed_bytes, size_t len)
 {
     const uint64_t half = h.l2_bytes / 2;
     if (half == 0) return len;
     uint64_t P = (handed_bytes + half / 2) / half;
     if (P <= 1) return len;
+    if (P > kMaxPieces) P = kMaxPieces;
     size_t pl = (size_t)((len + P - 1) / P);
     pl = (pl + 255) / 256 * 256;
     return pl < len ? pl : len;

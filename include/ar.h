@@ -267,11 +267,12 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
  * chunk r+1-s (mod n) from rank r.  One launch per step, 2(n-1) launches.
  * Chunk c is summed in the order c, c+1, ..., c+n-1.  When a step's partials
  * (4 count bytes) exceed half of the device's L2, every chunk is cut into P
- * pieces (P = those bytes over half of L2, rounded) and the ring runs piece by
- * piece -- a piece's reduce-scatter steps, then its all-gather steps, then
- * the next piece -- so one piece's partials stay in L2 between steps (handbook "集合通
- * 信：NCCL 的算法、协议…", §算法: a large message cut into blocks and
- * pipelined): 2(n-1) P launches, the same sums and HBM bytes. */
+ * pieces (P = those bytes over half of L2, rounded, at most 64) and the ring
+ * runs piece by piece -- a piece's reduce-scatter steps, then its all-gather
+ * steps, then the next piece -- so one piece's partials stay in L2 between
+ * steps (handbook "集合通信：NCCL 的算法、协议…", §算法: a large message cut
+ * into blocks and pipelined): 2(n-1) P launches, the same sums and HBM
+ * bytes. */
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
             ar_dtype dt, ar_stream_t stream);
 
@@ -282,7 +283,8 @@ int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
  * otherwise).  Same bits as ar_one_shot.  HBM: reads n S + n^2 S, writes
  * n (n-1) S + n S.  Two launches; when the staged bytes, n (n-1) S, exceed
  * half of the device's L2, the buffers are cut into P pieces (those bytes over
- * half of L2, rounded), each staged and reduced in turn: 2 P launches. */
+ * half of L2, rounded, at most 64), each staged and reduced in turn: 2 P
+ * launches. */
 int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                      ar_stream_t stream);
 
@@ -294,8 +296,8 @@ int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_
  * reads those.  Needs AR_OPT_REGISTERED (AR_ERR_INVALID otherwise).  Same
  * bits as ar_one_shot.  Two launches.  HBM: reads 2 n S, writes 2 n S.
  * When n S exceeds half of the device's L2, the buffers are cut into P
- * pieces (n S over half of L2, rounded), each copied and reduced in turn:
- * 2 P launches. */
+ * pieces (n S over half of L2, rounded, at most 64), each copied and reduced
+ * in turn: 2 P launches. */
 int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
 
@@ -320,10 +322,11 @@ int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t
  * may differ from one-shot's by the levels' roundings, for fp32 by the order
  * of the adds.  log2(n) launches; HBM per level: n S read, n S written.
  * When a level's output (n S) exceeds half of the device's L2 the buffer is
- * cut into P pieces (P = n S over half of L2, rounded), each taken through
- * all levels in turn, so one piece's level output stays in L2 for the next
- * level (handbook "集合通信：NCCL 的算法、协议…", §算法: the tree cuts a large
- * message into blocks and pipelines them): log2(n) P launches, same bits. */
+ * cut into P pieces (P = n S over half of L2, rounded, at most 64), each
+ * taken through all levels in turn, so one piece's level output stays in L2
+ * for the next level (handbook "集合通信：NCCL 的算法、协议…", §算法: the tree
+ * cuts a large message into blocks and pipelines them): log2(n) P launches,
+ * same bits. */
 int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t stream);
 
 /* The pairwise tree of ar_tree with all log2(n) levels done in registers in

@@ -38,7 +38,7 @@ def _ring_pieces(n, N, dtype, rounded):
     blocks."""
     half = torch.cuda.get_device_properties(0).L2_cache_size // 2
     pe = {"f32": 4, "bf16": 2, "f16": 2}[dtype] if rounded else 4
-    P = max(1, (N * pe + half // 2) // half)
+    P = min(64, max(1, (N * pe + half // 2) // half))
     C = oracle.chunk_elems(n, N, dtype)
     PL = min(C, -(-(-(-C // P)) // 256) * 256)
     return -(-C // PL)
@@ -258,7 +258,7 @@ def test_tree_in_pieces_whole_buffers(n, N, dtype):
     want = oracle.tree(xs, dtype)[0].view(bits_t)
     outs = [torch.empty_like(t) for t in ins]
     half = torch.cuda.get_device_properties(0).L2_cache_size // 2
-    P = max(1, (n * N * e + half // 2) // half)
+    P = min(64, max(1, (n * N * e + half // 2) // half))
     PL = min(N, -(-(-(-N // P)) // 256) * 256)
     h = ar.ar_create(n, N * e)
     try:

@@ -111,7 +111,7 @@ def test_pieces_whole_buffers_launches_and_records(mode, n, N):
     ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
     half = torch.cuda.get_device_properties(0).L2_cache_size // 2
     staged = n * (n - 1) * N * 2 if mode == "push" else n * N * 2
-    P = max(1, (staged + half // 2) // half)
+    P = min(64, max(1, (staged + half // 2) // half))
     PL = min(N, -(-(-(-N // P)) // 256) * 256)
     pieces = -(-N // PL)
     assert pieces > 1
