@@ -465,11 +465,18 @@ int ar_create(int n_ranks, size_t max_bytes, ar_handle* out)
         rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaMemset(h.two_shot_sync, 0, h.two_shot_sync_words * sizeof(unsigned)) != cudaSuccess)
         rc = AR_ERR_CUDA;
+    if (rc == AR_OK && (cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking) != cudaSuccess ||
+                        cudaEventCreateWithFlags(&h.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+                        cudaEventCreateWithFlags(&h.ev_join, cudaEventDisableTiming) != cudaSuccess))
+        rc = AR_ERR_CUDA;
     if (rc == AR_OK && cudaDeviceSynchronize() != cudaSuccess) rc = AR_ERR_CUDA;
     if (rc != AR_OK) {
         if (h.ring_scratch) cudaFree(h.ring_scratch);
         if (h.status) cudaFree(h.status);
         if (h.two_shot_sync) cudaFree(h.two_shot_sync);
+        if (h.side) cudaStreamDestroy(h.side);
+        if (h.ev_fork) cudaEventDestroy(h.ev_fork);
+        if (h.ev_join) cudaEventDestroy(h.ev_join);
         cudaGetLastError();
         c->magic = 0;
         delete c;
@@ -491,6 +498,9 @@ int ar_destroy(ar_handle hd)
         if (h->push_stage && cudaFree(h->push_stage) != cudaSuccess) r = AR_ERR_CUDA;
         if (h->registered && cudaFree(h->registered) != cudaSuccess) r = AR_ERR_CUDA;
         if (h->persist && cudaFree(h->persist) != cudaSuccess) r = AR_ERR_CUDA;
+        if (cudaStreamDestroy(h->side) != cudaSuccess) r = AR_ERR_CUDA;
+        if (cudaEventDestroy(h->ev_fork) != cudaSuccess) r = AR_ERR_CUDA;
+        if (cudaEventDestroy(h->ev_join) != cudaSuccess) r = AR_ERR_CUDA;
         free_timing(h->timing);
         return r;
     });

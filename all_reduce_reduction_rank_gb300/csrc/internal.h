@@ -55,6 +55,10 @@ struct Handle {
     size_t two_shot_sync_words = 0;
     float* ring_scratch = nullptr;  // [2][n][ring_chunk_max] fp32 partials
     size_t ring_chunk_max = 0;      // elements
+    // a second stream for the ring's pieces, forked from and joined to the
+    // caller's stream by these events within each call
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     DevStatus* status = nullptr;    // device
     cudaStream_t last_stream = nullptr;
     ar_traffic_t last{};

@@ -891,6 +891,10 @@ def run_ours(args):
     total_bytes = reduce_scalar(bytes_step * args.steps, "sum")
     value = total_bytes / (ms_max * 1e-3) / 1e9
     kernels = per_kernel(records, sampled, peak)
+    # launches in the timed region: the sampled steps' from their records (a step that records runs
+    # the ring's pieces on one stream, fewer launches than the two-stream steps), the others' from
+    # the untimed counting step
+    gpu_launches = wl.launches_per_step * (args.steps - sampled) + sum(r[4] for r in records)
     dom = max(kernels, key=lambda k: kernels[k]["share"])
     dk = kernels[dom]
     traffic = ncu_traffic(dom, dk["bytes_per_launch"])
@@ -926,7 +930,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2: 1.3 GiB touched per step vs 129 MB L2; no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "frac_of_peak": round(value / world / peak, 4), "frac_of_8tbs": round(value / world / NOMINAL_PEAK_GBS, 4),
-        "roofline": roofline, "kernels": kernels, "gpu_launches": wl.launches_per_step * args.steps,
+        "roofline": roofline, "kernels": kernels, "gpu_launches": gpu_launches,
         "launch_timing": {"steps_sampled": sampled, "every": every, "records": len(records),
                           "launches_recorded": sum(r[4] for r in records)},
         "host_issue_ms_per_step": round(host_ms / args.steps, 4),

@@ -217,7 +217,9 @@ typedef struct {
  * (max_bytes >= 16), on the calling thread's current CUDA device.  It
  * allocates, once, the ring's fp32 partial-sum scratch (2 x n_ranks x chunk
  * x 4 B, about 4 x max_bytes), the one-launch two-shot's tile flags (about
- * max_bytes / 128 bytes) and a status word.  *out is set only on AR_OK.
+ * max_bytes / 128 bytes) and a status word, and creates a stream and two
+ * events for the ring's two-stream pieces (see ar_ring).  *out is set only
+ * on AR_OK.
  * The n-rank bound is the pages' kMaxNumGPU = 16 (custom all-reduce notes,
  * §调用). */
 int ar_create(int n_ranks, size_t max_bytes, ar_handle* out);
@@ -272,7 +274,12 @@ int ar_two_shot(ar_handle h, const void* const* in, void* const* out, size_t cou
  * steps, then the next piece -- so one piece's partials stay in L2 between
  * steps (handbook "集合通信：NCCL 的算法、协议…", §算法: a large message cut
  * into blocks and pipelined): 2(n-1) P launches, the same sums and HBM
- * bytes. */
+ * bytes.  When the partials reach a tenth of L2 the pieces run on two
+ * streams, twice as many of half the length: even pieces on `stream`, odd
+ * ones on a stream the handle owns, forked from `stream` by an event at the
+ * start of the call and joined back into it at the end (so the call stays
+ * stream-ordered and graph-capturable); a call made while AR_OPT_TIMING
+ * records runs on `stream` alone. */
 int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
             ar_dtype dt, ar_stream_t stream);
 

@@ -34,13 +34,17 @@ def _cols(ts, idx, dtype):
 
 def _ring_pieces(n, N, dtype, rounded):
     """Pieces of a ring call: a step's partials (fp32, or the payload when rounded per hop) over
-    half of this device's L2, rounded; each chunk cut into that many pieces of whole 256-element
-    blocks."""
-    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    half of this device's L2, rounded, at most 64; each chunk cut into that many pieces of whole
+    256-element blocks; twice as many (half the length) when the partials reach a tenth of L2
+    and the call runs on two streams."""
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    half = l2 // 2
     pe = {"f32": 4, "bf16": 2, "f16": 2}[dtype] if rounded else 4
     P = min(64, max(1, (N * pe + half // 2) // half))
     C = oracle.chunk_elems(n, N, dtype)
-    PL = min(C, -(-(-(-C // P)) // 256) * 256)
+    PL = C if P == 1 else min(C, -(-(-(-C // P)) // 256) * 256)
+    if N * pe * 10 >= l2:
+        PL = min(C, -(-(-(-PL // 2)) // 256) * 256)
     return -(-C // PL)
 
 
@@ -268,5 +272,71 @@ def test_tree_in_pieces_whole_buffers(n, N, dtype):
         for r in range(n):
             bad = np.flatnonzero(outs[r].cpu().numpy().view(bits_t) != want)
             assert bad.size == 0, (r, bad[:5])
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+
+
+def test_ring_on_two_streams_in_a_cuda_graph():
+    # a ring call whose partials reach a tenth of L2 forks its odd pieces onto the handle's
+    # stream and joins them back: captured into a CUDA graph and replayed on new inputs, every
+    # element of every rank against the oracle each time
+    n, dtype = 8, "bf16"
+    N = (torch.cuda.get_device_properties(0).L2_cache_size // 4) // 4 + 4096   # 4 N bytes > L2 / 4
+    assert _ring_pieces(n, N, dtype, False) >= 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + 300)
+    outs = [torch.empty_like(t) for t in ins]
+    h = ar.ar_create(n, N * 2)
+    try:
+        s = torch.cuda.Stream()
+        _run(ar.ar_ring, h, ins, outs, N, dtype)   # outside capture first
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rc = ar.ar_ring(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], N, dtype, s)
+        assert rc == ar.AR_OK
+        for k in range(2):
+            src = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + 301 + k)
+            for t, x in zip(ins, src):
+                t.copy_(x)
+            for o in outs:
+                o.fill_(0x5A5A)
+            g.replay()
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK
+            want = oracle.ring([t.cpu().numpy().view(np.uint16) for t in ins], dtype)[0]
+            for r in range(n):
+                bad = np.flatnonzero(outs[r].cpu().numpy().view(np.uint16) != want)
+                assert bad.size == 0, (k, r, bad[:5])
+    finally:
+        assert ar.ar_destroy(h) == ar.AR_OK
+
+
+def test_ring_takes_one_stream_while_timing_records():
+    # with AR_OPT_TIMING recording, the same call runs its pieces on the caller's stream alone
+    # (one-stream piece count), each record timing its own launches; the sums are unchanged
+    n, dtype = 8, "bf16"
+    N = 16 << 20   # 32 MiB per rank: 4 N bytes = 64 MiB, above a tenth of L2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + 400)
+    want = oracle.ring([t.cpu().numpy().view(np.uint16) for t in ins], dtype)[0]
+    outs = [torch.empty_like(t) for t in ins]
+    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    P = min(64, max(1, (N * 4 + half // 2) // half))
+    C = oracle.chunk_elems(n, N, dtype)
+    PL = C if P == 1 else min(C, -(-(-(-C // P)) // 256) * 256)
+    one_stream = -(-C // PL)
+    h = ar.ar_create(n, N * 2)
+    try:
+        _run(ar.ar_ring, h, ins, outs, N, dtype)
+        assert ar.ar_traffic(h).launches == 2 * (n - 1) * _ring_pieces(n, N, dtype, False)
+        assert ar.ar_set_option(h, ar.AR_OPT_TIMING, 256) == ar.AR_OK
+        for o in outs:
+            o.fill_(0x5A5A)
+        _run(ar.ar_ring, h, ins, outs, N, dtype)
+        assert ar.ar_status(h) == ar.AR_OK
+        assert ar.ar_traffic(h).launches == 2 * (n - 1) * one_stream
+        recs = ar.ar_timing(h)
+        assert sum(r[4] for r in recs) == 2 * (n - 1) * one_stream
+        for r in range(n):
+            assert not np.flatnonzero(outs[r].cpu().numpy().view(np.uint16) != want).size
     finally:
         assert ar.ar_destroy(h) == ar.AR_OK
