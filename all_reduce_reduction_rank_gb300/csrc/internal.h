@@ -152,6 +152,52 @@ inline size_t piece_elems(const Handle& h, uint64_t handed_bytes, size_t len)
     return pl < len ? pl : len;
 }
 
+// Independent pieces on two streams.  A call's pieces do not depend on each
+// other, so when it has many the call runs twice as many, half as long,
+// alternately on the caller's stream and on the handle's side stream (forked
+// from the caller's stream by an event at the start, joined back by another
+// at the end, so the call stays stream-ordered and capturable in a CUDA
+// graph): one stream's launches fill the other's ramp and drain, and two
+// half-length pieces in flight hold in L2 what one piece did.  A call made
+// while timing records are taken stays on one stream, so that each record
+// times its own launches.
+inline bool recording(const Handle& h) { return h.timing.capacity && !h.timing.paused; }
+
+inline bool two_streams(const Handle& h, uint64_t handed_bytes, uint64_t l2_fraction)
+{
+    return h.side && h.l2_bytes > 0 && handed_bytes * l2_fraction >= (uint64_t)h.l2_bytes && !recording(h);
+}
+
+// Half a piece length, in whole 256-element blocks, at most `len`.
+inline size_t half_piece(size_t pl, size_t len)
+{
+    pl = (pl + 1) / 2;
+    pl = (pl + 255) / 256 * 256;
+    return pl < len ? pl : len;
+}
+
+struct PieceStreams {
+    Handle& h;
+    cudaStream_t main;
+    bool on;
+    int k = 0;
+    int fork() const
+    {
+        return on && (cudaEventRecord(h.ev_fork, main) != cudaSuccess ||
+                      cudaStreamWaitEvent(h.side, h.ev_fork, 0) != cudaSuccess)
+                   ? AR_ERR_CUDA
+                   : AR_OK;
+    }
+    cudaStream_t next() { return on && (k++ & 1) ? h.side : main; }   // the next piece's stream
+    int join() const   // also after a failed launch, so a stream capture is never left forked
+    {
+        return on && (cudaEventRecord(h.ev_join, h.side) != cudaSuccess ||
+                      cudaStreamWaitEvent(main, h.ev_join, 0) != cudaSuccess)
+                   ? AR_ERR_CUDA
+                   : AR_OK;
+    }
+};
+
 // blockIdx.x extent for a 2-D grid of `rows` rows (blockIdx.y) that each need
 // `work` thread-iterations, within the same CTA budget.
 inline unsigned grid_for_rows(const Handle& h, size_t work, int rows)

@@ -137,17 +137,25 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
             // and reduced in turn, so its staging is read back from L2.  Measured on GB300 (n = 8
             // bf16, back to back; pieces -> us): at 8 MiB per rank 1 -> 162.6, 4 -> 148.5,
             // 7 -> 143.4, 8 -> 142.4, 12 -> 156.0; at 64 MiB 1 -> 1357, 32 -> 1210, 57 -> 1150,
-            // 64 -> 1152; at 2 MiB 1 -> 36.3, 2 -> 34.8; at 1 MiB one piece is fastest.
-            const size_t PL = piece_elems(h, (uint64_t)NR * (NR - 1) * count * sizeof(T), count);
+            // 64 -> 1152; at 2 MiB 1 -> 36.3, 2 -> 34.8; at 1 MiB one piece is fastest.  Two streams
+            // (PieceStreams, twice the pieces) when the staged bytes exceed half of L2: at 2 / 8 /
+            // 64 MiB 35.0 -> 33.6, 144 -> 125, 1168 -> 1012 us; at 1 MiB 16.0 -> 16.8 (one stream).
+            const uint64_t staged = (uint64_t)NR * (NR - 1) * count * sizeof(T);
+            const bool dual = two_streams(h, staged, 2);
+            size_t PL = piece_elems(h, staged, count);
+            if (dual) PL = half_piece(PL, count);
             const size_t pv = PL / kVecElems<DT>;
             const dim3 grid(grid_for_rows(h, pv ? pv : 1, NR), NR);
             const bool small = grid.x * NR < (unsigned)h.sm_count;   // narrower CTAs, as one-shot's small form
             const Shape sh = narrow_shape(h, pv ? pv : 1, NR);
             const dim3 g_small(sh.grid_x, NR);
-            int nl = 0;
-            for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+            int nl = 0, rc = AR_OK;
+            PieceStreams streams{h, s, dual};
+            if (streams.fork() != AR_OK) return AR_ERR_CUDA;
+            for (size_t p_lo = 0; p_lo < count && rc == AR_OK; p_lo += PL) {
                 const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
                 const uint64_t S = (uint64_t)pc * sizeof(T);
+                const cudaStream_t s = streams.next();   // this piece's stream
                 // the piece: every pointer moved to its first element (within each staging slot too)
                 CPtrs<NR> ipp;
                 MPtrs<NR> opp;
@@ -164,7 +172,10 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
                     launch_kernel(h, push_kernel<NR, DT, false>, grid, kThreads, 0, s, ipp, st, h.stage_slot,
                                   pc / kVecElems<DT>, pc);
                 rec_end(h, s, AR_K_PUSH, (uint64_t)NR * S + (uint64_t)NR * (NR - 1) * S);
-                if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                if (launch_status() != AR_OK) {
+                    rc = AR_ERR_CUDA;
+                    break;
+                }
                 rec_begin(h, s);
                 if (small)
                     launch_kernel(h, push_reduce_kernel<NR, DT, true>, g_small, sh.block, 0, s, ipp, opp,
@@ -173,11 +184,12 @@ int launch_one_shot_push(Handle& h, const void* const* in, void* const* out, siz
                     launch_kernel(h, push_reduce_kernel<NR, DT, false>, grid, kThreads, 0, s, ipp, opp,
                                   (const uint8_t*)st, h.stage_slot, pc / kVecElems<DT>, pc);
                 rec_end(h, s, AR_K_PUSH_REDUCE, (uint64_t)NR * NR * S + (uint64_t)NR * S);
-                if (launch_status() != AR_OK) return AR_ERR_CUDA;
+                if (launch_status() != AR_OK) rc = AR_ERR_CUDA;
                 nl += 2;
             }
+            if (streams.join() != AR_OK) rc = AR_ERR_CUDA;
             *launches = nl;
-            return AR_OK;
+            return rc;
         });
     });
 }
@@ -189,12 +201,18 @@ int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, s
     // reduced by the one-shot kernel, so the one-shot reads the copy back from L2.  Measured on
     // GB300 (n = 8 bf16, back to back; pieces -> us): at 64 MiB per rank 1 -> 308.4, 4 -> 286.0,
     // 8 -> 277.1, 12 -> 286.7; at 16 MiB 1 -> 71.8, 2 -> 68.2, 4 -> 76.4; at 8 MiB one piece is
-    // fastest.
+    // fastest.  Two streams (PieceStreams, twice the pieces) when n S exceeds half of L2: at
+    // 16 / 64 MiB 68.3 -> 67.0, 279 -> 260 us; equal at 8 MiB.
     const size_t e = elem_bytes(dt);
-    const size_t PL = piece_elems(h, (uint64_t)h.n * count * e, count);
-    int total = 0;
-    for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+    const bool dual = two_streams(h, (uint64_t)h.n * count * e, 2);
+    size_t PL = piece_elems(h, (uint64_t)h.n * count * e, count);
+    if (dual) PL = half_piece(PL, count);
+    PieceStreams streams{h, s, dual};
+    if (streams.fork() != AR_OK) return AR_ERR_CUDA;
+    int total = 0, rc_all = AR_OK;
+    for (size_t p_lo = 0; p_lo < count && rc_all == AR_OK; p_lo += PL) {
         const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
+        const cudaStream_t s = streams.next();   // this piece's stream
         const int rc = dispatch_dtype(dt, [&](auto dtc) -> int {
             constexpr int DT = decltype(dtc)::value;
             return dispatch_ranks(h.n, [&](auto nrc) -> int {
@@ -218,7 +236,10 @@ int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, s
                 return launch_status();
             });
         });
-        if (rc != AR_OK) return rc;
+        if (rc != AR_OK) {
+            rc_all = rc;
+            break;
+        }
         const void* reg[kMaxRanks];
         void* op[kMaxRanks];
         for (int r = 0; r < h.n; ++r) {
@@ -227,11 +248,12 @@ int launch_one_shot_copyin(Handle& h, const void* const* in, void* const* out, s
         }
         int one = 0;
         const int rc2 = launch_one_shot(h, reg, op, pc, dt, s, &one);
-        if (rc2 != AR_OK) return rc2;
+        if (rc2 != AR_OK) rc_all = rc2;
         total += 1 + one;
     }
+    if (streams.join() != AR_OK) rc_all = AR_ERR_CUDA;
     *launches = total;
-    return AR_OK;
+    return rc_all;
 }
 
 }  // namespace argb

@@ -255,27 +255,17 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             // hop-rounded ring in 4 pieces 2224 against 2685 us; below half of L2 every extra
             // piece was slower, by about 1.4 us per added launch)
             const uint64_t half_l2 = h.l2_bytes / 2;
-            // two streams: a call whose step data is at least a tenth of L2 runs its pieces on two
-            // streams (even pieces on the caller's, odd ones on the handle's side stream, forked and
-            // joined by events), twice as many pieces as on one, so that one stream's launches fill
-            // the other's ramp and drain while two pieces together hold what one did.  Measured on
-            // GB300 (back to back; one stream -> two): n = 8 bf16 at 16 / 32 / 64 MiB per rank 101.3
-            // -> 88.4, 171 -> 157, 343 -> 312.5 us; n = 16 at 64 / 256 MiB 760 -> 674, 3072 -> 2705;
-            // n = 4 at 64 MiB 147.6 -> 132.9; the hop-rounded ring 8-14% less (16 MiB: 77.4 -> 70.3,
-            // 16.8 MB of step data); equal at 16.8 MB of fp32 partials (n = 8, 8 MiB), slower at
-            // 8.4 MB and below (hop-rounded ring at 8 MiB: 45.9 -> 51.7; 1 MiB: 26.9 -> 49 us).  A
-            // call that takes timing records runs on one stream, so that each record times its own
-            // launches.
+            // two streams (PieceStreams in internal.h) when a step's partials reach a tenth of L2.
+            // Measured on GB300 (back to back; one stream -> two): n = 8 bf16 at 16 / 32 / 64 MiB per
+            // rank 100.1 -> 88.8, 171.4 -> 157.5, 345.6 -> 312.6 us; n = 16 at 64 / 256 MiB 759 -> 666,
+            // 3096 -> 2715; n = 4 at 64 MiB 147.6 -> 132.9; the hop-rounded ring 7-14% less (16 MiB:
+            // 77.4 -> 70.3, 16.8 MB of step data); 58.8 -> 56.9 at 16.8 MB of fp32 partials (n = 8,
+            // 8 MiB), slower at 8.4 MB and below (hop-rounded ring at 8 MiB: 45.9 -> 51.7; 1 MiB: 26.9
+            // -> 49 us).  Twice the one-stream pieces was best at every size measured.
             const uint64_t step_data = (uint64_t)count * pe;
-            const bool dual = h.side && h.l2_bytes > 0 && step_data * 10 >= (uint64_t)h.l2_bytes &&
-                              !(h.timing.capacity && !h.timing.paused);
+            const bool dual = two_streams(h, step_data, 10);
             size_t PL = piece_elems(h, step_data, C);
-            if (dual) {
-                // twice the one-stream pieces: half the length, whole 256-element blocks
-                PL = (PL + 1) / 2;
-                PL = (PL + 255) / 256 * 256;
-                if (PL > C) PL = C;
-            }
+            if (dual) PL = half_piece(PL, C);
             const size_t cvec = (PL + kVecElems<DT> - 1) / kVecElems<DT>;
             const dim3 g_rs(grid_for_rows(h, (cvec + kRsUnroll - 1) / kRsUnroll, NR), NR);
             const dim3 g_ag(grid_for_rows(h, (cvec + kAgUnroll - 1) / kAgUnroll, NR), NR);
@@ -284,10 +274,8 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             const uint64_t step_bytes = (uint64_t)PL * NR * pe;
             const bool reorder = half_l2 > 0 && step_bytes > half_l2;
             int n_launch = 0, pieces = 0;
-            const cudaStream_t s_main = s;
-            if (dual && (cudaEventRecord(h.ev_fork, s_main) != cudaSuccess ||
-                         cudaStreamWaitEvent(h.side, h.ev_fork, 0) != cudaSuccess))
-                return AR_ERR_CUDA;
+            PieceStreams streams{h, s, dual};
+            if (streams.fork() != AR_OK) return AR_ERR_CUDA;
             // a piece is passed as every pointer moved to its first element and the count moved
             // with it, so the kernels' chunk arithmetic is the unpieced one (in-kernel piece offsets
             // cost the reduce-scatter step 19 registers and with them a CTA per SM)
@@ -306,7 +294,7 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
             int rc = AR_OK;
             for (size_t p_lo = 0; p_lo < C && rc == AR_OK; p_lo += PL) {
                 const size_t p_len = C - p_lo < PL ? C - p_lo : PL;
-                const cudaStream_t s = dual && (pieces & 1) ? h.side : s_main;   // this piece's stream
+                const cudaStream_t s = streams.next();   // this piece's stream
                 ++pieces;
                 uint64_t pn = 0;   // the piece's elements over all n chunks
                 for (int c = 0; c < NR; ++c) {
@@ -345,10 +333,7 @@ int launch_ring_impl(Handle& h, const void* const* in, void* const* out, size_t 
                 }
                 rec_end(h, s, AR_K_RING_AG_STEP, 2 * e * pn * (NR - 1), NR - 1);
             }
-            // join even after a failed launch, so a stream capture is never left forked
-            if (dual && (cudaEventRecord(h.ev_join, h.side) != cudaSuccess ||
-                         cudaStreamWaitEvent(s_main, h.ev_join, 0) != cudaSuccess))
-                rc = AR_ERR_CUDA;
+            if (streams.join() != AR_OK) rc = AR_ERR_CUDA;
             *launches = n_launch;
             return rc;
         });

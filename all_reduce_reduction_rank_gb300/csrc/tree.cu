@@ -81,14 +81,23 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
             // 8 -> 364, 12 -> 370, 16 -> 384; at 16 MiB 1 -> 112, 2 -> 89, 4 -> 96; at 8 MiB and
             // below one piece was fastest; n = 16 at 16 MiB 1 -> 317, 4 -> 226, 8 -> 244, and at
             // 64 MiB 1 -> 1258, 16 -> 959, 24 -> 939; n = 4 at 64 MiB 1 -> 159, 4 -> 131.  A piece
-            // is passed as every pointer moved to its first element.
-            const size_t PL = piece_elems(h, (uint64_t)NR * S, count);
+            // is passed as every pointer moved to its first element.  Two streams (PieceStreams,
+            // twice the pieces) when the level output exceeds half of L2: n = 8 at 8 / 16 / 64 MiB
+            // 44.9 -> 43.5, 89.2 -> 82.5, 364 -> 324 us; n = 16 at 16 / 64 MiB 225 -> 200, 961 ->
+            // 848 us; equal at 4 MiB.
+            const bool dual = two_streams(h, (uint64_t)NR * S, 2);
+            size_t PL = piece_elems(h, (uint64_t)NR * S, count);
+            if (dual) PL = half_piece(PL, count);
+            PieceStreams streams{h, s, dual};
+            if (streams.fork() != AR_OK) return AR_ERR_CUDA;
+            int rc = AR_OK;
             const size_t pvec = PL / kVecElems<DT>;
             const dim3 grid(grid_for_rows(h, pvec ? pvec : 1, NR / 2), NR / 2);
             int levels = 0, n_launch = 0;
             rec_begin(h, s);
-            for (size_t p_lo = 0; p_lo < count; p_lo += PL) {
+            for (size_t p_lo = 0; p_lo < count && rc == AR_OK; p_lo += PL) {
                 const size_t pc = count - p_lo < PL ? count - p_lo : PL;   // the piece's elements
+                const cudaStream_t ps = streams.next();   // this piece's stream
                 CPtrs<NR> ipp, opc;
                 MPtrs<NR> opp;
                 for (int q = 0; q < NR; ++q) {
@@ -98,14 +107,15 @@ int launch_tree(Handle& h, const void* const* in, void* const* out, size_t count
                 }
                 levels = 0;
                 for (int d = 1; d < NR; d <<= 1, ++levels, ++n_launch) {
-                    if (launch_kernel(h, tree_level_kernel<NR, DT>, grid, kThreads, 0, s, d == 1 ? ipp : opc, opp, d,
+                    if (launch_kernel(h, tree_level_kernel<NR, DT>, grid, kThreads, 0, ps, d == 1 ? ipp : opc, opp, d,
                                       pc / kVecElems<DT>, pc) != cudaSuccess)
-                        return AR_ERR_CUDA;
+                        rc = AR_ERR_CUDA;
                 }
             }
+            if (streams.join() != AR_OK) rc = AR_ERR_CUDA;
             rec_end(h, s, AR_K_TREE_LEVEL, 2ull * NR * S * (uint64_t)levels, n_launch);
             *launches = n_launch;
-            return launch_status();
+            return rc != AR_OK ? rc : launch_status();
         });
     });
 }

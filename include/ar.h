@@ -291,7 +291,7 @@ int ar_ring(ar_handle h, const void* const* in, void* const* out, size_t count,
  * n (n-1) S + n S.  Two launches; when the staged bytes, n (n-1) S, exceed
  * half of the device's L2, the buffers are cut into P pieces (those bytes over
  * half of L2, rounded, at most 64), each staged and reduced in turn: 2 P
- * launches. */
+ * launches, the pieces on two streams as ar_ring's do (twice as many). */
 int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                      ar_stream_t stream);
 
@@ -304,7 +304,8 @@ int ar_one_shot_push(ar_handle h, const void* const* in, void* const* out, size_
  * bits as ar_one_shot.  Two launches.  HBM: reads 2 n S, writes 2 n S.
  * When n S exceeds half of the device's L2, the buffers are cut into P
  * pieces (n S over half of L2, rounded, at most 64), each copied and reduced
- * in turn: 2 P launches. */
+ * in turn: 2 P launches, the pieces on two streams as ar_ring's do (twice as
+ * many). */
 int ar_one_shot_copyin(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt,
                        ar_stream_t stream);
 
@@ -333,7 +334,8 @@ int ar_ring_rounded(ar_handle h, const void* const* in, void* const* out, size_t
  * taken through all levels in turn, so one piece's level output stays in L2
  * for the next level (handbook "集合通信：NCCL 的算法、协议…", §算法: the tree
  * cuts a large message into blocks and pipelines them): log2(n) P launches,
- * same bits. */
+ * same bits; those pieces run on two streams as ar_ring's do (twice as many,
+ * half the length). */
 int ar_tree(ar_handle h, const void* const* in, void* const* out, size_t count, ar_dtype dt, ar_stream_t stream);
 
 /* The pairwise tree of ar_tree with all log2(n) levels done in registers in

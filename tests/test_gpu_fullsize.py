@@ -252,8 +252,9 @@ def test_ring_steps_in_the_l2_order_whole_buffers(dtype, n, N, call, ref):
 
 @pytest.mark.parametrize("n,N,dtype", [(8, 8 << 20, "bf16"), (4, (10 << 20) + 3, "f32"), (16, (8 << 20) + 5, "f16")])
 def test_tree_in_pieces_whole_buffers(n, N, dtype):
-    # a level's output (n S) over half of L2: the tree runs piece by piece through its levels;
-    # every element of every rank against the oracle's tree, and the launches the piece rule gives
+    # a level's output (n S) over half of L2: the tree runs piece by piece through its levels, on
+    # two streams; every element of every rank against the oracle's tree, and the launches the
+    # piece rule gives
     e = 4 if dtype == "f32" else 2
     ins = workloads.rank_inputs_device(n, N, dtype, "normal", workloads.seed_of(5) + 100 + n)
     np_t = np.float32 if dtype == "f32" else np.uint16
@@ -261,9 +262,12 @@ def test_tree_in_pieces_whole_buffers(n, N, dtype):
     xs = [t.cpu().numpy().view(np_t) for t in ins]
     want = oracle.tree(xs, dtype)[0].view(bits_t)
     outs = [torch.empty_like(t) for t in ins]
-    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    half = l2 // 2
     P = min(64, max(1, (n * N * e + half // 2) // half))
-    PL = min(N, -(-(-(-N // P)) // 256) * 256)
+    PL = N if P == 1 else min(N, -(-(-(-N // P)) // 256) * 256)
+    if n * N * e * 2 >= l2:   # two streams: twice the pieces
+        PL = min(N, -(-(-(-PL // 2)) // 256) * 256)
     h = ar.ar_create(n, N * e)
     try:
         _run(ar.ar_tree, h, ins, outs, N, dtype)

@@ -127,3 +127,34 @@ def test_pieces_whole_buffers_launches_and_records(mode, n, N):
         assert sum(r[3] for r in recs) == t.hbm_read_bytes + t.hbm_write_bytes
     for r in range(n):
         np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
+
+
+
+@pytest.mark.parametrize("mode,n,N", [("push", 8, (2 << 20) + 5), ("copyin", 8, (8 << 20) + 3),
+                                      ("copyin", 3, (24 << 20) + 1)])
+def test_pieces_on_two_streams_whole_buffers(mode, n, N):
+    # staged bytes over half of L2 and no timing records: the pieces run on two streams (twice as
+    # many, alternating between the caller's stream and the handle's); every element of every
+    # rank against the oracle, and the launches the rule gives
+    dtype = "bf16"
+    xs = workloads.rank_inputs(n, N, dtype, "normal", seed=29 + N % 11)
+    want = oracle.all_reduce(xs, dtype)
+    ins, outs = upload_ranks(xs), empty_ranks(n, N * 2)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    half = l2 // 2
+    staged = n * (n - 1) * N * 2 if mode == "push" else n * N * 2
+    assert staged * 2 >= l2
+    P = min(64, max(1, (staged + half // 2) // half))
+    PL = N if P == 1 else min(N, -(-(-(-N // P)) // 256) * 256)
+    PL = min(N, -(-(-(-PL // 2)) // 256) * 256)
+    opts = {"push_staging": 1} if mode == "push" else {"registered": 1}
+    with Handle(n, N * 2, **opts) as h:
+        call = ar.ar_one_shot_push if mode == "push" else ar.ar_one_shot_copyin
+        for _ in range(2):   # twice: the handle's second stream is reused
+            for o in outs:
+                o.fill(0x5A)
+            assert call(h, ptrs(ins), ptrs(outs), N, dtype) == ar.AR_OK
+            assert ar.ar_status(h) == ar.AR_OK
+            assert ar.ar_traffic(h).launches == 2 * -(-N // PL)
+            for r in range(n):
+                np.testing.assert_array_equal(outs[r].download(np.uint16), want[r])
