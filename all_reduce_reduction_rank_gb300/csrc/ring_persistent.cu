@@ -23,12 +23,22 @@
 //                      passed on;
 // and after the last step writes the last completed chunk it receives.
 //
-// Inbox of rank q: two slots (step parity) of `lps` lines.  Line l of a slot
-// holds elements 30 l .. 30 l + 29 of the chunk as fp32 words, and the flag
-// F(t) = 64 seq + t + 1 of the step t that wrote it.  seq is a call number
-// kept in device memory: every warp reads it at the start, and the call's
-// last warp to finish advances it, so each call -- also each replay of a
-// captured CUDA graph -- has its own, and no line of an earlier call matches.
+// Pieces: a CTA takes its slice in P pieces of sp elements (a multiple of 32
+// lines) and runs all 2(n-1) steps of the ring on one piece before the next,
+// so that what is in flight is one piece's messages.  P is the two inbox
+// slots of a whole step (all ranks' lines) over half of L2, rounded: large
+// calls then keep their messages in L2 instead of sending every line through
+// DRAM; small calls run in one piece (each piece pays the ring's hop latency
+// 2(n-1) times).  Message m = q (2n-2) + t is step t of piece q.
+//
+// Inbox of rank q: two slots (message parity) of `lps` lines.  Piece q of
+// CTA k uses lines [k sp/30, (k+1) sp/30) of a slot, the same lines for every
+// piece; line i of them holds elements 30 i .. 30 i + 29 of the piece's part
+// of the chunk as fp32 words, and the flag F(m) = 4096 seq + m + 1 of the
+// message m that wrote it.  seq is a call number kept in device memory: every
+// warp reads it at the start, and the call's last warp to finish advances it,
+// so each call -- also each replay of a captured CUDA graph -- has its own,
+// and no line of an earlier call or piece matches.
 //
 // Ordering follows the PTX memory model and does not assume that a 128-byte
 // line is stored atomically: a warp writes the data of 32 lines, then
@@ -37,10 +47,10 @@
 // reads the data.  A warp issues all loads of its 32 lines (and of the rank's
 // own elements) before it uses any, so a batch costs about one memory latency.
 //
-// Slot reuse: step t writes slot t % 2 of rank r+1, which step t-2 wrote
-// last.  Each receiving warp publishes ack = F(t') (release) once it has
-// consumed its batches of message t'; the sending warp waits for
-// ack >= F(t-2) before it writes.
+// Slot reuse: message m goes to slot m % 2 of rank r+1, which message m-2
+// used last.  Each receiving warp publishes ack = F(m') (release) once it has
+// consumed its batches of message m'; the sending warp waits for
+// ack >= F(m-2) before it writes.
 //
 // Every wait is bounded by spin_ns and a poll count.  A wait that runs out
 // records AR_ERR_FLAG_TIMEOUT (a line) or AR_ERR_WAIT_TIMEOUT (an ack) in the
@@ -164,8 +174,12 @@ __device__ bool wait_ack(const Persist& P, uint64_t seq, const uint64_t* ack, ui
     return false;
 }
 
-// Work of one warp: batches b = warp, warp + 8, ... of its CTA's slice, the
-// same batches on every rank, so warp w of CTA k of rank r exchanges lines and
+// Flags of a call: F(m) = kMsgBase seq + m + 1, with m < kMsgBase.
+constexpr uint64_t kMsgBase = 4096;
+static_assert(kMaxPieces * 30 < kMsgBase, "messages of a call must stay below kMsgBase");
+
+// Work of one warp, piece by piece: batches b = warp, warp + 8, ... of its
+// CTA's piece, the same batches on every rank, so warp w of CTA k of rank r exchanges lines and
 // acknowledgements only with warp w of CTA k of ranks r-1 and r+1: the step
 // loop has no block-wide barrier.  Per batch, software-pipelined: add and
 // store the batch (next rank's lines, outputs), acquire the next batch's
@@ -173,8 +187,8 @@ __device__ bool wait_ack(const Persist& P, uint64_t seq, const uint64_t* ack, ui
 // those loads are in flight.  A wait that gives up returns at once.
 template <int NR, int DT>
 __device__ __forceinline__ void persist_warp(const CPtrs<NR>& in, const MPtrs<NR>& out, const Persist& P, size_t C,
-                                             size_t count, size_t epc, uint64_t seq, int64_t spin_ns, int absent,
-                                             int prefetch, DevStatus* st)
+                                             size_t count, size_t epc, size_t sp, uint64_t seq, int64_t spin_ns,
+                                             int absent, int prefetch, DevStatus* st)
 {
     using T = typename Payload<DT>::scalar_t;
     constexpr int kI = kBatchLines / 4;   // lines per lane group per batch
@@ -185,138 +199,148 @@ __device__ __forceinline__ void persist_warp(const CPtrs<NR>& in, const MPtrs<NR
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 3, j = lane & 7;
     const int nw = j < 7 ? 4 : 2;
-    const size_t slice_lo = (size_t)k * epc;              // first element of the slice in a chunk
-    const size_t line_lo = slice_lo / kLineWords;         // its first line
+    const size_t slice_end = (size_t)k * epc + epc;       // end of the CTA's slice in a chunk
+    const int npieces = (int)((epc + sp - 1) / sp);
     uint64_t* const my_ack = P.acks + ((size_t)r * P.kcap + k) * kPWarps + warp;
     const uint64_t* const next_ack = P.acks + ((size_t)d * P.kcap + k) * kPWarps + warp;
-    auto inbox = [&](int q, int slot) { return P.inbox + ((size_t)q * 2 + slot) * P.lps * 8; };
+    auto inbox = [&](int rank, int slot) { return P.inbox + ((size_t)rank * 2 + slot) * P.lps * 8; };
 
-    // t in [0, 2n-2): send step t; t = 2n-2: only the last receive.
-    for (int t = 0; t <= 2 * NR - 2; ++t) {
-        const bool sends = t <= 2 * NR - 3;
-        // the chunk this step moves (received at t-1 and sent at t: the same)
-        const int c = t <= NR - 2 ? ((r - t) % NR + NR) % NR : ((r + NR - t) % NR + NR) % NR;
-        const size_t lo = (size_t)c * C;
-        const size_t len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
-        const size_t slice_hi = slice_lo + epc < len ? slice_lo + epc : len;
-        const size_t nlines = slice_hi > slice_lo ? (slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
-        const size_t nbatch = (nlines + kBatchLines - 1) / kBatchLines;
-        const T* const x = static_cast<const T*>(in.p[r]) + lo;
-        T* const y = static_cast<T*>(out.p[r]) + lo;
-        uint4* const rx = inbox(r, (t + 1) & 1);   // slot of message t-1
-        uint4* const tx = inbox(d, t & 1);         // slot of message t
-        const uint64_t f_in = 64 * seq + (uint64_t)t;        // F(t-1)
-        const uint64_t f_out = 64 * seq + (uint64_t)t + 1;   // F(t)
-        auto flag_ptr = [&](size_t bb) { return flag_of(rx, line_lo + bb * kBatchLines + lane); };
-        auto flag_live = [&](size_t bb) { return (line_lo + bb * kBatchLines + lane) * kLineWords < slice_hi; };
+    for (int q = 0; q < npieces; ++q) {
+        const size_t slice_lo = (size_t)k * epc + (size_t)q * sp;   // first element of the piece in a chunk
+        const size_t piece_end = slice_lo + sp < slice_end ? slice_lo + sp : slice_end;
+        const size_t line_lo = slice_lo / kLineWords;               // its first line
+        // inbox lines are indexed by the chunk's line numbers l, shifted so that
+        // this piece's lines land on the CTA's lines [k sp/30, (k+1) sp/30)
+        const ptrdiff_t shift = 8 * ((ptrdiff_t)((size_t)k * (sp / kLineWords)) - (ptrdiff_t)line_lo);
+        // t in [0, 2n-2): send step t; t = 2n-2: only the last receive.
+        for (int t = 0; t <= 2 * NR - 2; ++t) {
+            const bool sends = t <= 2 * NR - 3;
+            const uint64_t m = (uint64_t)q * (2 * NR - 2) + (uint64_t)t;   // the message this iteration sends
+            // the chunk this step moves (received at t-1 and sent at t: the same)
+            const int c = t <= NR - 2 ? ((r - t) % NR + NR) % NR : ((r + NR - t) % NR + NR) % NR;
+            const size_t lo = (size_t)c * C;
+            const size_t len = lo >= count ? 0 : (count - lo < C ? count - lo : C);
+            const size_t slice_hi = piece_end < len ? piece_end : len;
+            const size_t nlines = slice_hi > slice_lo ? (slice_hi - slice_lo + kLineWords - 1) / kLineWords : 0;
+            const size_t nbatch = (nlines + kBatchLines - 1) / kBatchLines;
+            const T* const x = static_cast<const T*>(in.p[r]) + lo;
+            T* const y = static_cast<T*>(out.p[r]) + lo;
+            uint4* const rx = inbox(r, (t + 1) & 1) + shift;   // slot of message m-1 (2n-2 is even)
+            uint4* const tx = inbox(d, t & 1) + shift;         // slot of message m
+            const uint64_t f_in = kMsgBase * seq + m;        // F(m-1)
+            const uint64_t f_out = kMsgBase * seq + m + 1;   // F(m)
+            auto flag_ptr = [&](size_t bb) { return flag_of(rx, line_lo + bb * kBatchLines + lane); };
+            auto flag_live = [&](size_t bb) { return (line_lo + bb * kBatchLines + lane) * kLineWords < slice_hi; };
 
-        // the rank's own elements of this step, pulled into L2 while the
-        // warp waits for the lines (small calls, whose steps are latency-bound)
-        if (prefetch && t >= 1 && t <= NR - 1) {
-            for (size_t bb = warp; bb < nbatch; bb += kPWarps) {
-                const size_t e0 = (line_lo + bb * kBatchLines) * kLineWords + (size_t)lane * (128 / sizeof(T));
-                if (e0 < slice_hi) prefetch_l2(x + e0);
+            // the rank's own elements of this step, pulled into L2 while the
+            // warp waits for the lines (small calls, whose steps are latency-bound)
+            if (prefetch && t >= 1 && t <= NR - 1) {
+                for (size_t bb = warp; bb < nbatch; bb += kPWarps) {
+                    const size_t e0 = (line_lo + bb * kBatchLines) * kLineWords + (size_t)lane * (128 / sizeof(T));
+                    if (e0 < slice_hi) prefetch_l2(x + e0);
+                }
             }
-        }
-        // step prologue: the receiver's acknowledgement of step t-2 (slot
-        // reuse) and the first batch's flags, polled together, one acquire
-        size_t b = warp;
-        {
-            const bool need_ack = sends && t >= 2, need_fl = t >= 1 && b < nbatch;
-            const uint64_t want_ack = 64 * seq + (uint64_t)(t - 2) + 1;
-            bool ok_ack = !need_ack || ld_relaxed(next_ack) >= want_ack;
-            bool ok_fl = !need_fl || !flag_live(b) || ld_relaxed(flag_ptr(b)) == f_in;
-            if (!__all_sync(kFull, ok_ack && ok_fl)) {
-                if (!__all_sync(kFull, ok_ack) && !wait_ack(P, seq, next_ack, want_ack, spin_ns, st)) return;
-                if (need_fl && !wait_lines(P, seq, flag_ptr(b), flag_live(b), f_in, spin_ns, st, r,
-                                           line_lo + b * kBatchLines + lane))
-                    return;
+            // step prologue: the receiver's acknowledgement of message m-2 (slot
+            // reuse) and the first batch's flags, polled together, one acquire
+            size_t b = warp;
+            {
+                const bool need_ack = sends && m >= 2, need_fl = t >= 1 && b < nbatch;
+                const uint64_t want_ack = kMsgBase * seq + m - 1;   // F(m-2)
+                bool ok_ack = !need_ack || ld_relaxed(next_ack) >= want_ack;
+                bool ok_fl = !need_fl || !flag_live(b) || ld_relaxed(flag_ptr(b)) == f_in;
+                if (!__all_sync(kFull, ok_ack && ok_fl)) {
+                    if (!__all_sync(kFull, ok_ack) && !wait_ack(P, seq, next_ack, want_ack, spin_ns, st)) return;
+                    if (need_fl && !wait_lines(P, seq, flag_ptr(b), flag_live(b), f_in, spin_ns, st, r,
+                                               line_lo + b * kBatchLines + lane))
+                        return;
+                }
+                fence_gpu();
+                __syncwarp();
             }
-            fence_gpu();
-            __syncwarp();
-        }
-        // a batch's loads: 8 lines and the rank's own elements, all issued
-        // before any is used
-        uint4 w[kI];
-        uint32_t xr[kI][kRawWords<DT>];
-        auto load_batch = [&](size_t bb) {
-            const size_t base = line_lo + bb * kBatchLines;
-#pragma unroll
-            for (int i = 0; i < kI; ++i) {
-                const size_t l = base + 4 * i + g;
-                w[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (t >= 1 && l * kLineWords < slice_hi) w[i] = ld16_cg(rx + 8 * l + j);
-            }
-            if (t <= NR - 1) {
+            // a batch's loads: 8 lines and the rank's own elements, all issued
+            // before any is used
+            uint4 w[kI];
+            uint32_t xr[kI][kRawWords<DT>];
+            auto load_batch = [&](size_t bb) {
+                const size_t base = line_lo + bb * kBatchLines;
 #pragma unroll
                 for (int i = 0; i < kI; ++i) {
                     const size_t l = base + 4 * i + g;
-                    load_raw<DT>(x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < slice_hi ? len : 0, xr[i]);
+                    w[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (t >= 1 && l * kLineWords < slice_hi) w[i] = ld16_cg(rx + 8 * l + j);
                 }
-            }
-        };
-        if (b < nbatch) load_batch(b);
-        while (b < nbatch) {
-            const size_t base = line_lo + b * kBatchLines;   // first line of the batch
+                if (t <= NR - 1) {
 #pragma unroll
-            for (int i = 0; i < kI; ++i) {
-                const size_t l = base + 4 * i + g;
-                const size_t e = l * kLineWords + 4 * (size_t)j;
-                if (l * kLineWords >= slice_hi) continue;
-                float v[4] = {__uint_as_float(w[i].x), __uint_as_float(w[i].y), __uint_as_float(w[i].z),
-                              __uint_as_float(w[i].w)};
-                if (t <= NR - 1) {   // reduce-scatter: add this rank's own chunk
-                    float xv[4];
-                    widen_raw<DT>(xr[i], xv);
-                    if (t == 0) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) v[u] = xv[u];
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) v[u] = v[u] + xv[u];
+                    for (int i = 0; i < kI; ++i) {
+                        const size_t l = base + 4 * i + g;
+                        load_raw<DT>(x, l * kLineWords + 4 * (size_t)j, nw, l * kLineWords < slice_hi ? len : 0, xr[i]);
                     }
                 }
-                if (t >= NR - 1) {   // a completed chunk: this rank's output
-                    if (t == NR - 1) {   // rounded once; the rounded value is passed on
+            };
+            if (b < nbatch) load_batch(b);
+            while (b < nbatch) {
+                const size_t base = line_lo + b * kBatchLines;   // first line of the batch
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) v[u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[u]));
+                for (int i = 0; i < kI; ++i) {
+                    const size_t l = base + 4 * i + g;
+                    const size_t e = l * kLineWords + 4 * (size_t)j;
+                    if (l * kLineWords >= slice_hi) continue;
+                    float v[4] = {__uint_as_float(w[i].x), __uint_as_float(w[i].y), __uint_as_float(w[i].z),
+                                  __uint_as_float(w[i].w)};
+                    if (t <= NR - 1) {   // reduce-scatter: add this rank's own chunk
+                        float xv[4];
+                        widen_raw<DT>(xr[i], xv);
+                        if (t == 0) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) v[u] = xv[u];
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) v[u] = v[u] + xv[u];
+                        }
                     }
-                    store_elems<DT>(y, e, nw, len, v);
+                    if (t >= NR - 1) {   // a completed chunk: this rank's output
+                        if (t == NR - 1) {   // rounded once; the rounded value is passed on
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) v[u] = Payload<DT>::widen1(Payload<DT>::narrow1(v[u]));
+                        }
+                        store_elems<DT>(y, e, nw, len, v);
+                    }
+                    if (sends) {
+                        if (j < 7)
+                            st16_plain(tx + 8 * l + j, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                                                  __float_as_uint(v[2]), __float_as_uint(v[3])));
+                        else
+                            st8_plain(tx + 8 * l + j, __float_as_uint(v[0]), __float_as_uint(v[1]));
+                    }
                 }
+                // the next batch: acquire its flags and issue its loads before
+                // this batch's release, so that they are in flight while this
+                // batch's stores drain
+                const size_t nb = b + kPWarps;
+                if (t >= 1 && nb < nbatch) {
+                    const bool ok = __all_sync(kFull, !flag_live(nb) || ld_acquire(flag_ptr(nb)) == f_in);
+                    if (!ok && !wait_lines(P, seq, flag_ptr(nb), flag_live(nb), f_in, spin_ns, st, r,
+                                           line_lo + nb * kBatchLines + lane))
+                        return;
+                    __syncwarp();
+                }
+                if (nb < nbatch) load_batch(nb);
                 if (sends) {
-                    if (j < 7)
-                        st16_plain(tx + 8 * l + j, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                                                              __float_as_uint(v[2]), __float_as_uint(v[3])));
-                    else
-                        st8_plain(tx + 8 * l + j, __float_as_uint(v[0]), __float_as_uint(v[1]));
+                    __syncwarp();
+                    fence_gpu();
+                    const size_t fl = base + lane;
+                    if (fl * kLineWords < slice_hi) st_relaxed(flag_of(tx, fl), f_out);
                 }
+                b = nb;
             }
-            // the next batch: acquire its flags and issue its loads before
-            // this batch's release, so that they are in flight while this
-            // batch's stores drain
-            const size_t nb = b + kPWarps;
-            if (t >= 1 && nb < nbatch) {
-                const bool ok = __all_sync(kFull, !flag_live(nb) || ld_acquire(flag_ptr(nb)) == f_in);
-                if (!ok && !wait_lines(P, seq, flag_ptr(nb), flag_live(nb), f_in, spin_ns, st, r,
-                                       line_lo + nb * kBatchLines + lane))
-                    return;
-                __syncwarp();
+            // message m-1 of this warp's batches is consumed (its last batch's
+            // values were used before the last fence; a step that sends nothing
+            // or had no batch fences here): acknowledge it for the sender's slot
+            // reuse.  The last message of the call needs none.
+            if (t >= 1 && (sends || q + 1 < npieces) && lane == 0) {
+                if (!sends || nbatch <= (size_t)warp) fence_gpu();
+                st_relaxed(my_ack, f_in);
             }
-            if (nb < nbatch) load_batch(nb);
-            if (sends) {
-                __syncwarp();
-                fence_gpu();
-                const size_t fl = base + lane;
-                if (fl * kLineWords < slice_hi) st_relaxed(flag_of(tx, fl), f_out);
-            }
-            b = nb;
-        }
-        // message t-1 of this warp's batches is consumed (its last batch's
-        // values were used before the last fence): acknowledge it for the
-        // sender's slot reuse
-        if (t >= 1 && sends && lane == 0) {
-            if (nbatch <= (size_t)warp) fence_gpu();
-            st_relaxed(my_ack, f_in);
         }
     }
 }
@@ -324,12 +348,12 @@ __device__ __forceinline__ void persist_warp(const CPtrs<NR>& in, const MPtrs<NR
 template <int NR, int DT>
 __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM: 128 registers, no spills
 ring_persistent_kernel(const __grid_constant__ CPtrs<NR> in, const __grid_constant__ MPtrs<NR> out,
-                       const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, int64_t spin_ns,
-                       int absent, int prefetch, DevStatus* st)
+                       const __grid_constant__ Persist P, size_t C, size_t count, size_t epc, size_t sp,
+                       int64_t spin_ns, int absent, int prefetch, DevStatus* st)
 {
     // the same for every warp: only this call's last warp advances it
     const uint64_t seq = ld_relaxed(P.epoch_w) + 1;
-    persist_warp<NR, DT>(in, out, P, C, count, epc, seq, spin_ns, absent, prefetch, st);
+    persist_warp<NR, DT>(in, out, P, C, count, epc, sp, seq, spin_ns, absent, prefetch, st);
     if ((threadIdx.x & 31) == 0) {
         fence_gpu();
         const unsigned total = gridDim.x * gridDim.y * (unsigned)kPWarps;
@@ -378,6 +402,22 @@ uint64_t persist_lines_per_step(int n, size_t count, int dt)
     return lines;
 }
 
+// Elements of a CTA's slice per piece: P = the two inbox slots of a step
+// (2 x 128 B x L lines) over half of L2, rounded, at most kMaxPieces; sp a
+// multiple of 32 lines.  Measured on GB300 (n = 8 bf16, one launch, µs;
+// pieces 1 / 2 / 4 / 8): 8 MiB per rank 129 / 173 / 275 / 491, 32 MiB 555 /
+// 441 / 469 / 659, 64 MiB 1111 / 1079 / 861 / 968; the rule gives 1, 2, 4.
+static size_t persist_piece_elems(const Handle& h, uint64_t L, size_t epc)
+{
+    const uint64_t half = (uint64_t)h.l2_bytes / 2, live = 2ull * 128ull * L;
+    uint64_t P = half ? (live + half / 2) / half : 1;
+    if (P < 1) P = 1;
+    if (P > kMaxPieces) P = kMaxPieces;
+    size_t sp = (epc + P - 1) / P;
+    sp = (sp + kBatchElems - 1) / kBatchElems * kBatchElems;
+    return sp < epc ? sp : epc;
+}
+
 int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, size_t count, int dt,
                            cudaStream_t s, int* launches)
 {
@@ -408,6 +448,8 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             K = (C + epc - 1) / epc;
             if (K < 1) K = 1;
             const size_t lps = persist_lps(h.n, h.max_bytes, h.sm_count);
+            const uint64_t L = persist_lines_per_step(NR, count, DT);
+            const size_t sp = persist_piece_elems(h, L, epc);
             if (K * epc / kLineWords > lps || (int)K > persist_kcap(h.n, h.sm_count)) return AR_ERR_CUDA;
             Persist P;
             P.inbox = reinterpret_cast<uint4*>(h.persist);
@@ -429,11 +471,10 @@ int launch_ring_persistent(Handle& h, const void* const* in, void* const* out, s
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             const uint64_t e = sizeof(typename Payload<DT>::scalar_t);
-            const uint64_t L = persist_lines_per_step(NR, count, DT);
             const uint64_t bytes = 2ull * ((uint64_t)NR * e * count + (uint64_t)(2 * NR - 2) * 128ull * L);
             rec_begin(h, s);
             const cudaError_t err = cudaLaunchKernelEx(&cfg, ring_persistent_kernel<NR, DT>, ip, op, P, C, count,
-                                                       epc, h.spin_ns, h.persist_absent,
+                                                       epc, sp, h.spin_ns, h.persist_absent,
                                                        (int)(count * e <= kPersistPrefetchBytes), h.status);
             rec_end(h, s, AR_K_RING_PERSISTENT, bytes);
             *launches = 1;

@@ -368,7 +368,11 @@ int ar_ring_rounded_fused(ar_handle h, const void* const* in, void* const* out, 
  * (handbook "集合通信：NCCL 的算法、协议…", §协议; "多 GPU 与 NCCL", §ring
  * all-reduce).  A rank's CTAs poll the flags of the lines the previous rank
  * sends instead of waiting for a kernel boundary, and acknowledge each
- * consumed step so that its two inbox slots can be reused.  Same bits as
+ * consumed step so that its two inbox slots can be reused.  When the two
+ * slots of a step (all ranks' lines) exceed half of L2, each CTA takes its
+ * share of every chunk in pieces (that ratio, rounded, at most 64), each
+ * piece through all 2(n-1) steps, so that the lines in flight stay in L2;
+ * still one launch.  Same bits as
  * ar_ring.  Needs AR_OPT_PERSISTENT (AR_ERR_INVALID otherwise).  Every wait
  * is bounded by AR_OPT_SPIN_NS: a wait that runs out ends the call early,
  * leaves the outputs incomplete and sets the status (ar_status) to

@@ -96,6 +96,71 @@ def test_persistent_ring_equals_ar_ring_at_a_large_size():
         assert torch.equal(a[r].body(), p[r].body())
 
 
+def _persist_pieces(n, N, dtype):
+    """Pieces of a persistent ring call: the two inbox slots of a step (128-byte lines of 30
+    words, all ranks' chunks) over half of this device's L2, rounded, at most 64."""
+    half = torch.cuda.get_device_properties(0).L2_cache_size // 2
+    C = oracle.chunk_elems(n, N, dtype)
+    lines = sum(-(-max(0, min(C, N - c * C)) // 30) for c in range(n))
+    return min(64, max(1, (2 * 128 * lines + half // 2) // half))
+
+
+@pytest.mark.parametrize("n,N,dtype", [(8, 16 * 1024 * 1024 + 5, "bf16"), (8, 32 * 1024 * 1024 + 3, "bf16"),
+                                       (4, 12_000_007, "f32"), (16, 24_000_001, "f16")])
+def test_persistent_ring_in_pieces_equals_ar_ring(n, N, dtype):
+    # calls whose inbox traffic exceeds L2 run their CTAs' slices in pieces (every piece through
+    # all 2(n-1) steps, the flags numbering the messages across pieces): every element of every
+    # rank equal to ar_ring's, on two calls of one handle
+    assert _persist_pieces(n, N, dtype) >= 2
+    e = E[dtype]
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(9) + n)
+    a = [torch.empty_like(t) for t in ins]
+    p = [torch.full_like(t, 0) for t in ins]
+    with Handle(n, N * e, persistent=1) as h:
+        ptr = lambda ts: [t.data_ptr() for t in ts]
+        assert ar.ar_ring(h, ptr(ins), ptr(a), N, dtype) == ar.AR_OK
+        for k in range(2):
+            assert ar.ar_ring_persistent(h, ptr(ins), ptr(p), N, dtype) == ar.AR_OK
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK
+            for r in range(n):
+                assert torch.equal(a[r].view(torch.int16 if e == 2 else torch.int32),
+                                   p[r].view(torch.int16 if e == 2 else torch.int32)), (k, r)
+            for t in p:
+                t.zero_()
+
+
+def test_persistent_ring_in_pieces_in_a_cuda_graph_against_the_oracle():
+    # captured once and replayed on new inputs: every replay has its own call number, so no line
+    # of an earlier replay or piece is taken; every element against the oracle's ring
+    n, N, dtype = 8, 12 * 1024 * 1024 + 77, "bf16"
+    assert _persist_pieces(n, N, dtype) >= 2
+    ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(9) + 100)
+    outs = [torch.empty_like(t) for t in ins]
+    with Handle(n, N * 2, persistent=1) as h:
+        s = torch.cuda.Stream()
+        assert ar.ar_ring_persistent(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs],
+                                     N, dtype) == ar.AR_OK
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rc = ar.ar_ring_persistent(h, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], N, dtype, s)
+        assert rc == ar.AR_OK
+        for k in range(2):
+            src = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(9) + 101 + k)
+            for t, x in zip(ins, src):
+                t.copy_(x)
+            for o in outs:
+                o.fill_(0x5A5A)
+            g.replay()
+            torch.cuda.synchronize()
+            assert ar.ar_status(h) == ar.AR_OK
+            want = oracle.ring([t.cpu().numpy().view(np.uint16) for t in ins], dtype)[0]
+            for r in range(n):
+                bad = np.flatnonzero(outs[r].cpu().numpy().view(np.uint16) != want)
+                assert bad.size == 0, (k, r, bad[:5])
+
+
 def test_persistent_ring_needs_its_buffers_and_rejects_bad_options():
     with Handle(4, 4096) as h:
         ins, outs = empty_ranks(4, 4096), empty_ranks(4, 4096)
