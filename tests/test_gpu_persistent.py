@@ -105,29 +105,35 @@ def _persist_pieces(n, N, dtype):
     return min(64, max(1, (2 * 128 * lines + half // 2) // half))
 
 
-@pytest.mark.parametrize("n,N,dtype", [(8, 16 * 1024 * 1024 + 5, "bf16"), (8, 32 * 1024 * 1024 + 3, "bf16"),
-                                       (4, 12_000_007, "f32"), (16, 24_000_001, "f16")])
-def test_persistent_ring_in_pieces_equals_ar_ring(n, N, dtype):
+@pytest.mark.parametrize("n,N,dtype,ctas_per_sm,in_place", [
+    (8, 16 * 1024 * 1024 + 5, "bf16", 0, False), (8, 32 * 1024 * 1024 + 3, "bf16", 0, False),
+    (4, 12_000_007, "f32", 0, False), (16, 24_000_001, "f16", 0, False),
+    (8, 16 * 1024 * 1024 + 5, "bf16", 1, False), (8, 16 * 1024 * 1024 + 5, "bf16", 0, True)])
+def test_persistent_ring_in_pieces_equals_ar_ring(n, N, dtype, ctas_per_sm, in_place):
     # calls whose inbox traffic exceeds L2 run their CTAs' slices in pieces (every piece through
     # all 2(n-1) steps, the flags numbering the messages across pieces): every element of every
-    # rank equal to ar_ring's, on two calls of one handle
+    # rank equal to ar_ring's, on two calls of one handle; one CTA per SM gives every warp many
+    # batches per piece (the slot acknowledgements are waited on), and in place each piece's
+    # outputs overwrite inputs that only that piece reads
     assert _persist_pieces(n, N, dtype) >= 2
     e = E[dtype]
+    iv = torch.int16 if e == 2 else torch.int32
     ins = workloads.rank_inputs_device(n, N, dtype, "normal_over_n", workloads.seed_of(9) + n)
+    keep = [t.clone() for t in ins]
     a = [torch.empty_like(t) for t in ins]
-    p = [torch.full_like(t, 0) for t in ins]
-    with Handle(n, N * e, persistent=1) as h:
+    opts = {"persistent": 1, **({"ctas_per_sm": ctas_per_sm} if ctas_per_sm else {})}
+    with Handle(n, N * e, **opts) as h:
         ptr = lambda ts: [t.data_ptr() for t in ts]
         assert ar.ar_ring(h, ptr(ins), ptr(a), N, dtype) == ar.AR_OK
         for k in range(2):
+            for t, x in zip(ins, keep):
+                t.copy_(x)
+            p = ins if in_place else [torch.zeros_like(t) for t in ins]
             assert ar.ar_ring_persistent(h, ptr(ins), ptr(p), N, dtype) == ar.AR_OK
             torch.cuda.synchronize()
             assert ar.ar_status(h) == ar.AR_OK
             for r in range(n):
-                assert torch.equal(a[r].view(torch.int16 if e == 2 else torch.int32),
-                                   p[r].view(torch.int16 if e == 2 else torch.int32)), (k, r)
-            for t in p:
-                t.zero_()
+                assert torch.equal(a[r].view(iv), p[r].view(iv)), (k, r)
 
 
 def test_persistent_ring_in_pieces_in_a_cuda_graph_against_the_oracle():
