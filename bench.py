@@ -22,7 +22,7 @@ roofline of the dominant kernel (algorithmic and DRAM rates), the oracle
 timed on the host (cpu_baseline), the end-to-end leg through host buffers
 (e2e) and the SM clocks seen during the timed region.  Everything else it
 measures goes to a details file (--details; by default bench_details.json
-in the run's output directory): a decode/prefill sweep of one-shot and
+beside this file; relative paths are taken from here): a decode/prefill sweep of one-shot and
 two-shot, the fused all-reduce + RMSNorm epilogue, every all-reduce call
 side by side (variants), the LL payload sweep, the n = 16 doubling sweep,
 the per-kernel table and the other CPU legs (cpu_parallel, cpu_calls).
@@ -1230,7 +1230,7 @@ def main(argv=None):
                         "barrier, 3 one launch with per-tile flags between CTAs)")
     p.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--details", default=os.path.join("gpurun_out", "bench_details.json"),
+    p.add_argument("--details", default="bench_details.json",
                    help="JSON file for everything beyond the headline line (sweeps, variants, per-kernel "
                         "table, CPU legs); '' for none")
     p.add_argument("--reference-budget", type=float, default=150.0,
